@@ -1,0 +1,148 @@
+/*
+ * zl_decode_attn — paged decode attention for GB300 (sm_103a), C ABI.
+ *
+ * The operation. Each running sequence adds one new query token and attends
+ * to its whole paged K/V cache in one fused, batched launch: the decode-phase
+ * "fused batch attention" on tensor cores that "ZhiLight：知乎开源的高性能 LLM
+ * 推理加速引擎" describes in section "4. Tensor Core 上的 Flash Attention", and
+ * that "ZhiLight: Zhihu's CUDA Inference Engine for Llama and DeepSeek on PCIe
+ * GPUs" lists in "Dual streams, host all-reduce and the memory model" (fused
+ * batch attention for decoding using tensor core instructions; prefix cache;
+ * DeepseekV2 MLA). For sequence b, query head h, kv head kh = h / (Hq/Hkv):
+ *
+ *   out[b,h,:] = sum_{t < seq_lens[b]} softmax_t(scale * q[b,h,:] . K_b[t,kh,:]) V_b[t,kh,:]
+ *   lse[b,h]   = ln sum_t exp(scale * q[b,h,:] . K_b[t,kh,:])
+ *
+ * where row t of K_b is slot (t mod page_size) of physical page
+ * block_table[b, t / page_size] (likewise V). Grouped-query heads sharing a
+ * kv head are evaluated together so each K/V byte is read once per group (the
+ * DataFun talk write-up, section "1. 大模型负载分析", names the head-sharing
+ * attention variants). Long or ragged contexts are split across CTAs and the
+ * partial results merged by log-sum-exp (the split-KV "flash_decoding" idea
+ * named under "技术架构：五层模块化设计").
+ *
+ * Conventions for every entry point:
+ *   - Ownership: the caller owns every buffer. The library never allocates or
+ *     frees device memory and never synchronises; it enqueues kernels on the
+ *     given stream only. Its only state is host-side (per-device attributes).
+ *   - Host errors return synchronously and launch nothing.
+ *   - Device data errors (a page id outside [0, num_pages), a seq_len outside
+ *     [0, block_table_stride * page_size], a pipeline wait that timed out)
+ *     cannot be returned without a sync: the kernel ORs a ZL_DEVERR_* bit into
+ *     *err_flags (when err_flags is not NULL) and writes zeros (lse = -inf)
+ *     for the affected sequence. Nothing traps.
+ *   - seq_lens[b] = 0 gives out = 0 and lse = -inf; that is not an error.
+ *   - Results depend only on logical content: remapping pages gives
+ *     bit-identical output, and repeated calls are bit-identical.
+ */
+#ifndef ZL_DECODE_ATTN_H
+#define ZL_DECODE_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / cudaEvent_t. NULL stream = the legacy default. */
+typedef struct CUstream_st* zl_stream_t;
+typedef struct CUevent_st* zl_event_t;
+
+typedef enum {
+  ZL_OK = 0,
+  ZL_ERR_INVALID_ARG = 1, /* NULL or misaligned pointer, bad size or stride */
+  ZL_ERR_UNSUPPORTED = 2, /* a valid shape this build does not implement */
+  ZL_ERR_WORKSPACE = 3,   /* workspace NULL or smaller than required */
+  ZL_ERR_CUDA = 4         /* a CUDA runtime call or launch failed */
+} zl_status;
+
+/* Bits the kernels OR into *err_flags. */
+#define ZL_DEVERR_BAD_PAGE 1u    /* block_table entry outside [0, num_pages) */
+#define ZL_DEVERR_BAD_SEQ_LEN 2u /* seq_len < 0 or > block_table_stride * page_size */
+#define ZL_DEVERR_TIMEOUT 4u     /* a pipeline wait gave up after ~2 s */
+
+typedef struct {
+  size_t struct_size; /* sizeof(zl_decode_attn_params), for ABI checks */
+
+  /* Query, bf16 [B, q_len, Hq, D_qk], contiguous, 16-byte aligned. */
+  const void* q;
+  /* K and V pools, bf16. Row (page, slot, head) of D_qk elements starts at
+     page*page_stride + slot*token_stride + head*head_stride (elements); the
+     row itself is contiguous. Strides are multiples of 8 elements, the base
+     16-byte aligned. [num_pages, page_size, Hkv, D] ("NHD") and
+     [num_pages, Hkv, page_size, D] ("HND") are both expressible.
+     MLA: v_pool must be NULL; V is the first D_v columns of the K row. */
+  const void* k_pool;
+  const void* v_pool;
+  int64_t page_stride, token_stride, head_stride;
+
+  /* int32 [B, block_table_stride]: physical page of each logical page. */
+  const int32_t* block_table;
+  int64_t block_table_stride;
+  /* int32 [B], device: tokens in the cache, the new token included. */
+  const int32_t* seq_lens;
+
+  /* Output, bf16 [B, q_len, Hq, D_v], contiguous, 16-byte aligned. */
+  void* out;
+  /* Optional fp32 [B, q_len, Hq], natural-log log-sum-exp of the scaled
+     scores; NULL to skip. */
+  float* lse;
+
+  int32_t B, q_len, Hq, Hkv, D_qk, D_v, page_size, num_pages;
+  /* Host-side upper bound of seq_lens (0 = unknown); used only to size the
+     grid for small problems. Results do not depend on it. */
+  int32_t max_seq_len;
+  float scale; /* softmax scale, e.g. 1/sqrt(D) */
+
+  /* Caller-owned device scratch of at least zl_decode_attn_workspace_size()
+     bytes, 256-byte aligned. Contents need no initialisation. */
+  void* workspace;
+  size_t workspace_bytes;
+
+  /* Optional device word; kernels atomically OR ZL_DEVERR_* bits into it. */
+  uint32_t* err_flags;
+
+  /* Number of CTAs of the attention kernel; 0 = one wave on this device.
+     Any value >= 1 gives the same result within fp32 rounding: the work is
+     split into that many equal token ranges and merged. */
+  int32_t num_ctas;
+
+  /* Optional profiling events recorded on the stream immediately before and
+     after the attention kernel (not the merge); NULL to skip. */
+  zl_event_t attn_begin, attn_end;
+} zl_decode_attn_params;
+
+/*
+ * GQA / MHA / MQA decode over separate K and V pools.
+ *   Supported: D_qk = D_v = 128; 1 <= Hq/Hkv <= 16; Hq % Hkv == 0;
+ *   page_size a multiple of 16 (<= 1024); q_len = 1; 1 <= B <= 4096.
+ *   Anything else returns ZL_ERR_UNSUPPORTED (or ZL_ERR_INVALID_ARG when the
+ *   value is not meaningful at all, e.g. Hkv = 0).
+ */
+zl_status zl_decode_attn(const zl_decode_attn_params* params, zl_stream_t stream);
+
+/*
+ * Absorbed multi-head latent attention (MLA) decode: one shared latent row per
+ * token of width D_qk = 576 (512 latent + 64 rope); V is its first D_v = 512
+ * columns. Hkv = 1, v_pool = NULL, Hq a multiple of 64 (<= 128),
+ * page_size a multiple of 64, q_len = 1. The "ZhiLight：知乎开源的高性能 LLM
+ * 推理加速引擎" page lists MLA support under "功能生态" and flash_mla under
+ * "技术架构：五层模块化设计".
+ */
+zl_status zl_decode_attn_mla(const zl_decode_attn_params* params, zl_stream_t stream);
+
+/* Workspace bytes zl_decode_attn (resp. zl_decode_attn_mla) needs for these
+   params. Only the shape fields and num_ctas are read; pointers may be NULL.
+   Needs a current CUDA device (the default grid depends on its SM count). */
+zl_status zl_decode_attn_workspace_size(const zl_decode_attn_params* params, size_t* bytes);
+zl_status zl_decode_attn_mla_workspace_size(const zl_decode_attn_params* params, size_t* bytes);
+
+/* Static description of a status code. */
+const char* zl_status_string(zl_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZL_DECODE_ATTN_H */

@@ -1,0 +1,247 @@
+"""Paged decode attention for GB300: Python binding of libzl_decode_attn.so.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of the library (declared in include/zl_decode_attn.h). There is no CPU
+or PyTorch fallback; if the library is missing or fails to load, every call
+raises.
+
+    import paged_decode_attention_gqa_gb300 as zl
+    out = zl.decode_attn(q, k_pool, v_pool, block_table, seq_lens,
+                         page_size=16, scale=128 ** -0.5)
+
+Tensors are torch CUDA tensors (PyTorch provides device memory and streams).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+from ._build import LIB_PATH, build  # noqa: F401  (build() is the public build step)
+
+__all__ = [
+    "ZlError", "Params", "lib", "decode_attn", "decode_attn_mla", "workspace_size",
+    "workspace_size_mla", "call", "build", "LIB_PATH", "DEVERR_BAD_PAGE", "DEVERR_BAD_SEQ_LEN",
+    "DEVERR_TIMEOUT", "HEADER", "declared_symbols",
+]
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "zl_decode_attn.h")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA = range(5)
+DEVERR_BAD_PAGE, DEVERR_BAD_SEQ_LEN, DEVERR_TIMEOUT = 1, 2, 4
+
+
+class ZlError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{msg} (zl_status {status})")
+        self.status = status
+
+
+class Params(ctypes.Structure):
+    """Mirror of zl_decode_attn_params."""
+    _fields_ = [
+        ("struct_size", ctypes.c_size_t),
+        ("q", ctypes.c_void_p),
+        ("k_pool", ctypes.c_void_p),
+        ("v_pool", ctypes.c_void_p),
+        ("page_stride", ctypes.c_int64),
+        ("token_stride", ctypes.c_int64),
+        ("head_stride", ctypes.c_int64),
+        ("block_table", ctypes.c_void_p),
+        ("block_table_stride", ctypes.c_int64),
+        ("seq_lens", ctypes.c_void_p),
+        ("out", ctypes.c_void_p),
+        ("lse", ctypes.c_void_p),
+        ("B", ctypes.c_int32),
+        ("q_len", ctypes.c_int32),
+        ("Hq", ctypes.c_int32),
+        ("Hkv", ctypes.c_int32),
+        ("D_qk", ctypes.c_int32),
+        ("D_v", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("num_pages", ctypes.c_int32),
+        ("max_seq_len", ctypes.c_int32),
+        ("scale", ctypes.c_float),
+        ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
+        ("err_flags", ctypes.c_void_p),
+        ("num_ctas", ctypes.c_int32),
+        ("attn_begin", ctypes.c_void_p),
+        ("attn_end", ctypes.c_void_p),
+    ]
+
+
+_lib = None
+_lib_lock = threading.Lock()
+
+
+def lib():
+    """The loaded library (built first if missing or stale). Raises on failure."""
+    global _lib
+    with _lib_lock:
+        if _lib is None:
+            try:
+                path = build()
+                handle = ctypes.CDLL(path)
+            except Exception as e:  # no fallback: the CUDA path is the product
+                raise RuntimeError(f"libzl_decode_attn could not be built or loaded: {e}") from e
+            P = ctypes.POINTER(Params)
+            for name in ("zl_decode_attn", "zl_decode_attn_mla"):
+                fn = getattr(handle, name)
+                fn.restype = ctypes.c_int
+                fn.argtypes = [P, ctypes.c_void_p]
+            for name in ("zl_decode_attn_workspace_size", "zl_decode_attn_mla_workspace_size"):
+                fn = getattr(handle, name)
+                fn.restype = ctypes.c_int
+                fn.argtypes = [P, ctypes.POINTER(ctypes.c_size_t)]
+            handle.zl_status_string.restype = ctypes.c_char_p
+            handle.zl_status_string.argtypes = [ctypes.c_int]
+            _lib = handle
+        return _lib
+
+
+def declared_symbols(header: str = HEADER):
+    """Function names the public header declares."""
+    text = open(header).read()
+    return sorted(set(re.findall(r"^\s*(?:zl_status|const char\*)\s+(zl_\w+)\s*\(", text, re.M)))
+
+
+def _check(status: int, what: str):
+    if status != OK:
+        raise ZlError(status, f"{what}: {lib().zl_status_string(status).decode()}")
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _pool_strides(pool: torch.Tensor, layout: str):
+    """(page, token, head) element strides of a 4-D pool in NHD or HND layout."""
+    if pool.dim() != 4:
+        raise ValueError("pools are 4-D: [pages, slot, head, dim] (NHD) or [pages, head, slot, dim]")
+    s = pool.stride()
+    if layout == "NHD":
+        return s[0], s[1], s[2]
+    if layout == "HND":
+        return s[0], s[2], s[1]
+    raise ValueError(f"unknown layout {layout!r}")
+
+
+def make_params(q, k_pool, v_pool, block_table, seq_lens, out, *, page_size, scale, Hkv,
+                D_v, lse=None, workspace=None, err_flags=None, num_ctas=0, max_seq_len=0,
+                layout="NHD", events=None) -> Params:
+    B, q_len, Hq, D_qk = q.shape
+    ps, ts, hs = _pool_strides(k_pool, layout)
+    if v_pool is not None and _pool_strides(v_pool, layout) != (ps, ts, hs):
+        raise ValueError("K and V pools must share strides")
+    if k_pool.stride(3) != 1 or not q.is_contiguous() or not out.is_contiguous():
+        raise ValueError("q, out and the pool rows must be contiguous")
+    if block_table.stride(1) != 1:
+        raise ValueError("block_table rows must be contiguous")
+    p = Params()
+    p.struct_size = ctypes.sizeof(Params)
+    p.q, p.k_pool, p.v_pool = _ptr(q), _ptr(k_pool), _ptr(v_pool)
+    p.page_stride, p.token_stride, p.head_stride = ps, ts, hs
+    p.block_table = _ptr(block_table)
+    p.block_table_stride = block_table.stride(0)
+    p.seq_lens = _ptr(seq_lens)
+    p.out, p.lse = _ptr(out), _ptr(lse)
+    p.B, p.q_len, p.Hq, p.Hkv, p.D_qk, p.D_v = B, q_len, Hq, Hkv, D_qk, D_v
+    p.page_size = page_size
+    p.num_pages = k_pool.shape[0]
+    p.max_seq_len = int(max_seq_len)
+    p.scale = float(scale)
+    if workspace is not None:
+        p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    p.err_flags = _ptr(err_flags)
+    p.num_ctas = int(num_ctas)
+    if events is not None:
+        p.attn_begin, p.attn_end = events[0].cuda_event, events[1].cuda_event
+    return p
+
+
+def workspace_size(params: Params) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().zl_decode_attn_workspace_size(ctypes.byref(params), ctypes.byref(n)),
+           "zl_decode_attn_workspace_size")
+    return n.value
+
+
+def workspace_size_mla(params: Params) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().zl_decode_attn_mla_workspace_size(ctypes.byref(params), ctypes.byref(n)),
+           "zl_decode_attn_mla_workspace_size")
+    return n.value
+
+
+_ws_cache: dict = {}
+
+
+def _workspace(device, nbytes):
+    """A cached device byte buffer of at least nbytes (256-byte aligned by torch)."""
+    key = (device.type, device.index)
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf
+
+
+def call(params: Params, *, mla: bool, stream=None):
+    """Invoke the entry point on ``stream`` (default: torch's current stream)."""
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    fn = lib().zl_decode_attn_mla if mla else lib().zl_decode_attn
+    _check(fn(ctypes.byref(params), ctypes.c_void_p(stream.cuda_stream)),
+           "zl_decode_attn_mla" if mla else "zl_decode_attn")
+
+
+def _run(q, k_pool, v_pool, block_table, seq_lens, *, mla, page_size, scale, Hkv, D_v, out, lse,
+         workspace, err_flags, num_ctas, max_seq_len, layout, stream, events):
+    if out is None:
+        out = torch.empty(q.shape[:3] + (D_v,), dtype=torch.bfloat16, device=q.device)
+    p = make_params(q, k_pool, v_pool, block_table, seq_lens, out, page_size=page_size,
+                    scale=scale, Hkv=Hkv, D_v=D_v, lse=lse, err_flags=err_flags,
+                    num_ctas=num_ctas, max_seq_len=max_seq_len, layout=layout, events=events)
+    need = workspace_size_mla(p) if mla else workspace_size(p)
+    if workspace is None:
+        workspace = _workspace(q.device, need)
+    p.workspace = workspace.data_ptr()
+    p.workspace_bytes = workspace.numel() * workspace.element_size()
+    call(p, mla=mla, stream=stream)
+    return out
+
+
+def decode_attn(q, k_pool, v_pool, block_table, seq_lens, *, page_size, scale, out=None, lse=None,
+                workspace=None, err_flags=None, num_ctas=0, max_seq_len=0, layout="NHD",
+                stream=None, events=None):
+    """GQA/MHA/MQA paged decode attention (zl_decode_attn).
+
+    q [B, 1, Hq, 128] bf16; k_pool, v_pool [pages, page_size, Hkv, 128] (layout
+    "NHD") or [pages, Hkv, page_size, 128] ("HND") bf16; block_table int32
+    [B, max_pages]; seq_lens int32 [B]. Returns out [B, 1, Hq, 128] bf16.
+    """
+    Hkv = k_pool.shape[2] if layout == "NHD" else k_pool.shape[1]
+    return _run(q, k_pool, v_pool, block_table, seq_lens, mla=False, page_size=page_size,
+                scale=scale, Hkv=Hkv, D_v=q.shape[3], out=out, lse=lse, workspace=workspace,
+                err_flags=err_flags, num_ctas=num_ctas, max_seq_len=max_seq_len, layout=layout,
+                stream=stream, events=events)
+
+
+def decode_attn_mla(q, kv_pool, block_table, seq_lens, *, page_size, scale, D_v=512, out=None,
+                    lse=None, workspace=None, err_flags=None, num_ctas=0, max_seq_len=0,
+                    stream=None, events=None):
+    """Absorbed MLA paged decode (zl_decode_attn_mla).
+
+    q [B, 1, Hq, 576] bf16; kv_pool [pages, page_size, 1, 576] bf16 (V = first
+    D_v columns). Returns out [B, 1, Hq, D_v] bf16.
+    """
+    return _run(q, kv_pool, None, block_table, seq_lens, mla=True, page_size=page_size,
+                scale=scale, Hkv=1, D_v=D_v, out=out, lse=lse, workspace=workspace,
+                err_flags=err_flags, num_ctas=num_ctas, max_seq_len=max_seq_len, layout="NHD",
+                stream=stream, events=events)

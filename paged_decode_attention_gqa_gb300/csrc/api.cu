@@ -1,0 +1,217 @@
+// C-ABI front end: argument validation, split plan (grid size), TMA tensor
+// maps, workspace layout, launches. Declared in include/zl_decode_attn.h.
+#include "../../include/zl_decode_attn.h"
+#include "kernels.h"
+
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+namespace {
+
+using zl::GqaParams;
+
+constexpr double kLog2e = 1.4426950408889634;
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// cuTensorMapEncodeTiled from the driver, fetched once through the runtime so
+// the library links against cudart only.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+struct DeviceInfo {
+  int device = -1;
+  int sms = 0;
+};
+
+zl_status current_device(DeviceInfo* info) {
+  static int sm_count[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ZL_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return ZL_ERR_UNSUPPORTED;
+  if (sm_count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return ZL_ERR_CUDA;
+    sm_count[dev] = n;
+  }
+  info->device = dev;
+  info->sms = sm_count[dev];
+  return ZL_OK;
+}
+
+// ------------------------------------------------------------------ GQA plan
+struct GqaPlan {
+  int hpc = 0, nhg = 0, g = 0, grid = 0;
+  size_t off_lse = 0, off_o = 0, bytes = 0;
+};
+
+zl_status gqa_validate_shape(const zl_decode_attn_params* a) {
+  if (!a || a->struct_size != sizeof(zl_decode_attn_params)) return ZL_ERR_INVALID_ARG;
+  if (a->B < 1 || a->Hq < 1 || a->Hkv < 1 || a->q_len < 1 || a->page_size < 1 ||
+      a->num_pages < 1 || a->block_table_stride < 1 || a->D_qk < 1 || a->D_v < 1 ||
+      a->num_ctas < 0 || a->max_seq_len < 0)
+    return ZL_ERR_INVALID_ARG;
+  if (a->Hq % a->Hkv != 0) return ZL_ERR_INVALID_ARG;
+  if (!(a->scale > 0.f) || !std::isfinite(a->scale)) return ZL_ERR_INVALID_ARG;
+  if (a->D_qk != zl::kGqaHeadDim || a->D_v != zl::kGqaHeadDim) return ZL_ERR_UNSUPPORTED;
+  if (a->Hq / a->Hkv > 16) return ZL_ERR_UNSUPPORTED;
+  if (a->q_len != 1) return ZL_ERR_UNSUPPORTED;
+  if (a->page_size % zl::kGqaTile != 0 || a->page_size > 1024) return ZL_ERR_UNSUPPORTED;
+  if (a->B > zl::kMaxBatch) return ZL_ERR_UNSUPPORTED;
+  return ZL_OK;
+}
+
+zl_status gqa_plan(const zl_decode_attn_params* a, GqaPlan* plan) {
+  zl_status st = gqa_validate_shape(a);
+  if (st != ZL_OK) return st;
+  DeviceInfo dev;
+  if ((st = current_device(&dev)) != ZL_OK) return st;
+  plan->g = a->Hq / a->Hkv;
+  plan->hpc = zl::gqa_heads_per_cta(a->Hkv);
+  plan->nhg = a->Hkv / plan->hpc;
+  int grid = a->num_ctas;
+  if (grid == 0) {
+    const int per_sm = zl::gqa_ctas_per_sm(plan->hpc, plan->g > 8, dev.device);
+    if (per_sm < 1) return ZL_ERR_CUDA;
+    grid = dev.sms * per_sm;
+    if (a->max_seq_len > 0) {
+      // No more CTAs than tiles: B * head groups * ceil(max_seq_len / 16).
+      const int64_t tiles = int64_t(a->B) * plan->nhg *
+                            ((int64_t(a->max_seq_len) + zl::kGqaTile - 1) / zl::kGqaTile);
+      if (tiles < grid) grid = int(tiles < 1 ? 1 : tiles);
+    }
+  }
+  plan->grid = grid;
+  const size_t rows = size_t(grid) * 2 * plan->hpc * plan->g;  // partial slots
+  plan->off_lse = round_up(size_t(a->B + 1) * sizeof(int32_t), 256);
+  plan->off_o = plan->off_lse + round_up(rows * sizeof(float), 256);
+  plan->bytes = plan->off_o + rows * zl::kGqaHeadDim * sizeof(float);
+  return ZL_OK;
+}
+
+zl_status encode_pool_map(CUtensorMap* map, const void* pool, const zl_decode_attn_params* a,
+                          int box_heads) {
+  auto encode = tensor_map_encoder();
+  if (!encode) return ZL_ERR_CUDA;
+  const cuuint64_t dims[4] = {cuuint64_t(a->D_qk), cuuint64_t(a->page_size), cuuint64_t(a->Hkv),
+                              cuuint64_t(a->num_pages)};
+  const cuuint64_t strides[3] = {cuuint64_t(a->token_stride) * 2, cuuint64_t(a->head_stride) * 2,
+                                 cuuint64_t(a->page_stride) * 2};
+  const cuuint32_t box[4] = {64, cuuint32_t(zl::kGqaTile), cuuint32_t(box_heads), 1};
+  const cuuint32_t elem[4] = {1, 1, 1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(pool),
+                            dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ZL_OK : ZL_ERR_UNSUPPORTED;
+}
+
+zl_status validate_pointers(const zl_decode_attn_params* a, bool need_v) {
+  if (!a->q || !a->k_pool || !a->block_table || !a->seq_lens || !a->out)
+    return ZL_ERR_INVALID_ARG;
+  if (need_v && !a->v_pool) return ZL_ERR_INVALID_ARG;
+  if (!need_v && a->v_pool) return ZL_ERR_INVALID_ARG;
+  if (!aligned(a->q, 16) || !aligned(a->k_pool, 16) || !aligned(a->out, 16) ||
+      (a->v_pool && !aligned(a->v_pool, 16)) || !aligned(a->block_table, 4) ||
+      !aligned(a->seq_lens, 4) || (a->lse && !aligned(a->lse, 4)) ||
+      (a->err_flags && !aligned(a->err_flags, 4)))
+    return ZL_ERR_INVALID_ARG;
+  if (a->page_stride <= 0 || a->token_stride <= 0 || a->head_stride <= 0 ||
+      a->page_stride % 8 || a->token_stride % 8 || a->head_stride % 8)
+    return ZL_ERR_INVALID_ARG;
+  return ZL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* zl_status_string(zl_status s) {
+  switch (s) {
+    case ZL_OK: return "ok";
+    case ZL_ERR_INVALID_ARG: return "invalid argument";
+    case ZL_ERR_UNSUPPORTED: return "unsupported shape or layout";
+    case ZL_ERR_WORKSPACE: return "workspace missing or too small";
+    case ZL_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+zl_status zl_decode_attn_workspace_size(const zl_decode_attn_params* a, size_t* bytes) {
+  if (!bytes) return ZL_ERR_INVALID_ARG;
+  GqaPlan plan;
+  const zl_status st = gqa_plan(a, &plan);
+  if (st != ZL_OK) return st;
+  *bytes = plan.bytes;
+  return ZL_OK;
+}
+
+zl_status zl_decode_attn(const zl_decode_attn_params* a, zl_stream_t stream) {
+  zl_status st = gqa_validate_shape(a);
+  if (st != ZL_OK) return st;
+  if ((st = validate_pointers(a, true)) != ZL_OK) return st;
+  GqaPlan plan;
+  if ((st = gqa_plan(a, &plan)) != ZL_OK) return st;
+  if (!a->workspace || !aligned(a->workspace, 256) || a->workspace_bytes < plan.bytes)
+    return ZL_ERR_WORKSPACE;
+
+  GqaParams p;
+  std::memset(&p, 0, sizeof(p));
+  if ((st = encode_pool_map(&p.tmap_k, a->k_pool, a, plan.hpc)) != ZL_OK) return st;
+  if ((st = encode_pool_map(&p.tmap_v, a->v_pool, a, plan.hpc)) != ZL_OK) return st;
+  p.q = static_cast<const __nv_bfloat16*>(a->q);
+  p.out = static_cast<__nv_bfloat16*>(a->out);
+  p.lse = a->lse;
+  p.block_table = a->block_table;
+  p.seq_lens = a->seq_lens;
+  p.bt_stride = a->block_table_stride;
+  char* ws = static_cast<char*>(a->workspace);
+  p.ws_prefix = reinterpret_cast<int32_t*>(ws);
+  p.ws_lse = reinterpret_cast<float*>(ws + plan.off_lse);
+  p.ws_o = reinterpret_cast<float*>(ws + plan.off_o);
+  p.err_flags = a->err_flags;
+  p.B = a->B;
+  p.Hq = a->Hq;
+  p.Hkv = a->Hkv;
+  p.g = plan.g;
+  p.page_size = a->page_size;
+  p.num_pages = a->num_pages;
+  p.hpc = plan.hpc;
+  p.nhg = plan.nhg;
+  p.scale_log2 = float(double(a->scale) * kLog2e);
+
+  const cudaError_t e = zl::gqa_decode_launch(p, plan.grid, reinterpret_cast<cudaStream_t>(stream),
+                                              reinterpret_cast<cudaEvent_t>(a->attn_begin),
+                                              reinterpret_cast<cudaEvent_t>(a->attn_end));
+  return e == cudaSuccess ? ZL_OK : ZL_ERR_CUDA;
+}
+
+zl_status zl_decode_attn_mla_workspace_size(const zl_decode_attn_params* a, size_t* bytes) {
+  (void)a;
+  (void)bytes;
+  return ZL_ERR_UNSUPPORTED;
+}
+
+zl_status zl_decode_attn_mla(const zl_decode_attn_params* a, zl_stream_t stream) {
+  (void)a;
+  (void)stream;
+  return ZL_ERR_UNSUPPORTED;
+}
+
+}  // extern "C"

@@ -1,0 +1,43 @@
+// Internal interface between the C-ABI front end (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace zl {
+
+constexpr int kGqaTile = 16;     // tokens per pipeline stage of the GQA kernel
+constexpr int kGqaHeadDim = 128; // D_qk = D_v
+constexpr int kMaxBatch = 4096;  // sequences per call (prefix table lives in smem)
+
+// Everything the GQA attention kernel and its merge kernel read.
+struct GqaParams {
+  CUtensorMap tmap_k;  // 4-D {D, page_size, Hkv, num_pages}, box {64, 16, HPC, 1}, 128B swizzle
+  CUtensorMap tmap_v;  // same geometry over the V pool
+  const __nv_bfloat16* q;  // [B, Hq, 128]
+  __nv_bfloat16* out;      // [B, Hq, 128]
+  float* lse;              // [B, Hq] natural log, or nullptr
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int64_t bt_stride;
+  int32_t* ws_prefix;  // [B + 1] tile prefix sums, written by CTA 0
+  float* ws_o;         // [G][2][HPC][g][128] normalised partial outputs
+  float* ws_lse;       // [G][2][HPC][g] base-2 lse of the partials (NaN = bad piece)
+  uint32_t* err_flags; // or nullptr
+  int B, Hq, Hkv, g, page_size, num_pages;
+  int hpc;             // kv heads per CTA
+  int nhg;             // Hkv / hpc head groups
+  float scale_log2;    // scale * log2(e)
+};
+
+// kv heads handled by one CTA for this Hkv (largest of 8, 4, 2, 1 dividing it).
+int gqa_heads_per_cta(int Hkv);
+// CTAs of the attention kernel that fit on one SM (0 on error).
+int gqa_ctas_per_sm(int hpc, bool rows16, int device);
+// Launches the attention kernel on `grid` CTAs, then the merge kernel.
+cudaError_t gqa_decode_launch(const GqaParams& p, int grid, cudaStream_t stream,
+                              cudaEvent_t attn_begin, cudaEvent_t attn_end);
+
+}  // namespace zl

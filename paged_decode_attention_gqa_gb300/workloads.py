@@ -291,7 +291,7 @@ WORKLOADS = {
 
 def random_case(seed, *, B, Hq, Hkv, D=128, page_size=16, lens=None, max_len=300, layout="NHD",
                 pool_factor=1.5, poison=True, q_len=1, mla=False, D_v=None, scale=None,
-                shared_prefix_pages=0) -> Workload:
+                shared_prefix_pages=0, values=True) -> Workload:
     """A small randomized case for parity sweeps (explicit or random lengths)."""
     rng = _structure_rng(seed)
     if lens is None:

@@ -1,0 +1,79 @@
+"""The C-ABI library: it builds, loads, exports what the header declares, and
+rejects bad arguments on the host before touching the GPU (CPU only)."""
+import ctypes
+
+import pytest
+import torch
+
+import paged_decode_attention_gqa_gb300 as zl
+
+
+def test_builds_and_exports_every_declared_symbol():
+    lib = zl.lib()
+    names = zl.declared_symbols()
+    assert {"zl_decode_attn", "zl_decode_attn_mla", "zl_decode_attn_workspace_size",
+            "zl_decode_attn_mla_workspace_size", "zl_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings():
+    lib = zl.lib()
+    for code in range(5):
+        assert lib.zl_status_string(code)
+    assert lib.zl_status_string(0) == b"ok"
+
+
+def _params(**over):
+    """A fully valid-looking GQA parameter block with fake aligned pointers."""
+    p = zl.Params()
+    p.struct_size = ctypes.sizeof(zl.Params)
+    fake = 1 << 20
+    p.q = p.k_pool = p.v_pool = p.out = fake
+    p.block_table = p.seq_lens = fake
+    p.page_stride, p.token_stride, p.head_stride = 16 * 8 * 128, 8 * 128, 128
+    p.block_table_stride = 8
+    p.B, p.q_len, p.Hq, p.Hkv, p.D_qk, p.D_v = 4, 1, 32, 8, 128, 128
+    p.page_size, p.num_pages = 16, 64
+    p.scale = 128 ** -0.5
+    for k, v in over.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(struct_size=8), zl.ERR_INVALID_ARG),
+    (dict(B=0), zl.ERR_INVALID_ARG),
+    (dict(Hkv=0), zl.ERR_INVALID_ARG),
+    (dict(Hq=30), zl.ERR_INVALID_ARG),           # Hq % Hkv != 0
+    (dict(scale=0.0), zl.ERR_INVALID_ARG),
+    (dict(scale=float("nan")), zl.ERR_INVALID_ARG),
+    (dict(num_ctas=-1), zl.ERR_INVALID_ARG),
+    (dict(q=None), zl.ERR_INVALID_ARG),
+    (dict(v_pool=None), zl.ERR_INVALID_ARG),
+    (dict(out=None), zl.ERR_INVALID_ARG),
+    (dict(q=(1 << 20) + 2), zl.ERR_INVALID_ARG),  # misaligned
+    (dict(token_stride=100), zl.ERR_INVALID_ARG),  # not a multiple of 8 elements
+    (dict(D_qk=64, D_v=64), zl.ERR_UNSUPPORTED),
+    (dict(Hq=8 * 32), zl.ERR_UNSUPPORTED),         # group of 32 heads
+    (dict(q_len=2), zl.ERR_UNSUPPORTED),
+    (dict(page_size=8), zl.ERR_UNSUPPORTED),
+    (dict(B=5000), zl.ERR_UNSUPPORTED),
+])
+def test_host_validation(over, code):
+    p = _params(**over)
+    assert zl.lib().zl_decode_attn(ctypes.byref(p), None) == code
+
+
+def test_null_params():
+    assert zl.lib().zl_decode_attn(None, None) == zl.ERR_INVALID_ARG
+    n = ctypes.c_size_t(0)
+    assert zl.lib().zl_decode_attn_workspace_size(None, ctypes.byref(n)) == zl.ERR_INVALID_ARG
+
+
+def test_no_cpu_fallback():
+    """Without a GPU the valid call fails loudly instead of computing on the CPU."""
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    p = _params()
+    assert zl.lib().zl_decode_attn(ctypes.byref(p), None) != zl.OK

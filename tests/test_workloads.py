@@ -67,3 +67,14 @@ def test_pages_are_distinct_without_prefix():
     ids = np.concatenate([c2.block_table[i, :(L + 15) // 16] for i, L in enumerate(c2.seq_lens)])
     assert np.unique(ids).size == ids.size
     assert ids.min() >= 0 and ids.max() < c2.num_pages
+
+
+def test_random_case_structure():
+    w = wl.random_case(7, B=6, Hq=16, Hkv=4, lens=[1, 15, 16, 17, 0, 300])
+    assert w.q.shape == (6, 1, 16, 128) and w.k_pool.shape[1:] == (16, 4, 128)
+    assert (w.block_table[4] == -1).all()
+    h = wl.random_case(7, B=6, Hq=16, Hkv=4, lens=[1, 15, 16, 17, 0, 300], layout="HND")
+    assert torch.equal(w.k_pool.view(torch.int16),
+                       h.k_pool.permute(0, 2, 1, 3).contiguous().view(torch.int16))
+    m = wl.random_case(8, B=2, Hq=16, Hkv=1, D=576, D_v=512, mla=True, page_size=64)
+    assert m.mla and m.v_pool is None and m.k_pool.shape[1:] == (64, 1, 576)
