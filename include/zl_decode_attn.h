@@ -138,6 +138,29 @@ zl_status zl_decode_attn_mla(const zl_decode_attn_params* params, zl_stream_t st
 zl_status zl_decode_attn_workspace_size(const zl_decode_attn_params* params, size_t* bytes);
 zl_status zl_decode_attn_mla_workspace_size(const zl_decode_attn_params* params, size_t* bytes);
 
+/*
+ * zl_decode_attn without a caller-provided workspace, for callers that cannot
+ * allocate device memory (a host that already reserved all of it for its own
+ * pool, a plugin interface with no scratch allocator, a loop that cannot
+ * afford cudaMalloc's implicit synchronisation). The pages describe no such
+ * entry point; it has no counterpart there.
+ *   - Same arguments, checks and results as zl_decode_attn; workspace and
+ *     workspace_bytes are ignored.
+ *   - The scratch is one array of ZL_NOALLOC_WORKSPACE_BYTES in the library's
+ *     own device memory; every GPU that loads the library holds it until the
+ *     process exits. A call whose zl_decode_attn_workspace_size() exceeds it
+ *     returns ZL_ERR_WORKSPACE (a smaller num_ctas shrinks the need).
+ *   - The first call on each device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Calls allocate nothing: no cudaMalloc, cudaFree or allocating library
+ *     routine. All calls share the one array, which keeps the last call's
+ *     contents; nothing in it needs clearing (each launch writes what it later
+ *     reads). Calls that overlap on the GPU (other streams, other threads)
+ *     race on it: serialise them.
+ */
+#define ZL_NOALLOC_WORKSPACE_BYTES (8u << 20)
+zl_status zl_decode_attn_noalloc(const zl_decode_attn_params* params, zl_stream_t stream);
+
 /* Static description of a status code. */
 const char* zl_status_string(zl_status status);
 

@@ -25,7 +25,7 @@ from ._build import LIB_PATH, build  # noqa: F401  (build() is the public build 
 
 __all__ = [
     "ZlError", "Params", "lib", "decode_attn", "decode_attn_mla", "workspace_size",
-    "workspace_size_mla", "call", "build", "LIB_PATH", "DEVERR_BAD_PAGE", "DEVERR_BAD_SEQ_LEN",
+    "workspace_size_mla", "call", "call_noalloc", "build", "LIB_PATH", "DEVERR_BAD_PAGE", "DEVERR_BAD_SEQ_LEN",
     "DEVERR_TIMEOUT", "HEADER", "declared_symbols",
 ]
 
@@ -91,7 +91,7 @@ def lib():
             except Exception as e:  # no fallback: the CUDA path is the product
                 raise RuntimeError(f"libzl_decode_attn could not be built or loaded: {e}") from e
             P = ctypes.POINTER(Params)
-            for name in ("zl_decode_attn", "zl_decode_attn_mla"):
+            for name in ("zl_decode_attn", "zl_decode_attn_mla", "zl_decode_attn_noalloc"):
                 fn = getattr(handle, name)
                 fn.restype = ctypes.c_int
                 fn.argtypes = [P, ctypes.c_void_p]
@@ -190,6 +190,15 @@ def _workspace(device, nbytes):
         buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
         _ws_cache[key] = buf
     return buf
+
+
+def call_noalloc(params: Params, stream=None):
+    """zl_decode_attn_noalloc: the library's own static scratch, no workspace
+    argument and no allocation (see the header for its limits)."""
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    _check(lib().zl_decode_attn_noalloc(ctypes.byref(params), ctypes.c_void_p(stream.cuda_stream)),
+           "zl_decode_attn_noalloc")
 
 
 def call(params: Params, *, mla: bool, stream=None):
