@@ -34,7 +34,8 @@ METRIC = "decode-attn KV read GB/s (Llama-3-8B shape)"
 UNIT = "GB/s"
 WORKLOAD = "llama3_8b_decode"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
-KERNEL_SRC = os.path.join(ROOT, "paged_decode_attention_gqa_gb300", "csrc", "gqa_decode.cu")
+CSRC = os.path.join(ROOT, "paged_decode_attention_gqa_gb300", "csrc")
+KERNEL_SRC = {"gqa": os.path.join(CSRC, "gqa_decode.cu"), "mla": os.path.join(CSRC, "mla_decode.cu")}
 
 
 def measured_peaks():
@@ -46,12 +47,12 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def kernel_hash():
-    with open(KERNEL_SRC, "rb") as f:
+def kernel_hash(kind):
+    with open(KERNEL_SRC[kind], "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def traffic_per_launch(workload):
+def traffic_per_launch(workload, kind):
     """DRAM bytes per attention launch from the committed ncu summary, if the
     kernel source has not changed since it was captured; else None."""
     if not os.path.exists(TRAFFIC_FILE):
@@ -59,20 +60,34 @@ def traffic_per_launch(workload):
     with open(TRAFFIC_FILE) as f:
         d = json.load(f)
     e = d.get(workload)
-    if not e or e.get("kernel_sha256_16") != kernel_hash():
+    if not e or e.get("kernel_sha256_16") != kernel_hash(kind):
         return None
     return e.get("dram_bytes_per_launch")
 
 
 def kv_bytes(w):
-    """Algorithmic bytes: K and V rows of every visible token, once."""
-    return int(np.asarray(w.seq_lens, dtype=np.int64).sum()) * w.Hkv * 2 * w.D_qk * 2
+    """Algorithmic bytes: the K and V rows of every visible token, once (MLA:
+    the one latent row, V being part of it)."""
+    tokens = int(np.asarray(w.seq_lens, dtype=np.int64).sum())
+    if w.mla:
+        return tokens * w.D_qk * 2
+    return tokens * w.Hkv * 2 * w.D_qk * 2
 
 
 def io_bytes(w):
     """Q read + out written + block table and seq_lens read (per launch)."""
     pages = int(((w.seq_lens.astype(np.int64) + w.page_size - 1) // w.page_size).sum())
-    return w.B * w.Hq * w.D_qk * 2 * 2 + pages * 4 + w.B * 4
+    return w.B * w.Hq * (w.D_qk + w.D_v) * 2 + pages * 4 + w.B * 4
+
+
+def metric_name(workload):
+    return METRIC if workload == WORKLOAD else f"decode-attn KV read GB/s ({workload})"
+
+
+def make_workload(name, batch=None):
+    from paged_decode_attention_gqa_gb300 import workloads
+    fn = workloads.WORKLOADS[name]
+    return fn(B=batch) if batch else fn()
 
 
 class ClockSampler:
@@ -143,13 +158,14 @@ def time_oracle(w, min_seconds=10.0, max_calls=50):
     import oracle
     orc = oracle.load()
     threads = cpu_cores()
-    q, k, v = w.bits(w.q), w.bits(w.k_pool), w.bits(w.v_pool)
+    q, k = w.bits(w.q), w.bits(w.k_pool)
+    v = None if w.mla else w.bits(w.v_pool)
     times = []
     t_start = time.perf_counter()
     while len(times) < max_calls and (time.perf_counter() - t_start) < min_seconds:
         t0 = time.perf_counter()
         orc.decode_attn(q, k, v, w.strides, w.block_table, w.seq_lens, Hkv=w.Hkv,
-                        page_size=w.page_size, num_pages=w.num_pages, scale=w.scale,
+                        page_size=w.page_size, num_pages=w.num_pages, scale=w.scale, D_v=w.D_v,
                         num_threads=threads)
         times.append(time.perf_counter() - t0)
     return statistics.median(times), len(times), threads
@@ -165,16 +181,17 @@ def run_reference(args, world, rank, budget_s=120.0):
     if rank != 0:
         return
     from paged_decode_attention_gqa_gb300 import workloads
-    w = workloads.llama3_8b_decode()
+    w = make_workload(args.workload, args.batch)
     import oracle
     orc = oracle.load()
     threads = cpu_cores()
-    q, k, v = w.bits(w.q), w.bits(w.k_pool), w.bits(w.v_pool)
+    q, k = w.bits(w.q), w.bits(w.k_pool)
+    v = None if w.mla else w.bits(w.v_pool)
 
     def run(n):
         orc.decode_attn(q[:n], k, v, w.strides, w.block_table[:n], w.seq_lens[:n], Hkv=w.Hkv,
                         page_size=w.page_size, num_pages=w.num_pages, scale=w.scale,
-                        num_threads=threads)
+                        D_v=w.D_v, num_threads=threads)
 
     t0 = time.perf_counter()
     run(8)
@@ -187,12 +204,13 @@ def run_reference(args, world, rank, budget_s=120.0):
     for _ in range(args.steps):
         run(n)
     dt = (time.perf_counter() - t0) / args.steps
-    sample_bytes = int(w.seq_lens[:n].astype(np.int64).sum()) * w.Hkv * 2 * w.D_qk * 2
+    sample_bytes = kv_bytes(w) * int(w.seq_lens[:n].astype(np.int64).sum()) // int(
+        w.seq_lens.astype(np.int64).sum())
     gbs = sample_bytes / dt / 1e9
     sample = (f"first {n} of {w.B} sequences per step (all heads), "
               f"{int(w.seq_lens[:n].sum())} tokens")
     line = {
-        "impl": "reference", "metric": METRIC, "value": gbs, "unit": UNIT, "n_gpus": world,
+        "impl": "reference", "metric": metric_name(args.workload), "value": gbs, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": config_of(w, world),
@@ -204,16 +222,18 @@ def run_reference(args, world, rank, budget_s=120.0):
 
 
 def config_of(w, world):
-    return {"workload": WORKLOAD, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.D_qk,
-            "page_size": w.page_size, "seq_len": "U[512,4096]", "q_len": w.q_len,
-            "kv_bytes_per_step": kv_bytes(w), "seed": w.seed,
-            "l2": "no flush: KV working set per step exceeds the 129 MB L2",
+    lens = w.seq_lens
+    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D_qk": w.D_qk,
+            "D_v": w.D_v, "page_size": w.page_size,
+            "seq_len": f"{int(lens.min())}..{int(lens.max())} (sum {int(lens.sum())})",
+            "q_len": w.q_len, "kv_bytes_per_step": kv_bytes(w), "seed": w.seed,
+            "l2": ("no flush: KV working set per step exceeds the 129 MB L2"
+                   if kv_bytes(w) > 4 * 129e6 else "L2 flushed between steps"),
             "parallelism": f"replicas x{world}"}
 
 
 def run_ours(args, world, rank, local):
     import paged_decode_attention_gqa_gb300 as zl
-    from paged_decode_attention_gqa_gb300 import workloads
 
     if world > 1:
         import torch.distributed as dist
@@ -226,8 +246,10 @@ def run_ours(args, world, rank, local):
         dist.barrier()
     zl.lib()
 
-    w = workloads.llama3_8b_decode()
-    q, k, v = w.q.to(dev), w.k_pool.to(dev), w.v_pool.to(dev)
+    w = make_workload(args.workload, args.batch)
+    kind = "mla" if w.mla else "gqa"
+    q, k = w.q.to(dev), w.k_pool.to(dev)
+    v = None if w.mla else w.v_pool.to(dev)
     bt = torch.from_numpy(w.block_table).to(dev)
     sl = torch.from_numpy(w.seq_lens).to(dev)
     out = torch.empty(w.B, 1, w.Hq, w.D_v, dtype=torch.bfloat16, device=dev)
@@ -235,12 +257,19 @@ def run_ours(args, world, rank, local):
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     p = zl.make_params(q, k, v, bt, sl, out, page_size=w.page_size, scale=w.scale, Hkv=w.Hkv,
                        D_v=w.D_v, lse=lse, err_flags=err, max_seq_len=w.max_seq_len)
-    ws = torch.empty(zl.workspace_size(p), dtype=torch.uint8, device=dev)
+    need = zl.workspace_size_mla(p) if w.mla else zl.workspace_size(p)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     p.workspace, p.workspace_bytes = ws.data_ptr(), ws.numel()
     stream = torch.cuda.current_stream()
+    # Small working sets are flushed from L2 between steps (a 2x L2 write).
+    flush = None
+    if kv_bytes(w) <= 4 * 129e6:
+        flush = torch.empty(int(2 * 129e6) // 4, dtype=torch.int32, device=dev)
 
     def step():
-        zl.call(p, mla=False, stream=stream)
+        if flush is not None:
+            flush.zero_()
+        zl.call(p, mla=w.mla, stream=stream)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -258,8 +287,9 @@ def run_ours(args, world, rank, local):
         a.record(stream)
         b.record(stream)
     sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.4)
+    if not args.no_clocks:
+        sampler.start()
+        time.sleep(0.4)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -283,27 +313,41 @@ def run_ours(args, world, rank, local):
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
-    launches = 2 * args.steps
+    launches = args.steps * (2 if kind == "gqa" else 1)   # attention (+ merge)
+    if flush is not None:
+        launches += args.steps                              # the L2 flush memset
 
     # ---- end to end through the public API: host inputs in, host result out
-    pin_q = w.q.pin_memory()
-    pin_bt = torch.from_numpy(w.block_table).pin_memory()
-    pin_sl = torch.from_numpy(w.seq_lens).pin_memory()
-    pin_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    e2e_steps = max(10, min(args.steps, 2000))
-    h2d = pin_q.numel() * 2 + pin_bt.numel() * 4 + pin_sl.numel() * 4
-    d2h = pin_out.numel() * 2
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        q.copy_(pin_q, non_blocking=True)
-        bt.copy_(pin_bt, non_blocking=True)
-        sl.copy_(pin_sl, non_blocking=True)
-        zl.decode_attn(q, k, v, bt, sl, page_size=w.page_size, scale=w.scale, out=out,
-                       workspace=ws, max_seq_len=w.max_seq_len)
-        pin_out.copy_(out, non_blocking=True)
-    torch.cuda.synchronize()
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    e2e = None
+    if not args.no_e2e:
+        pin_q = w.q.pin_memory()
+        pin_bt = torch.from_numpy(w.block_table).pin_memory()
+        pin_sl = torch.from_numpy(w.seq_lens).pin_memory()
+        pin_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        e2e_steps = max(10, min(args.steps, 2000))
+        h2d = pin_q.numel() * 2 + pin_bt.numel() * 4 + pin_sl.numel() * 4
+        d2h = pin_out.numel() * 2
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            q.copy_(pin_q, non_blocking=True)
+            bt.copy_(pin_bt, non_blocking=True)
+            sl.copy_(pin_sl, non_blocking=True)
+            if flush is not None:
+                flush.zero_()
+            if w.mla:
+                zl.decode_attn_mla(q, k, bt, sl, page_size=w.page_size, scale=w.scale, D_v=w.D_v,
+                                   out=out, workspace=ws, max_seq_len=w.max_seq_len)
+            else:
+                zl.decode_attn(q, k, v, bt, sl, page_size=w.page_size, scale=w.scale, out=out,
+                               workspace=ws, max_seq_len=w.max_seq_len)
+            pin_out.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        e2e_s = (time.perf_counter() - t0) / e2e_steps
+        e2e = {"value": kv_bytes(w) * world / e2e_s / 1e9, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "us_per_step": e2e_s * 1e6,
+               "note": "q, block table and seq_lens copied in from pinned host memory and the "
+                       "output copied back every step; the KV cache is device-resident state"}
 
     if rank != 0:
         if world > 1:
@@ -315,9 +359,13 @@ def run_ours(args, world, rank, local):
     peak, peak_kind = measured_peaks()
     algo = kvb + io_bytes(w)
     achieved = algo / (attn_ms * 1e-3) / 1e9
-    cpu_s, cpu_calls, cores = time_oracle(w) if not args.no_cpu_baseline else (None, 0, 0)
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu_s, cpu_calls, cores = time_oracle(w)
+        cpu = {"value": kvb / cpu_s / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"the whole workload per call, {cpu_calls} calls (median)"}
     line = {
-        "metric": METRIC,
+        "metric": metric_name(args.workload),
         "value": kvb * world / (ms * 1e-3) / 1e9,
         "unit": UNIT,
         "n_gpus": world,
@@ -334,19 +382,17 @@ def run_ours(args, world, rank, local):
         "config": config_of(w, world),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "kernel": "gqa_decode_kernel", "attn_us_per_launch": attn_ms * 1e3,
+                     "kernel": f"{kind}_decode_kernel", "attn_us_per_launch": attn_ms * 1e3,
                      "algorithmic_bytes_per_launch": algo,
-                     "traffic": traffic_per_launch(WORKLOAD)},
-        "cpu_baseline": None if cpu_s is None else {
-            "value": kvb / cpu_s / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"the whole workload per call, {cpu_calls} calls (median)"},
-        "e2e": {"value": kvb * world / e2e_s / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "us_per_step": e2e_s * 1e6,
-                "note": "q, block table and seq_lens copied in from pinned host memory and the "
-                        "output copied back every step; the KV cache is device-resident state"},
+                     "traffic": traffic_per_launch(w.name, kind)},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clocks,
     }
+    if w.mla:
+        flops = 2.0 * int(w.seq_lens.astype(np.int64).sum()) * w.Hq * (w.D_qk + w.D_v)
+        line["tensor"] = {"tflops": flops / (attn_ms * 1e-3) / 1e12, "flops_per_launch": flops}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
@@ -359,7 +405,13 @@ def main():
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="workload to time (the bench line is the default one; others are "
+                         "for per-workload tables and profiling)")
+    ap.add_argument("--batch", type=int, default=None, help="override the batch size")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":
