@@ -105,6 +105,48 @@ zl_status gqa_plan(const zl_decode_attn_params* a, GqaPlan* plan) {
   return ZL_OK;
 }
 
+// ------------------------------------------------------------------ MLA plan
+struct MlaPlan {
+  int clusters = 0;
+  size_t off_lse = 0, off_o = 0, bytes = 0;
+};
+
+zl_status mla_validate_shape(const zl_decode_attn_params* a) {
+  if (!a || a->struct_size != sizeof(zl_decode_attn_params)) return ZL_ERR_INVALID_ARG;
+  if (a->B < 1 || a->Hq < 1 || a->Hkv < 1 || a->q_len < 1 || a->page_size < 1 ||
+      a->num_pages < 1 || a->block_table_stride < 1 || a->D_qk < 1 || a->D_v < 1 ||
+      a->num_ctas < 0 || a->max_seq_len < 0)
+    return ZL_ERR_INVALID_ARG;
+  if (!(a->scale > 0.f) || !std::isfinite(a->scale)) return ZL_ERR_INVALID_ARG;
+  if (a->Hkv != 1) return ZL_ERR_INVALID_ARG;
+  if (a->D_qk != zl::kMlaDqk || a->D_v != zl::kMlaDv) return ZL_ERR_UNSUPPORTED;
+  if (a->Hq != zl::kMlaHeads) return ZL_ERR_UNSUPPORTED;
+  if (a->q_len != 1) return ZL_ERR_UNSUPPORTED;
+  if (a->page_size % zl::kMlaTile != 0 || a->page_size > 1024) return ZL_ERR_UNSUPPORTED;
+  if (a->B > zl::kMlaMaxBatch) return ZL_ERR_UNSUPPORTED;
+  return ZL_OK;
+}
+
+zl_status mla_plan(const zl_decode_attn_params* a, MlaPlan* plan) {
+  zl_status st = mla_validate_shape(a);
+  if (st != ZL_OK) return st;
+  DeviceInfo dev;
+  if ((st = current_device(&dev)) != ZL_OK) return st;
+  int clusters = a->num_ctas > 0 ? (a->num_ctas + 1) / 2 : dev.sms / 2;
+  if (a->num_ctas == 0 && a->max_seq_len > 0) {
+    const int64_t tiles =
+        int64_t(a->B) * ((int64_t(a->max_seq_len) + zl::kMlaTile - 1) / zl::kMlaTile);
+    if (tiles < clusters) clusters = int(tiles < 1 ? 1 : tiles);
+  }
+  if (clusters < 1) clusters = 1;
+  plan->clusters = clusters;
+  const size_t rows = size_t(clusters) * 2 * zl::kMlaHeads;
+  plan->off_lse = round_up(size_t(a->B + 1) * sizeof(int32_t), 256);
+  plan->off_o = plan->off_lse + round_up(rows * sizeof(float), 256);
+  plan->bytes = plan->off_o + rows * zl::kMlaDv * sizeof(float);
+  return ZL_OK;
+}
+
 zl_status encode_pool_map(CUtensorMap* map, const void* pool, const zl_decode_attn_params* a,
                           int box_heads) {
   auto encode = tensor_map_encoder();
@@ -203,15 +245,69 @@ zl_status zl_decode_attn(const zl_decode_attn_params* a, zl_stream_t stream) {
 }
 
 zl_status zl_decode_attn_mla_workspace_size(const zl_decode_attn_params* a, size_t* bytes) {
-  (void)a;
-  (void)bytes;
-  return ZL_ERR_UNSUPPORTED;
+  if (!bytes) return ZL_ERR_INVALID_ARG;
+  MlaPlan plan;
+  const zl_status st = mla_plan(a, &plan);
+  if (st != ZL_OK) return st;
+  *bytes = plan.bytes;
+  return ZL_OK;
 }
 
 zl_status zl_decode_attn_mla(const zl_decode_attn_params* a, zl_stream_t stream) {
-  (void)a;
-  (void)stream;
-  return ZL_ERR_UNSUPPORTED;
+  zl_status st = mla_validate_shape(a);
+  if (st != ZL_OK) return st;
+  if ((st = validate_pointers(a, false)) != ZL_OK) return st;
+  MlaPlan plan;
+  if ((st = mla_plan(a, &plan)) != ZL_OK) return st;
+  if (!a->workspace || !aligned(a->workspace, 256) || a->workspace_bytes < plan.bytes)
+    return ZL_ERR_WORKSPACE;
+  auto encode = tensor_map_encoder();
+  if (!encode) return ZL_ERR_CUDA;
+
+  zl::MlaParams p;
+  std::memset(&p, 0, sizeof(p));
+  {
+    const cuuint64_t dims[3] = {cuuint64_t(zl::kMlaDqk), cuuint64_t(a->page_size),
+                                cuuint64_t(a->num_pages)};
+    const cuuint64_t strides[2] = {cuuint64_t(a->token_stride) * 2, cuuint64_t(a->page_stride) * 2};
+    const cuuint32_t box[3] = {64, cuuint32_t(zl::kMlaTile), 1};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    if (encode(&p.tmap_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a->k_pool), dims,
+               strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return ZL_ERR_UNSUPPORTED;
+  }
+  {
+    const cuuint64_t dims[3] = {cuuint64_t(zl::kMlaDqk), cuuint64_t(zl::kMlaHeads),
+                                cuuint64_t(a->B)};
+    const cuuint64_t strides[2] = {cuuint64_t(zl::kMlaDqk) * 2,
+                                   cuuint64_t(zl::kMlaDqk) * zl::kMlaHeads * 2};
+    const cuuint32_t box[3] = {64, cuuint32_t(zl::kMlaHeads), 1};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    if (encode(&p.tmap_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a->q), dims,
+               strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return ZL_ERR_UNSUPPORTED;
+  }
+  p.out = static_cast<__nv_bfloat16*>(a->out);
+  p.lse = a->lse;
+  p.block_table = a->block_table;
+  p.seq_lens = a->seq_lens;
+  p.bt_stride = a->block_table_stride;
+  char* ws = static_cast<char*>(a->workspace);
+  p.ws_prefix = reinterpret_cast<int32_t*>(ws);
+  p.ws_lse = reinterpret_cast<float*>(ws + plan.off_lse);
+  p.ws_o = reinterpret_cast<float*>(ws + plan.off_o);
+  p.err_flags = a->err_flags;
+  p.B = a->B;
+  p.page_size = a->page_size;
+  p.num_pages = a->num_pages;
+  p.scale_log2 = float(double(a->scale) * kLog2e);
+  const cudaError_t e = zl::mla_decode_launch(p, plan.clusters,
+                                              reinterpret_cast<cudaStream_t>(stream),
+                                              reinterpret_cast<cudaEvent_t>(a->attn_begin),
+                                              reinterpret_cast<cudaEvent_t>(a->attn_end));
+  return e == cudaSuccess ? ZL_OK : ZL_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -32,6 +32,34 @@ struct GqaParams {
   float scale_log2;    // scale * log2(e)
 };
 
+constexpr int kMlaTile = 64;       // tokens per MLA tile (page sizes are multiples of it)
+constexpr int kMlaDqk = 576;       // latent 512 + rope 64
+constexpr int kMlaDv = 512;        // V = first 512 latent columns
+constexpr int kMlaHeads = 128;     // query heads (= TMEM lanes)
+constexpr int kMlaMaxBatch = 2048; // sequences per MLA call
+
+// Everything the MLA kernel and its merge kernel read.
+struct MlaParams {
+  CUtensorMap tmap_kv;  // 3-D {576, page_size, num_pages}, box {64, 64, 1}, 128B swizzle
+  CUtensorMap tmap_q;   // 3-D {576, 128, B}, box {64, 128, 1}, 128B swizzle
+  __nv_bfloat16* out;   // [B, 128, 512]
+  float* lse;           // [B, 128] natural log, or nullptr
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int64_t bt_stride;
+  int32_t* ws_prefix;   // [B + 1] tile prefix sums
+  float* ws_o;          // [clusters][2][128][512] normalised partial outputs
+  float* ws_lse;        // [clusters][2][128] base-2 lse of partials (NaN = bad piece)
+  uint32_t* err_flags;
+  int B, page_size, num_pages;
+  float scale_log2;
+};
+
+size_t mla_smem_bytes();
+// Launches `clusters` CTA pairs of the MLA kernel, then its merge kernel.
+cudaError_t mla_decode_launch(const MlaParams& p, int clusters, cudaStream_t stream,
+                              cudaEvent_t attn_begin, cudaEvent_t attn_end);
+
 // kv heads handled by one CTA for this Hkv (largest of 8, 4, 2, 1 dividing it).
 int gqa_heads_per_cta(int Hkv);
 // CTAs of the attention kernel that fit on one SM (0 on error).

@@ -77,3 +77,27 @@ def test_no_cpu_fallback():
         pytest.skip("a GPU is present")
     p = _params()
     assert zl.lib().zl_decode_attn(ctypes.byref(p), None) != zl.OK
+
+
+def _mla_params(**over):
+    p = _params(Hq=128, Hkv=1, D_qk=576, D_v=512, page_size=64, v_pool=None)
+    p.page_stride, p.token_stride, p.head_stride = 64 * 576, 576, 576
+    for k, v in over.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(struct_size=8), zl.ERR_INVALID_ARG),
+    (dict(Hkv=2, Hq=128), zl.ERR_INVALID_ARG),
+    (dict(v_pool=1 << 20), zl.ERR_INVALID_ARG),   # MLA takes V from the latent row
+    (dict(q=None), zl.ERR_INVALID_ARG),
+    (dict(D_qk=512, D_v=512), zl.ERR_UNSUPPORTED),
+    (dict(Hq=64), zl.ERR_UNSUPPORTED),
+    (dict(page_size=16), zl.ERR_UNSUPPORTED),
+    (dict(q_len=2), zl.ERR_UNSUPPORTED),
+    (dict(B=3000), zl.ERR_UNSUPPORTED),
+])
+def test_mla_host_validation(over, code):
+    p = _mla_params(**over)
+    assert zl.lib().zl_decode_attn_mla(ctypes.byref(p), None) == code
