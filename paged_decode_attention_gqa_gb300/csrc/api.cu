@@ -277,18 +277,7 @@ zl_status zl_decode_attn_mla(const zl_decode_attn_params* a, zl_stream_t stream)
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return ZL_ERR_UNSUPPORTED;
   }
-  {
-    const cuuint64_t dims[3] = {cuuint64_t(zl::kMlaDqk), cuuint64_t(zl::kMlaHeads),
-                                cuuint64_t(a->B)};
-    const cuuint64_t strides[2] = {cuuint64_t(zl::kMlaDqk) * 2,
-                                   cuuint64_t(zl::kMlaDqk) * zl::kMlaHeads * 2};
-    const cuuint32_t box[3] = {64, cuuint32_t(zl::kMlaHeads), 1};
-    const cuuint32_t elem[3] = {1, 1, 1};
-    if (encode(&p.tmap_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a->q), dims,
-               strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return ZL_ERR_UNSUPPORTED;
-  }
+  p.q = static_cast<const __nv_bfloat16*>(a->q);
   p.out = static_cast<__nv_bfloat16*>(a->out);
   p.lse = a->lse;
   p.block_table = a->block_table;

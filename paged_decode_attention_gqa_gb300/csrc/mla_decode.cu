@@ -36,30 +36,36 @@ constexpr uint32_t kErrBadPage = 1u;
 constexpr uint32_t kErrBadLen = 2u;
 constexpr uint32_t kErrTimeout = 4u;
 
-constexpr int kTile = kMlaTile;               // tokens per tile (= page size granule)
+constexpr int kTile = kMlaTile;               // tokens per tile
 constexpr int kRows = 128;                    // query heads = TMEM lanes
-constexpr int kBoxQ = kRows * 128;            // 16 KB: 128 rows x 64 bf16
-constexpr int kBoxKV = kTile * 128;           // 8 KB: 64 tokens x 64 bf16
+constexpr int kBoxKV = kTile * 128;           // 4 KB: 32 tokens x 64 bf16
 constexpr int kMaxBoxes = 5;                  // rank 0: 4 latent + 1 rope
-constexpr int kStages = 2;
-constexpr int kStageBytes = kMaxBoxes * kBoxKV;  // 40 KB
-constexpr int kXStride = 64 * 4 + 16;            // exchange row (padded against bank conflicts)
-constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + kMaxBoxes * kBoxQ;
+constexpr int kStages = 6;
+constexpr int kStageBytes = kMaxBoxes * kBoxKV;  // 20 KB
+constexpr int kSBufs = 3;                        // S buffers in TMEM (QK runs up to 2 tiles ahead)
+constexpr int kPBytes = kRows * kTile * 2;       // 8 KB: P tile, 64-byte rows
+constexpr int kXBytes = kRows * kTile * 4;       // 16 KB: fp32 partial scores, 128-byte rows
+constexpr int kOffKV = 0;
 constexpr int kOffP = kOffKV + kStages * kStageBytes;
-constexpr int kOffX = kOffP + kRows * 128;
-constexpr int kOffBar = kOffX + kRows * kXStride;
+constexpr int kOffX = kOffP + 2 * kPBytes;       // received partials (double buffer)
+constexpr int kOffStg = kOffX + 2 * kXBytes;     // outgoing partials (double buffer)
+constexpr int kOffBar = kOffStg + 2 * kXBytes;
 enum : int {
-  B_Q_FULL = 0, B_Q_EMPTY, B_KV_FULL0, B_KV_FULL1, B_KV_EMPTY0, B_KV_EMPTY1, B_S_FULL0,
-  B_S_FULL1, B_S_EMPTY0, B_S_EMPTY1, B_P_FULL, B_PV_DONE, B_X_FULL, B_X_FREE, B_FINAL, B_COUNT
+  B_Q_FULL = 0,
+  B_KV_FULL0, B_KV_EMPTY0 = B_KV_FULL0 + kStages, B_S_FULL0 = B_KV_EMPTY0 + kStages,
+  B_S_EMPTY0 = B_S_FULL0 + kSBufs, B_P_FULL0 = B_S_EMPTY0 + kSBufs, B_PV_DONE0 = B_P_FULL0 + 2,
+  B_X_FULL0 = B_PV_DONE0 + 2, B_STAGED0 = B_X_FULL0 + 2, B_FINAL = B_STAGED0 + 2, B_COUNT
 };
-constexpr int kOffMisc = kOffBar + 8 * 16;
+constexpr int kOffMisc = kOffBar + 8 * B_COUNT;
 constexpr int kOffPrefix = kOffMisc + 64;
 constexpr size_t kSmemBytes = 1024 + kOffPrefix + size_t(kMlaMaxBatch + 1) * 4;
 static_assert(kSmemBytes <= 232448, "MLA kernel exceeds 227 KB of shared memory");
+static_assert(kOffP % 1024 == 0 && kOffKV % 1024 == 0, "swizzle atoms need aligned buffers");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;    // O half: columns [0, 256)
-constexpr uint32_t kTmemS = 256;  // S buffers: [256, 320) and [320, 384)
+constexpr uint32_t kTmemS = 256;  // S buffers: kSBufs x kTile columns from 256
+constexpr uint32_t kTmemQ = kTmemS + kSBufs * kTile;  // Q (this rank's columns), bf16 pairs
+static_assert(kTmemQ + 160 <= 512, "TMEM holds O, S buffers and Q");
 constexpr int kThreads = 192;
 
 __device__ __forceinline__ void raise_error(uint32_t* flags, uint32_t bits) {
@@ -94,18 +100,21 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
   const int64_t cap = p.bt_stride * int64_t(p.page_size);
 
   if (tid == 0) {
-    mbar_init(bar(B_Q_FULL), 1);
-    mbar_init(bar(B_Q_EMPTY), 1);
+    mbar_init(bar(B_Q_FULL), kRows);  // softmax threads wrote this piece's Q into TMEM
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(B_KV_FULL0 + s), 1);
       mbar_init(bar(B_KV_EMPTY0 + s), 1);
-      mbar_init(bar(B_S_FULL0 + s), 1);
-      mbar_init(bar(B_S_EMPTY0 + s), kRows);
     }
-    mbar_init(bar(B_P_FULL), kRows);
-    mbar_init(bar(B_PV_DONE), 1);
-    mbar_init(bar(B_X_FULL), kRows);
-    mbar_init(bar(B_X_FREE), kRows);
+    for (int i = 0; i < kSBufs; ++i) {
+      mbar_init(bar(B_S_FULL0 + i), 1);
+      mbar_init(bar(B_S_EMPTY0 + i), kRows);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(B_P_FULL0 + i), kRows);
+      mbar_init(bar(B_PV_DONE0 + i), 1);
+      mbar_init(bar(B_X_FULL0 + i), 1);      // local expect_tx + the peer's bulk-copy bytes
+      mbar_init(bar(B_STAGED0 + i), kRows);  // all rows of the outgoing partial written
+    }
     mbar_init(bar(B_FINAL), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -116,7 +125,6 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&p.tmap_kv);
-    tma_prefetch_desc(&p.tmap_q);
   }
   // Tiles (of 64 tokens) per sequence, exclusive prefix sum.
   if (warp == 2) {
@@ -165,21 +173,15 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int it = 0, piece = 0;
+      int it = 0;
       bool ok = true;
       for (int64_t idx = s_c; idx < e_c && ok;) {
         const int b = locate(prefix, B, idx);
         const int j0 = int(idx - prefix[b]);
         const int64_t pend = min(e_c, int64_t(prefix[b + 1]));
-        if (!mbar_wait(bar(B_Q_EMPTY), (piece & 1) ^ 1u, abort_flag)) { ok = false; break; }
-        mbar_arrive_expect_tx(bar(B_Q_FULL), nbox * kBoxQ);
-        for (int i = 0; i < nbox; ++i) {
-          const int col = i < 4 ? int(rank) * 256 + 64 * i : 512;
-          tma_load_3d(sbase + kOffQ + i * kBoxQ, &p.tmap_q, bar(B_Q_FULL), col, 0, b);
-        }
         for (int j = j0; j < j0 + int(pend - idx); ++j, ++it) {
-          const int s = it & 1;
-          if (!mbar_wait(bar(B_KV_EMPTY0 + s), ((it >> 1) & 1) ^ 1u, abort_flag)) {
+          const int s = it % kStages;
+          if (!mbar_wait(bar(B_KV_EMPTY0 + s), ((it / kStages) & 1) ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
@@ -197,7 +199,6 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
             }
           }
         }
-        ++piece;
         idx = pend;
       }
       if (!ok) {
@@ -207,65 +208,79 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       // Leave no copy in flight: wait for the last stages and the last Q.
       const volatile int never = 0;
       for (int j = (it > kStages ? it - kStages : 0); j < it; ++j)
-        mbar_wait(bar(B_KV_FULL0 + (j & 1)), (j >> 1) & 1, &never);
-      if (piece > 0) mbar_wait(bar(B_Q_FULL), (piece - 1) & 1, &never);
+        mbar_wait(bar(B_KV_FULL0 + j % kStages), (j / kStages) & 1, &never);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // An event loop: issue whichever is ready first, QK of the next tile (its
+    // K/V staged and an S buffer free, up to kSBufs tiles ahead) or PV of the
+    // oldest tile whose P is written.
     if (lane == 0) {
       const uint32_t idesc_qk = umma_idesc_bf16(kRows, kTile, false);
       const uint32_t idesc_pv = umma_idesc_bf16(kRows, 256, true);
-      int it = 0, piece = 0, pending = -1;
-      bool pending_first = false, ok = true;
-      auto issue_pv = [&](int j, bool first) -> bool {
-        if (!mbar_wait(bar(B_P_FULL), j & 1, abort_flag)) return false;
-        tc_fence_after();
-        const int s = j & 1;
-        const uint32_t vbase = sbase + kOffKV + s * kStageBytes;
+      const int total = int(e_c - s_c);
+      int qk = 0, pv = 0, qpiece = 0;
+      bool ok = true;
+      uint64_t last_progress = globaltimer_ns();
+      while (pv < total && ok) {
+        bool progressed = false;
+        if (qk < total) {
+          const int64_t idx = s_c + qk;
+          const int b = locate(prefix, B, idx);
+          const bool first = (qk == 0) || (idx == prefix[b]);
+          const bool last = (qk == total - 1) || (idx + 1 == prefix[b + 1]);
+          const int s = qk % kStages, sb = qk % kSBufs;
+          if (mbar_test(bar(B_KV_FULL0 + s), (qk / kStages) & 1) &&
+              mbar_test(bar(B_S_EMPTY0 + sb), ((qk / kSBufs) & 1) ^ 1u) &&
+              (!first || mbar_test(bar(B_Q_FULL), qpiece & 1))) {
+            tc_fence_after();
+            const uint32_t kvbase = sbase + kOffKV + s * kStageBytes;
+            // S = Q K^T: A = Q from TMEM (16 dims = 8 columns per step), B = K
+            // K-major with the 128-byte swizzle.
+            for (int i = 0; i < nbox; ++i) {
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint64_t a = umma_smem_desc(sbase + kOffP + kk * 32, 0, 1024, 2);
-          const uint64_t bdesc = umma_smem_desc(vbase + kk * 16 * 128, kBoxKV, 1024, 2);
-          umma_bf16(tmem + kTmemO, a, bdesc, idesc_pv, (first && kk == 0) ? 0u : 1u);
-        }
-        umma_commit(bar(B_KV_EMPTY0 + s));
-        umma_commit(bar(B_PV_DONE));
-        return true;
-      };
-      for (int64_t idx = s_c; idx < e_c && ok;) {
-        const int b = locate(prefix, B, idx);
-        const int64_t pend = min(e_c, int64_t(prefix[b + 1]));
-        const int ntiles = int(pend - idx);
-        if (!mbar_wait(bar(B_Q_FULL), piece & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        for (int t = 0; t < ntiles; ++t, ++it) {
-          const int s = it & 1;
-          const uint32_t ph = (it >> 1) & 1;
-          if (!mbar_wait(bar(B_KV_FULL0 + s), ph, abort_flag) ||
-              !mbar_wait(bar(B_S_EMPTY0 + s), ph ^ 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t kvbase = sbase + kOffKV + s * kStageBytes;
-          for (int i = 0; i < nbox; ++i) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t a = umma_smem_desc(sbase + kOffQ + i * kBoxQ + kk * 32, 0, 1024, 2);
-              const uint64_t bdesc = umma_smem_desc(kvbase + i * kBoxKV + kk * 32, 0, 1024, 2);
-              umma_bf16(tmem + kTmemS + 64 * s, a, bdesc, idesc_qk, (i | kk) ? 1u : 0u);
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t bdesc = umma_smem_desc(kvbase + i * kBoxKV + kk * 32, 0, 1024, 2);
+                umma_bf16_tmem_a(tmem + kTmemS + kTile * sb, tmem + kTmemQ + 32 * i + 8 * kk, bdesc,
+                                 idesc_qk, (i | kk) ? 1u : 0u);
+              }
             }
+            umma_commit(bar(B_S_FULL0 + sb));
+            if (last) ++qpiece;
+            ++qk;
+            progressed = true;
           }
-          umma_commit(bar(B_S_FULL0 + s));
-          if (t == ntiles - 1) umma_commit(bar(B_Q_EMPTY));
-          if (pending >= 0 && !issue_pv(pending, pending_first)) { ok = false; break; }
-          pending = it;
-          pending_first = (t == 0);  // first PV of a piece overwrites O
         }
-        ++piece;
-        idx = pend;
+        if (pv < qk) {
+          const int pb = pv & 1;
+          if (mbar_test(bar(B_P_FULL0 + pb), (pv >> 1) & 1)) {
+            const int64_t idx = s_c + pv;
+            const int b = locate(prefix, B, idx);
+            const bool first = (pv == 0) || (idx == prefix[b]);  // overwrite O
+            tc_fence_after();
+            // O[:, rank half] (+)= P V: A = P, K-major with the 64-byte swizzle
+            // (8-row atoms of 512 B); B = V, MN-major with the 128-byte swizzle
+            // (8-token groups 1 KB apart, the next 64 columns in the next box).
+            const int s = pv % kStages;
+            const uint32_t vbase = sbase + kOffKV + s * kStageBytes;
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk) {
+              const uint64_t a = umma_smem_desc(sbase + kOffP + pb * kPBytes + kk * 32, 0, 512, 4);
+              const uint64_t bdesc = umma_smem_desc(vbase + kk * 16 * 128, kBoxKV, 1024, 2);
+              umma_bf16(tmem + kTmemO, a, bdesc, idesc_pv, (first && kk == 0) ? 0u : 1u);
+            }
+            umma_commit(bar(B_KV_EMPTY0 + s));
+            umma_commit(bar(B_PV_DONE0 + pb));
+            ++pv;
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          last_progress = globaltimer_ns();
+        } else if (*abort_flag || globaltimer_ns() - last_progress > kWaitTimeoutNs) {
+          ok = false;
+        }
       }
-      if (ok && pending >= 0 && !issue_pv(pending, pending_first)) ok = false;
       if (!ok) {
         raise_error(p.err_flags, kErrTimeout);
         *abort_flag = 1;
@@ -281,13 +296,69 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     const int row = 32 * q4 + lane;                 // query head = TMEM lane
     const uint32_t tl = tmem + (uint32_t(32 * q4) << 16);
     const float c = p.scale_log2;
-    const uint32_t my_x = sbase + kOffX + row * kXStride;
-    const uint32_t peer_x = mapa_shared(my_x, peer);
-    const uint32_t peer_xfull = mapa_shared(bar(B_X_FULL), peer);
-    const uint32_t peer_xfree = mapa_shared(bar(B_X_FREE), peer);
+    const uint32_t peer_x = mapa_shared(sbase + kOffX, peer);
+    const uint32_t peer_xfull = mapa_shared(bar(B_X_FULL0), peer);
     const int stid = tid - 64;                       // 0..127 within the softmax group
+    const int total = int(e_c - s_c);                // tiles of this cluster
+    const uint32_t swz = uint32_t(row & 7);          // 16-byte chunk swizzle of this row
+
+    // send(j): this rank's partial scores of tile j. The rows go to the local
+    // staging buffer j & 1; once all 128 are there, one thread bulk-copies the
+    // 16 KB into the peer's receive buffer j & 1, crediting the bytes to the
+    // peer's X_FULL barrier. No flow-control barrier is needed: the peer sends
+    // tile j + 2 into our buffer only after receiving our tile j + 1, which we
+    // send after reading tile j; and our staging buffer j & 1 is rewritten only
+    // after the peer's tile j + 1 reached us, which it sent after receiving j.
+    auto send = [&](int j, uint32_t (&sv)[kTile]) -> bool {
+      const int sb = j % kSBufs, xb = j & 1;
+      if (!mbar_wait(bar(B_S_FULL0 + sb), (j / kSBufs) & 1, abort_flag)) return false;
+      tc_fence_after();
+      tmem_ld32(tl + kTmemS + kTile * sb, sv);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar(B_S_EMPTY0 + sb));
+      const uint32_t dst = sbase + kOffStg + xb * kXBytes + row * 128;
+#pragma unroll
+      for (int k = 0; k < kTile / 4; ++k)
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst + ((k ^ swz) << 4)),
+                     "r"(sv[4 * k]), "r"(sv[4 * k + 1]), "r"(sv[4 * k + 2]), "r"(sv[4 * k + 3])
+                     : "memory");
+      fence_proxy_async_smem();
+      mbar_arrive(bar(B_STAGED0 + xb));
+      if (stid == 0) {
+        if (!mbar_wait(bar(B_STAGED0 + xb), (j >> 1) & 1, abort_flag)) return false;
+        bulk_copy_to_peer(peer_x + xb * kXBytes, sbase + kOffStg + xb * kXBytes, kXBytes,
+                          peer_xfull + 8 * xb);
+      }
+      return true;
+    };
+
+    // Q of sequence b (this rank's columns, 2 bf16 per 32-bit column) into
+    // TMEM, one head row per thread; the MMA issuer waits on Q_FULL.
+    auto load_q = [&](int b) {
+      const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (int64_t(b) * kRows + row) * kMlaDqk);
+      for (int i = 0; i < nbox; ++i) {
+        const int col = i < 4 ? int(rank) * 256 + 64 * i : 512;
+        uint32_t v[32];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint4 u = __ldg(qrow + col / 8 + k);
+          v[4 * k] = u.x;
+          v[4 * k + 1] = u.y;
+          v[4 * k + 2] = u.z;
+          v[4 * k + 3] = u.w;
+        }
+        tmem_st32(tl + kTmemQ + 32 * i, v);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(B_Q_FULL));
+    };
+
+    uint32_t sv_cur[kTile], sv_nxt[kTile];
+    if (total > 0) load_q(locate(prefix, B, s_c));
+    bool ok = total == 0 || send(0, sv_cur);
     int it = 0;
-    bool ok = true;
     for (int64_t idx = s_c; idx < e_c && ok;) {
       const int b = locate(prefix, B, idx);
       const int j0 = int(idx - prefix[b]);
@@ -296,56 +367,43 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       const bool partial = (j0 > 0) || (pend < prefix[b + 1]);
       const int slot = (idx == s_c) ? 0 : 1;
       const int L = p.seq_lens[b];
+      const int32_t* bt_row = p.block_table + int64_t(b) * p.bt_stride;
       float m_used = -CUDART_INF_F, l = 0.f;
       int bad = 0;
+      int page_cur = bt_row[(j0 * kTile) / p.page_size];
       for (int t = 0; t < ntiles; ++t, ++it) {
-        const int s = it & 1;
+        const int pb = it & 1;                       // P and exchange buffers
         const uint32_t ph = (it >> 1) & 1;
         const int tok0 = (j0 + t) * kTile;
         const int valid = min(kTile, L - tok0);
-        const int page = p.block_table[int64_t(b) * p.bt_stride + tok0 / p.page_size];
-        bad |= (page < 0 || page >= p.num_pages) ? 1 : 0;
+        // block-table entry of the next tile, loaded one tile ahead
+        const int page_nxt = (t + 1 < ntiles) ? bt_row[(tok0 + kTile) / p.page_size] : 0;
+        bad |= (page_cur < 0 || page_cur >= p.num_pages) ? 1 : 0;
 
-        // my partial scores for this tile
-        if (!mbar_wait(bar(B_S_FULL0 + s), ph, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        uint32_t sv[64];
+        // receive the peer's partial of this tile and sum
+        if (stid == 0) mbar_arrive_expect_tx(bar(B_X_FULL0 + pb), kXBytes);
+        if (!mbar_wait_cluster(bar(B_X_FULL0 + pb), ph, abort_flag)) { ok = false; break; }
+        float x[kTile];
         {
-          uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
-          uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
-          tmem_ld32(tl + kTmemS + 64 * s, lo);
-          tmem_ld32(tl + kTmemS + 64 * s + 32, hi);
-          tmem_wait_ld();
-        }
-        tc_fence_before();
-        mbar_arrive(bar(B_S_EMPTY0 + s));
-
-        // swap partials with the peer through distributed shared memory
-        if (!mbar_wait_cluster(bar(B_X_FREE), (it & 1) ^ 1u, abort_flag)) { ok = false; break; }
+          const uint32_t src = sbase + kOffX + pb * kXBytes + row * 128;
 #pragma unroll
-        for (int k = 0; k < 16; ++k)
-          st_cluster_v4(peer_x + 16 * k, __uint_as_float(sv[4 * k]), __uint_as_float(sv[4 * k + 1]),
-                        __uint_as_float(sv[4 * k + 2]), __uint_as_float(sv[4 * k + 3]));
-        mbar_arrive_remote(peer_xfull);
-        if (!mbar_wait_cluster(bar(B_X_FULL), it & 1, abort_flag)) { ok = false; break; }
-        float x[64];
-        {
-          const float4* mine = reinterpret_cast<const float4*>(smem + kOffX + row * kXStride);
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const float4 v = mine[k];
-            x[4 * k] = __uint_as_float(sv[4 * k]) + v.x;
-            x[4 * k + 1] = __uint_as_float(sv[4 * k + 1]) + v.y;
-            x[4 * k + 2] = __uint_as_float(sv[4 * k + 2]) + v.z;
-            x[4 * k + 3] = __uint_as_float(sv[4 * k + 3]) + v.w;
+          for (int k = 0; k < kTile / 4; ++k) {
+            float v0, v1, v2, v3;
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(v0), "=f"(v1), "=f"(v2), "=f"(v3)
+                         : "r"(src + ((k ^ swz) << 4))
+                         : "memory");
+            x[4 * k] = __uint_as_float(sv_cur[4 * k]) + v0;
+            x[4 * k + 1] = __uint_as_float(sv_cur[4 * k + 1]) + v1;
+            x[4 * k + 2] = __uint_as_float(sv_cur[4 * k + 2]) + v2;
+            x[4 * k + 3] = __uint_as_float(sv_cur[4 * k + 3]) + v3;
           }
         }
-        mbar_arrive_remote(peer_xfree);
 
         // online softmax (base 2); the max moves only when it grows by > 8
         float mx = -CUDART_INF_F;
 #pragma unroll
-        for (int k = 0; k < 64; ++k) {
+        for (int k = 0; k < kTile; ++k) {
           x[k] = (k < valid) ? x[k] * c : -CUDART_INF_F;
           mx = fmaxf(mx, x[k]);
         }
@@ -358,10 +416,10 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
           m_used = mx;
           rescale = true;
         }
-        uint32_t pk[32];
+        uint32_t pk[kTile / 2];
         float lsum = 0.f;
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
+        for (int k = 0; k < kTile / 2; ++k) {
           pk[k] = pack_bf16x2(ex2_approx(x[2 * k] - m_used), ex2_approx(x[2 * k + 1] - m_used));
           const float2 f = unpack_bf16x2(pk[k]);
           lsum += f.x + f.y;
@@ -370,7 +428,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
 
         // tail tile: zero the V rows past the end (NaN there would poison 0 * V)
         if (valid < kTile) {
-          const uint32_t vb = sbase + kOffKV + s * kStageBytes;
+          const uint32_t vb = sbase + kOffKV + (it % kStages) * kStageBytes;
           const int nz = (kTile - valid) * 4 * 8;  // 16-byte chunks in 4 latent boxes
           for (int z = stid; z < nz; z += kRows) {
             const int chunk = z & 7, box = (z >> 3) & 3, r = valid + (z >> 5);
@@ -381,12 +439,23 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
           }
         }
 
-        // P buffer and O are free once the previous PV finished
-        if (it > 0 && !mbar_wait(bar(B_PV_DONE), (it - 1) & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
+        // send the next tile's partial (its QK ran while this tile was summed);
+        // a new sequence first needs its Q in TMEM (every QK of this one is done:
+        // this tile's S was read above)
+        if (it + 1 < total && t + 1 == ntiles) load_q(locate(prefix, B, s_c + it + 1));
+        if (it + 1 < total && !send(it + 1, sv_nxt)) { ok = false; break; }
+
+        // P buffer pb is free once PV(it - 2) finished; a rescale of O also
+        // needs PV(it - 1) finished.
+        if (it >= 2 && !mbar_wait(bar(B_PV_DONE0 + pb), ph ^ 1u, abort_flag)) { ok = false; break; }
         // tcgen05.ld/st are warp-wide: rescale when any row of the warp needs it
         // (rows that do not need it multiply by exactly 1).
         if (__any_sync(0xffffffffu, rescale)) {
+          if (it >= 1 && !mbar_wait(bar(B_PV_DONE0 + (pb ^ 1)), ((it - 1) >> 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll 1
           for (int cc = 0; cc < 8; ++cc) {
             uint32_t o[32];
@@ -398,24 +467,31 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
           }
           tmem_wait_st();
         }
-        // P row: 64 bf16 in the 128-byte-swizzled K-major layout of the A operand
+        // P row: kTile bf16 = 64 bytes, K-major with the 64-byte swizzle
+        // (16-byte chunk c of row r lands at chunk c ^ ((r >> 1) & 3)).
         {
-          const uint32_t prow = sbase + kOffP + row * 128;
+          const uint32_t prow = sbase + kOffP + pb * kPBytes + row * 64;
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
+          for (int k = 0; k < 4; ++k)
             asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
-                             prow + ((k ^ (row & 7)) << 4)),
+                             prow + ((k ^ ((row >> 1) & 3)) << 4)),
                          "r"(pk[4 * k]), "r"(pk[4 * k + 1]), "r"(pk[4 * k + 2]), "r"(pk[4 * k + 3])
                          : "memory");
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(bar(B_P_FULL));
+        mbar_arrive(bar(B_P_FULL0 + pb));
+#pragma unroll
+        for (int k = 0; k < kTile; ++k) sv_cur[k] = sv_nxt[k];
+        page_cur = page_nxt;
       }
       if (!ok) break;
 
       // ---- epilogue of the piece: O / l
-      if (!mbar_wait(bar(B_PV_DONE), (it - 1) & 1, abort_flag)) { ok = false; break; }
+      if (!mbar_wait(bar(B_PV_DONE0 + ((it - 1) & 1)), ((it - 1) >> 1) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       if (bad && stid == 0) raise_error(p.err_flags, kErrBadPage);
       const float inv = bad ? 0.f : 1.f / l;

@@ -298,3 +298,62 @@ __device__ __forceinline__ void tmem_wait_st() {
 }
 
 }  // namespace zl
+
+namespace zl {
+
+// Store 16 bytes into another CTA's shared memory and credit those bytes to an
+// mbarrier of that CTA (transaction-count completion, no separate arrive).
+__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint32_t a, uint32_t b,
+                                            uint32_t c, uint32_t d, uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+          remote_addr),
+      "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar)
+      : "memory");
+}
+
+}  // namespace zl
+
+namespace zl {
+
+// Non-blocking probe of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Bulk copy from this CTA's shared memory into another CTA's shared memory of
+// the cluster; the bytes are credited to an mbarrier of the destination CTA.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src,
+                                                  uint32_t bytes, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst_cluster),
+      "r"(src), "r"(bytes), "r"(bar_cluster)
+      : "memory");
+}
+
+}  // namespace zl
+
+namespace zl {
+
+// D[tmem] (+)= A[tmem] * B[smem]: A (M rows = TMEM lanes, K-major, two bf16
+// per 32-bit column) read from tensor memory, issued by one thread.
+__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+}  // namespace zl

@@ -95,6 +95,7 @@ def _mla_params(**over):
     (dict(D_qk=512, D_v=512), zl.ERR_UNSUPPORTED),
     (dict(Hq=64), zl.ERR_UNSUPPORTED),
     (dict(page_size=16), zl.ERR_UNSUPPORTED),
+    (dict(page_size=48), zl.ERR_UNSUPPORTED),
     (dict(q_len=2), zl.ERR_UNSUPPORTED),
     (dict(B=3000), zl.ERR_UNSUPPORTED),
 ])
