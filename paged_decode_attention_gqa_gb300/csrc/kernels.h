@@ -32,7 +32,7 @@ struct GqaParams {
   float scale_log2;    // scale * log2(e)
 };
 
-constexpr int kMlaTile = 32;       // tokens per MLA tile (page sizes are multiples of it)
+constexpr int kMlaTile = 64;       // tokens per MLA tile (page sizes are multiples of it)
 constexpr int kMlaDqk = 576;       // latent 512 + rope 64
 constexpr int kMlaDv = 512;        // V = first 512 latent columns
 constexpr int kMlaHeads = 128;     // query heads (= TMEM lanes)
@@ -40,7 +40,7 @@ constexpr int kMlaMaxBatch = 1024; // sequences per MLA call
 
 // Everything the MLA kernel and its merge kernel read.
 struct MlaParams {
-  CUtensorMap tmap_kv;  // 3-D {576, page_size, num_pages}, box {64, 32, 1}, 128B swizzle
+  CUtensorMap tmap_kv;  // 3-D {576, page_size, num_pages}, box {64, 64, 1}, 128B swizzle
   const __nv_bfloat16* q;  // [B, 128, 576]
   __nv_bfloat16* out;   // [B, 128, 512]
   float* lse;           // [B, 128] natural log, or nullptr

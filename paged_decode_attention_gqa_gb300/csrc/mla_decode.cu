@@ -19,8 +19,9 @@
 // 256 columns of O = P V in TMEM (N = 256, V read MN-major straight from the
 // tile it loaded). Every K/V byte leaves HBM once.
 //
-// Warp roles (192 threads): warp 0 TMA producer, warp 1 MMA issuer (and TMEM
-// owner), warps 2-5 softmax / epilogue, one thread per head row (TMEM lane).
+// Warp roles (224 threads): warp 0 TMA producer, warp 1 MMA issuer (and TMEM
+// owner), warps 2-5 softmax / epilogue, one thread per head row (TMEM lane),
+// warp 6 releases the exchange buffer to the peer.
 // The running max is only moved when it grows by more than 2^8, so O in TMEM
 // is rarely rescaled (P <= 256 meanwhile).
 #include "kernels.h"
@@ -40,33 +41,34 @@ constexpr int kTile = kMlaTile;               // tokens per tile
 constexpr int kRows = 128;                    // query heads = TMEM lanes
 constexpr int kBoxKV = kTile * 128;           // 4 KB: 32 tokens x 64 bf16
 constexpr int kMaxBoxes = 5;                  // rank 0: 4 latent + 1 rope
-constexpr int kStages = 6;
-constexpr int kStageBytes = kMaxBoxes * kBoxKV;  // 20 KB
-constexpr int kSBufs = 3;                        // S buffers in TMEM (QK runs up to 2 tiles ahead)
-constexpr int kPBytes = kRows * kTile * 2;       // 8 KB: P tile, 64-byte rows
-constexpr int kXBytes = kRows * kTile * 4;       // 16 KB: fp32 partial scores, 128-byte rows
+constexpr int kStages = 3;
+constexpr int kStageBytes = kMaxBoxes * kBoxKV;  // 40 KB
+constexpr int kXRow = kTile * 4;                 // 256 B: one row of fp32 partial scores
+constexpr int kXBytes = kRows * kXRow;           // 32 KB
 constexpr int kOffKV = 0;
-constexpr int kOffP = kOffKV + kStages * kStageBytes;
-constexpr int kOffX = kOffP + 2 * kPBytes;       // received partials (double buffer)
-constexpr int kOffStg = kOffX + 2 * kXBytes;     // outgoing partials (double buffer)
+constexpr int kOffX = kOffKV + kStages * kStageBytes;  // received partials (single buffer)
+constexpr int kOffStg = kOffX + kXBytes;               // own partials (double buffer)
 constexpr int kOffBar = kOffStg + 2 * kXBytes;
 enum : int {
   B_Q_FULL = 0,
-  B_KV_FULL0, B_KV_EMPTY0 = B_KV_FULL0 + kStages, B_S_FULL0 = B_KV_EMPTY0 + kStages,
-  B_S_EMPTY0 = B_S_FULL0 + kSBufs, B_P_FULL0 = B_S_EMPTY0 + kSBufs, B_PV_DONE0 = B_P_FULL0 + 2,
-  B_X_FULL0 = B_PV_DONE0 + 2, B_STAGED0 = B_X_FULL0 + 2, B_FINAL = B_STAGED0 + 2, B_COUNT
+  B_KV_FULL0, B_KV_EMPTY0 = B_KV_FULL0 + kStages, B_S_FULL = B_KV_EMPTY0 + kStages,
+  B_S_EMPTY, B_P_FULL, B_PV_DONE, B_X_FULL, B_X_FREE, B_READ_DONE, B_STAGED0,
+  B_FINAL = B_STAGED0 + 2,
+  B_COUNT
 };
 constexpr int kOffMisc = kOffBar + 8 * B_COUNT;
 constexpr int kOffPrefix = kOffMisc + 64;
 constexpr size_t kSmemBytes = 1024 + kOffPrefix + size_t(kMlaMaxBatch + 1) * 4;
 static_assert(kSmemBytes <= 232448, "MLA kernel exceeds 227 KB of shared memory");
-static_assert(kOffP % 1024 == 0 && kOffKV % 1024 == 0, "swizzle atoms need aligned buffers");
+static_assert(kOffKV % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle atoms need aligned buffers");
+// TMEM columns (fp32 or bf16 pairs), 128 lanes = 128 heads:
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 0;    // O half: columns [0, 256)
-constexpr uint32_t kTmemS = 256;  // S buffers: kSBufs x kTile columns from 256
-constexpr uint32_t kTmemQ = kTmemS + kSBufs * kTile;  // Q (this rank's columns), bf16 pairs
-static_assert(kTmemQ + 160 <= 512, "TMEM holds O, S buffers and Q");
-constexpr int kThreads = 192;
+constexpr uint32_t kTmemO = 0;                // O, this rank's 256 columns of D_v
+constexpr uint32_t kTmemS = 256;              // S tile: kTile fp32 columns
+constexpr uint32_t kTmemP = kTmemS + kTile;   // P tile: kTile bf16 = kTile / 2 columns
+constexpr uint32_t kTmemQ = kTmemP + kTile / 2;  // Q, this rank's 320 or 256 dims
+static_assert(kTmemQ + 160 <= kTmemCols, "TMEM holds O, S, P and Q");
+constexpr int kThreads = 224;  // producer, MMA, 4 softmax warps, exchange warp
 
 __device__ __forceinline__ void raise_error(uint32_t* flags, uint32_t bits) {
   if (flags) atomicOr(flags, bits);
@@ -105,16 +107,15 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       mbar_init(bar(B_KV_FULL0 + s), 1);
       mbar_init(bar(B_KV_EMPTY0 + s), 1);
     }
-    for (int i = 0; i < kSBufs; ++i) {
-      mbar_init(bar(B_S_FULL0 + i), 1);
-      mbar_init(bar(B_S_EMPTY0 + i), kRows);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(B_P_FULL0 + i), kRows);
-      mbar_init(bar(B_PV_DONE0 + i), 1);
-      mbar_init(bar(B_X_FULL0 + i), 1);      // local expect_tx + the peer's bulk-copy bytes
+    mbar_init(bar(B_S_FULL), 1);
+    mbar_init(bar(B_S_EMPTY), kRows);
+    mbar_init(bar(B_P_FULL), kRows);
+    mbar_init(bar(B_PV_DONE), 1);
+    mbar_init(bar(B_X_FULL), 1);      // local expect_tx + the peer's bulk-copy bytes
+    mbar_init(bar(B_X_FREE), 1);      // the peer has read our previous partial
+    mbar_init(bar(B_READ_DONE), kRows);  // all rows of the received partial read
+    for (int i = 0; i < 2; ++i)
       mbar_init(bar(B_STAGED0 + i), kRows);  // all rows of the outgoing partial written
-    }
     mbar_init(bar(B_FINAL), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -213,7 +214,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // An event loop: issue whichever is ready first, QK of the next tile (its
-    // K/V staged and an S buffer free, up to kSBufs tiles ahead) or PV of the
+    // K/V staged and the S tile read out by the softmax warps) or PV of the
     // oldest tile whose P is written.
     if (lane == 0) {
       const uint32_t idesc_qk = umma_idesc_bf16(kRows, kTile, false);
@@ -229,9 +230,9 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
           const int b = locate(prefix, B, idx);
           const bool first = (qk == 0) || (idx == prefix[b]);
           const bool last = (qk == total - 1) || (idx + 1 == prefix[b + 1]);
-          const int s = qk % kStages, sb = qk % kSBufs;
+          const int s = qk % kStages;
           if (mbar_test(bar(B_KV_FULL0 + s), (qk / kStages) & 1) &&
-              mbar_test(bar(B_S_EMPTY0 + sb), ((qk / kSBufs) & 1) ^ 1u) &&
+              mbar_test(bar(B_S_EMPTY), (qk & 1) ^ 1u) &&
               (!first || mbar_test(bar(B_Q_FULL), qpiece & 1))) {
             tc_fence_after();
             const uint32_t kvbase = sbase + kOffKV + s * kStageBytes;
@@ -241,39 +242,36 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
                 const uint64_t bdesc = umma_smem_desc(kvbase + i * kBoxKV + kk * 32, 0, 1024, 2);
-                umma_bf16_tmem_a(tmem + kTmemS + kTile * sb, tmem + kTmemQ + 32 * i + 8 * kk, bdesc,
-                                 idesc_qk, (i | kk) ? 1u : 0u);
+                umma_bf16_tmem_a(tmem + kTmemS, tmem + kTmemQ + 32 * i + 8 * kk, bdesc, idesc_qk,
+                                 (i | kk) ? 1u : 0u);
               }
             }
-            umma_commit(bar(B_S_FULL0 + sb));
+            umma_commit(bar(B_S_FULL));
             if (last) ++qpiece;
             ++qk;
             progressed = true;
           }
         }
-        if (pv < qk) {
-          const int pb = pv & 1;
-          if (mbar_test(bar(B_P_FULL0 + pb), (pv >> 1) & 1)) {
-            const int64_t idx = s_c + pv;
-            const int b = locate(prefix, B, idx);
-            const bool first = (pv == 0) || (idx == prefix[b]);  // overwrite O
-            tc_fence_after();
-            // O[:, rank half] (+)= P V: A = P, K-major with the 64-byte swizzle
-            // (8-row atoms of 512 B); B = V, MN-major with the 128-byte swizzle
-            // (8-token groups 1 KB apart, the next 64 columns in the next box).
-            const int s = pv % kStages;
-            const uint32_t vbase = sbase + kOffKV + s * kStageBytes;
+        if (pv < qk && mbar_test(bar(B_P_FULL), pv & 1)) {
+          const int64_t idx = s_c + pv;
+          const int b = locate(prefix, B, idx);
+          const bool first = (pv == 0) || (idx == prefix[b]);  // overwrite O
+          tc_fence_after();
+          // O[:, rank half] (+)= P V: A = P from TMEM (16 tokens = 8 columns per
+          // step); B = V, MN-major with the 128-byte swizzle (8-token groups 1 KB
+          // apart, the next 64 columns in the next box).
+          const int s = pv % kStages;
+          const uint32_t vbase = sbase + kOffKV + s * kStageBytes;
 #pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk) {
-              const uint64_t a = umma_smem_desc(sbase + kOffP + pb * kPBytes + kk * 32, 0, 512, 4);
-              const uint64_t bdesc = umma_smem_desc(vbase + kk * 16 * 128, kBoxKV, 1024, 2);
-              umma_bf16(tmem + kTmemO, a, bdesc, idesc_pv, (first && kk == 0) ? 0u : 1u);
-            }
-            umma_commit(bar(B_KV_EMPTY0 + s));
-            umma_commit(bar(B_PV_DONE0 + pb));
-            ++pv;
-            progressed = true;
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            const uint64_t bdesc = umma_smem_desc(vbase + kk * 16 * 128, kBoxKV, 1024, 2);
+            umma_bf16_tmem_a(tmem + kTmemO, tmem + kTmemP + 8 * kk, bdesc, idesc_pv,
+                             (first && kk == 0) ? 0u : 1u);
           }
+          umma_commit(bar(B_KV_EMPTY0 + s));
+          umma_commit(bar(B_PV_DONE));
+          ++pv;
+          progressed = true;
         }
         if (progressed) {
           last_progress = globaltimer_ns();
@@ -290,6 +288,22 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       const volatile int never = 0;
       mbar_wait(bar(B_FINAL), 0, &never);
     }
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ exchange warp
+    // Once all rows of received tile j are read, tell the peer its next bulk
+    // copy may land (the remote arrive's latency stays off the softmax path).
+    if (lane == 0) {
+      const uint32_t peer_xfree = mapa_shared(bar(B_X_FREE), peer);
+      const int total = int(e_c - s_c);
+      for (int j = 0; j < total; ++j) {
+        if (!mbar_wait(bar(B_READ_DONE), j & 1, abort_flag)) {
+          raise_error(p.err_flags, kErrTimeout);
+          *abort_flag = 1;
+          break;
+        }
+        mbar_arrive_remote(peer_xfree);
+      }
+    }
   } else {
     // ------------------------------------------------------------ softmax / epilogue
     const int q4 = warp & 3;
@@ -297,38 +311,47 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     const uint32_t tl = tmem + (uint32_t(32 * q4) << 16);
     const float c = p.scale_log2;
     const uint32_t peer_x = mapa_shared(sbase + kOffX, peer);
-    const uint32_t peer_xfull = mapa_shared(bar(B_X_FULL0), peer);
+    const uint32_t peer_xfull = mapa_shared(bar(B_X_FULL), peer);
     const int stid = tid - 64;                       // 0..127 within the softmax group
     const int total = int(e_c - s_c);                // tiles of this cluster
-    const uint32_t swz = uint32_t(row & 7);          // 16-byte chunk swizzle of this row
+    // 16-byte chunk k of this row in an exchange buffer (swizzled by row).
+    auto xaddr = [&](uint32_t buf, int k) -> uint32_t {
+      return buf + uint32_t(row * kXRow) + ((uint32_t(k) ^ uint32_t(row & 7)) << 4);
+    };
 
     // send(j): this rank's partial scores of tile j. The rows go to the local
-    // staging buffer j & 1; once all 128 are there, one thread bulk-copies the
-    // 16 KB into the peer's receive buffer j & 1, crediting the bytes to the
-    // peer's X_FULL barrier. No flow-control barrier is needed: the peer sends
-    // tile j + 2 into our buffer only after receiving our tile j + 1, which we
-    // send after reading tile j; and our staging buffer j & 1 is rewritten only
-    // after the peer's tile j + 1 reached us, which it sent after receiving j.
-    auto send = [&](int j, uint32_t (&sv)[kTile]) -> bool {
-      const int sb = j % kSBufs, xb = j & 1;
-      if (!mbar_wait(bar(B_S_FULL0 + sb), (j / kSBufs) & 1, abort_flag)) return false;
+    // staging buffer j & 1 (they are re-read from there when tile j is summed);
+    // once all 128 are there, one thread bulk-copies the buffer into the peer's
+    // receive buffer j & 1, crediting the bytes to the peer's X_FULL barrier.
+    // No flow-control barrier is needed: the peer sends tile j + 2 into our
+    // buffer only after receiving our tile j + 1, which we send after summing
+    // tile j; and staging buffer j & 1 is rewritten only after the peer's tile
+    // j + 1 reached us, which the peer sent after receiving our tile j.
+    auto send = [&](int j) -> bool {
+      const int xb = j & 1;
+      if (!mbar_wait(bar(B_S_FULL), j & 1, abort_flag)) return false;
       tc_fence_after();
-      tmem_ld32(tl + kTmemS + kTile * sb, sv);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(bar(B_S_EMPTY0 + sb));
-      const uint32_t dst = sbase + kOffStg + xb * kXBytes + row * 128;
+      const uint32_t stg = sbase + kOffStg + xb * kXBytes;
+#pragma unroll 1
+      for (int h = 0; h < kTile / 32; ++h) {
+        uint32_t v[32];
+        tmem_ld32(tl + kTmemS + 32 * h, v);
+        tmem_wait_ld();
 #pragma unroll
-      for (int k = 0; k < kTile / 4; ++k)
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst + ((k ^ swz) << 4)),
-                     "r"(sv[4 * k]), "r"(sv[4 * k + 1]), "r"(sv[4 * k + 2]), "r"(sv[4 * k + 3])
-                     : "memory");
+        for (int k = 0; k < 8; ++k)
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(xaddr(stg, 8 * h + k)),
+                       "r"(v[4 * k]), "r"(v[4 * k + 1]), "r"(v[4 * k + 2]), "r"(v[4 * k + 3])
+                       : "memory");
+      }
+      tc_fence_before();
+      mbar_arrive(bar(B_S_EMPTY));                   // QK of the next tile may start
       fence_proxy_async_smem();
       mbar_arrive(bar(B_STAGED0 + xb));
       if (stid == 0) {
         if (!mbar_wait(bar(B_STAGED0 + xb), (j >> 1) & 1, abort_flag)) return false;
-        bulk_copy_to_peer(peer_x + xb * kXBytes, sbase + kOffStg + xb * kXBytes, kXBytes,
-                          peer_xfull + 8 * xb);
+        // the peer's single receive buffer must have been read (tile j - 1)
+        if (j >= 1 && !mbar_wait_cluster(bar(B_X_FREE), (j - 1) & 1, abort_flag)) return false;
+        bulk_copy_to_peer(peer_x, stg, kXBytes, peer_xfull);
       }
       return true;
     };
@@ -355,9 +378,8 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       mbar_arrive(bar(B_Q_FULL));
     };
 
-    uint32_t sv_cur[kTile], sv_nxt[kTile];
     if (total > 0) load_q(locate(prefix, B, s_c));
-    bool ok = total == 0 || send(0, sv_cur);
+    bool ok = total == 0 || send(0);
     int it = 0;
     for (int64_t idx = s_c; idx < e_c && ok;) {
       const int b = locate(prefix, B, idx);
@@ -372,34 +394,34 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       int bad = 0;
       int page_cur = bt_row[(j0 * kTile) / p.page_size];
       for (int t = 0; t < ntiles; ++t, ++it) {
-        const int pb = it & 1;                       // P and exchange buffers
-        const uint32_t ph = (it >> 1) & 1;
+        const int xb = it & 1;
         const int tok0 = (j0 + t) * kTile;
         const int valid = min(kTile, L - tok0);
         // block-table entry of the next tile, loaded one tile ahead
         const int page_nxt = (t + 1 < ntiles) ? bt_row[(tok0 + kTile) / p.page_size] : 0;
         bad |= (page_cur < 0 || page_cur >= p.num_pages) ? 1 : 0;
 
-        // receive the peer's partial of this tile and sum
-        if (stid == 0) mbar_arrive_expect_tx(bar(B_X_FULL0 + pb), kXBytes);
-        if (!mbar_wait_cluster(bar(B_X_FULL0 + pb), ph, abort_flag)) { ok = false; break; }
+        // receive the peer's partial of this tile; S = own + peer
+        if (stid == 0) mbar_arrive_expect_tx(bar(B_X_FULL), kXBytes);
+        if (!mbar_wait_cluster(bar(B_X_FULL), it & 1, abort_flag)) { ok = false; break; }
         float x[kTile];
         {
-          const uint32_t src = sbase + kOffX + pb * kXBytes + row * 128;
+          const uint32_t own = sbase + kOffStg + xb * kXBytes;
+          const uint32_t got = sbase + kOffX;
 #pragma unroll
           for (int k = 0; k < kTile / 4; ++k) {
-            float v0, v1, v2, v3;
+            float a0, a1, a2, a3, b0, b1, b2, b3;
             asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(v0), "=f"(v1), "=f"(v2), "=f"(v3)
-                         : "r"(src + ((k ^ swz) << 4))
-                         : "memory");
-            x[4 * k] = __uint_as_float(sv_cur[4 * k]) + v0;
-            x[4 * k + 1] = __uint_as_float(sv_cur[4 * k + 1]) + v1;
-            x[4 * k + 2] = __uint_as_float(sv_cur[4 * k + 2]) + v2;
-            x[4 * k + 3] = __uint_as_float(sv_cur[4 * k + 3]) + v3;
+                         : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3) : "r"(xaddr(own, k)) : "memory");
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(b0), "=f"(b1), "=f"(b2), "=f"(b3) : "r"(xaddr(got, k)) : "memory");
+            x[4 * k] = a0 + b0;
+            x[4 * k + 1] = a1 + b1;
+            x[4 * k + 2] = a2 + b2;
+            x[4 * k + 3] = a3 + b3;
           }
         }
-
+        mbar_arrive(bar(B_READ_DONE));  // the exchange warp releases the buffer to the peer
         // online softmax (base 2); the max moves only when it grows by > 8
         float mx = -CUDART_INF_F;
 #pragma unroll
@@ -439,23 +461,13 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
           }
         }
 
-        // send the next tile's partial (its QK ran while this tile was summed);
-        // a new sequence first needs its Q in TMEM (every QK of this one is done:
-        // this tile's S was read above)
-        if (it + 1 < total && t + 1 == ntiles) load_q(locate(prefix, B, s_c + it + 1));
-        if (it + 1 < total && !send(it + 1, sv_nxt)) { ok = false; break; }
-
-        // P buffer pb is free once PV(it - 2) finished; a rescale of O also
-        // needs PV(it - 1) finished.
-        if (it >= 2 && !mbar_wait(bar(B_PV_DONE0 + pb), ph ^ 1u, abort_flag)) { ok = false; break; }
+        // The P tile in TMEM is free (and O stable for a rescale) once PV(it - 1)
+        // finished.
+        if (it >= 1 && !mbar_wait(bar(B_PV_DONE), (it - 1) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
         // tcgen05.ld/st are warp-wide: rescale when any row of the warp needs it
         // (rows that do not need it multiply by exactly 1).
         if (__any_sync(0xffffffffu, rescale)) {
-          if (it >= 1 && !mbar_wait(bar(B_PV_DONE0 + (pb ^ 1)), ((it - 1) >> 1) & 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
 #pragma unroll 1
           for (int cc = 0; cc < 8; ++cc) {
             uint32_t o[32];
@@ -465,30 +477,22 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
             for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
             tmem_st32(tl + kTmemO + 32 * cc, o);
           }
-          tmem_wait_st();
         }
-        // P row: kTile bf16 = 64 bytes, K-major with the 64-byte swizzle
-        // (16-byte chunk c of row r lands at chunk c ^ ((r >> 1) & 3)).
-        {
-          const uint32_t prow = sbase + kOffP + pb * kPBytes + row * 64;
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
-                             prow + ((k ^ ((row >> 1) & 3)) << 4)),
-                         "r"(pk[4 * k]), "r"(pk[4 * k + 1]), "r"(pk[4 * k + 2]), "r"(pk[4 * k + 3])
-                         : "memory");
-        }
-        fence_proxy_async_smem();
+        tmem_st32(tl + kTmemP, pk);                  // P row: 64 bf16 in 32 columns
+        tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(B_P_FULL0 + pb));
-#pragma unroll
-        for (int k = 0; k < kTile; ++k) sv_cur[k] = sv_nxt[k];
+        mbar_arrive(bar(B_P_FULL));
+
+        // send the next tile's partial; a new sequence first needs its Q in TMEM
+        // (every QK of this one is done: this tile's S was read out)
+        if (it + 1 < total && t + 1 == ntiles) load_q(locate(prefix, B, s_c + it + 1));
+        if (it + 1 < total && !send(it + 1)) { ok = false; break; }
         page_cur = page_nxt;
       }
       if (!ok) break;
 
       // ---- epilogue of the piece: O / l
-      if (!mbar_wait(bar(B_PV_DONE0 + ((it - 1) & 1)), ((it - 1) >> 1) & 1, abort_flag)) {
+      if (!mbar_wait(bar(B_PV_DONE), (it - 1) & 1, abort_flag)) {
         ok = false;
         break;
       }

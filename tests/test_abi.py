@@ -96,6 +96,7 @@ def _mla_params(**over):
     (dict(Hq=64), zl.ERR_UNSUPPORTED),
     (dict(page_size=16), zl.ERR_UNSUPPORTED),
     (dict(page_size=48), zl.ERR_UNSUPPORTED),
+    (dict(page_size=32), zl.ERR_UNSUPPORTED),
     (dict(q_len=2), zl.ERR_UNSUPPORTED),
     (dict(B=3000), zl.ERR_UNSUPPORTED),
 ])

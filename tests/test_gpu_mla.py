@@ -38,7 +38,7 @@ def test_mla_any_split(num_ctas):
     _parity(_mla_case(602, [700, 1500, 33, 2048]), num_ctas=num_ctas)
 
 
-@pytest.mark.parametrize("P", [32, 64, 128, 256])
+@pytest.mark.parametrize("P", [64, 128, 256])
 def test_mla_page_sizes(P):
     _parity(_mla_case(603 + P, [P - 1, P, P + 1, 3 * P + 5], page_size=P))
 
