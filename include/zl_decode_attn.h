@@ -14,7 +14,11 @@
  *   lse[b,h]   = ln sum_t exp(scale * q[b,h,:] . K_b[t,kh,:])
  *
  * where row t of K_b is slot (t mod page_size) of physical page
- * block_table[b, t / page_size] (likewise V). Grouped-query heads sharing a
+ * block_table[b, t / page_size] (likewise V). With q_len > 1 new tokens per
+ * sequence (speculative or multi-token-prediction decode: all of them are
+ * already in the cache, the last q_len of its seq_lens[b] tokens), query
+ * token i < q_len attends causally to t < seq_lens[b] - q_len + 1 + i, and
+ * q, out, lse gain a q_len axis after B. Grouped-query heads sharing a
  * kv head are evaluated together so each K/V byte is read once per group (the
  * DataFun talk write-up, section "1. 大模型负载分析", names the head-sharing
  * attention variants). Long or ragged contexts are split across CTAs and the
@@ -115,8 +119,11 @@ typedef struct {
 
 /*
  * GQA / MHA / MQA decode over separate K and V pools.
- *   Supported: D_qk = D_v = 128; 1 <= Hq/Hkv <= 16; Hq % Hkv == 0;
- *   page_size a multiple of 16 (<= 1024); q_len = 1; 1 <= B <= 4096.
+ *   Supported: D_qk = D_v = 128; Hq % Hkv == 0; 1 <= (Hq/Hkv) * q_len <= 16
+ *   (the query rows one kv head serves share one 16-row tensor-core tile);
+ *   page_size a multiple of 16 (<= 1024); 1 <= B <= 4096. A query row that
+ *   sees no token (seq_lens[b] < q_len) gives out = 0 and lse = -inf. A bad
+ *   page id zeroes every query row of its sequence and kv head.
  *   Anything else returns ZL_ERR_UNSUPPORTED (or ZL_ERR_INVALID_ARG when the
  *   value is not meaningful at all, e.g. Hkv = 0).
  */

@@ -70,8 +70,7 @@ zl_status gqa_validate_shape(const zl_decode_attn_params* a) {
   if (a->Hq % a->Hkv != 0) return ZL_ERR_INVALID_ARG;
   if (!(a->scale > 0.f) || !std::isfinite(a->scale)) return ZL_ERR_INVALID_ARG;
   if (a->D_qk != zl::kGqaHeadDim || a->D_v != zl::kGqaHeadDim) return ZL_ERR_UNSUPPORTED;
-  if (a->Hq / a->Hkv > 16) return ZL_ERR_UNSUPPORTED;
-  if (a->q_len != 1) return ZL_ERR_UNSUPPORTED;
+  if (a->Hq / a->Hkv * a->q_len > 16) return ZL_ERR_UNSUPPORTED;  // (query, head) rows per tile
   if (a->page_size % zl::kGqaTile != 0 || a->page_size > 1024) return ZL_ERR_UNSUPPORTED;
   if (a->B > zl::kMaxBatch) return ZL_ERR_UNSUPPORTED;
   return ZL_OK;
@@ -87,7 +86,8 @@ zl_status gqa_plan(const zl_decode_attn_params* a, GqaPlan* plan) {
   plan->nhg = a->Hkv / plan->hpc;
   int grid = a->num_ctas;
   if (grid == 0) {
-    const int per_sm = zl::gqa_ctas_per_sm(plan->hpc, plan->g > 8, dev.device);
+    const int per_sm =
+        zl::gqa_ctas_per_sm(plan->hpc, plan->g * a->q_len > 8, a->q_len > 1, dev.device);
     if (per_sm < 1) return ZL_ERR_CUDA;
     grid = dev.sms * per_sm;
     if (a->max_seq_len > 0) {
@@ -98,7 +98,7 @@ zl_status gqa_plan(const zl_decode_attn_params* a, GqaPlan* plan) {
     }
   }
   plan->grid = grid;
-  const size_t rows = size_t(grid) * 2 * plan->hpc * plan->g;  // partial slots
+  const size_t rows = size_t(grid) * 2 * plan->hpc * plan->g * a->q_len;  // partial slots
   plan->off_lse = round_up(size_t(a->B + 1) * sizeof(int32_t), 256);
   plan->off_o = plan->off_lse + round_up(rows * sizeof(float), 256);
   plan->bytes = plan->off_o + rows * zl::kGqaHeadDim * sizeof(float);
@@ -229,6 +229,7 @@ zl_status zl_decode_attn(const zl_decode_attn_params* a, zl_stream_t stream) {
   p.ws_o = reinterpret_cast<float*>(ws + plan.off_o);
   p.err_flags = a->err_flags;
   p.B = a->B;
+  p.q_len = a->q_len;
   p.Hq = a->Hq;
   p.Hkv = a->Hkv;
   p.g = plan.g;

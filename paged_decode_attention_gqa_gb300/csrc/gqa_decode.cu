@@ -19,7 +19,9 @@
 // "ZhiLight: Zhihu's CUDA Inference Engine..." page, "Dual streams, host
 // all-reduce and the memory model"), S = Q K^T and O += P V run on mma.sync,
 // and the online softmax (running max, rescaled sum) stays in registers with
-// quad shuffles.
+// quad shuffles. With q_len > 1 query tokens per sequence the rows are the
+// (token, head) pairs, g * q_len <= 16 of them, each with its causal limit
+// (the CAUSAL instances; q_len = 1 runs the instances without the limit).
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -60,7 +62,7 @@ __device__ __forceinline__ int locate_seq(const int* prefix, int B, int nhg, int
   return lo;
 }
 
-template <int HPC, bool ROWS16>
+template <int HPC, bool ROWS16, bool CAUSAL>
 __global__ void __launch_bounds__(GqaCfg<HPC>::kThreads, 1)
 gqa_decode_kernel(const __grid_constant__ GqaParams p) {
   using Cfg = GqaCfg<HPC>;
@@ -220,14 +222,24 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
     const int slot = (idx == s_c) ? 0 : 1;
     const int L = p.seq_lens[b];
     const int head0 = (hg * HPC + w) * g;  // first query head of this kv head
+    // m16 tile rows r < R = g * q_len are (query token i = r / g, head head0 + r % g);
+    // the rest are zero. Query i sees tokens t < L - q_len + 1 + i (the new
+    // tokens are in the cache; each sees itself and what precedes it).
+    const int R = g * p.q_len;
+    const int ra = gid, rb = gid + 8;
+    const int lim_a = L - p.q_len + 1 + ra / g;
+    const int lim_b = L - p.q_len + 1 + rb / g;
+    auto qrow_index = [&](int r) -> int64_t {
+      return (int64_t(b) * p.q_len + r / g) * p.Hq + head0 + r % g;
+    };
 
-    // Q rows of the m16 tile: query heads head0 + r, r < g (the rest zero).
     uint32_t qa[8][4];
     {
-      const bool r0 = gid < g, r1 = ROWS16 && (gid + 8 < g);
-      const uint32_t* q0 = reinterpret_cast<const uint32_t*>(
-          p.q + (int64_t(b) * p.Hq + head0 + gid) * kGqaHeadDim);
-      const uint32_t* q1 = q0 + 8 * kGqaHeadDim / 2;
+      const bool r0 = ra < R, r1 = ROWS16 && rb < R;
+      const uint32_t* q0 =
+          reinterpret_cast<const uint32_t*>(p.q + (r0 ? qrow_index(ra) : 0) * kGqaHeadDim);
+      const uint32_t* q1 =
+          reinterpret_cast<const uint32_t*>(p.q + (r1 ? qrow_index(rb) : 0) * kGqaHeadDim);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         const int wd = ks * 8 + t4;  // 32-bit word index of d = 16ks + 2t4
@@ -244,11 +256,35 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
     for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
     int bad = 0;
 
+    // One row's online-softmax step in base 2 over this thread's four scores
+    // (tokens 2t4, 2t4+1, 2t4+8, 2t4+9 of the tile; vis = visible tokens of
+    // the row in this tile). A row with nothing visible yet keeps m = -inf and
+    // contributes zeros.
+    auto row_step = [&](float sa, float sb, float sc, float sd, int vis, float& m, float& l,
+                        uint32_t& p_lo, uint32_t& p_hi) -> float {
+      const float x0 = 2 * t4 < vis ? sa * scale_log2 : -CUDART_INF_F;
+      const float x1 = 2 * t4 + 1 < vis ? sb * scale_log2 : -CUDART_INF_F;
+      const float x2 = 2 * t4 + 8 < vis ? sc * scale_log2 : -CUDART_INF_F;
+      const float x3 = 2 * t4 + 9 < vis ? sd * scale_log2 : -CUDART_INF_F;
+      float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float mn = fmaxf(m, mx);
+      const float base = mn == -CUDART_INF_F ? 0.f : mn;
+      const float alpha = ex2_approx(m - base);
+      m = mn;
+      p_lo = pack_bf16x2(ex2_approx(x0 - base), ex2_approx(x1 - base));
+      p_hi = pack_bf16x2(ex2_approx(x2 - base), ex2_approx(x3 - base));
+      const float2 f0 = unpack_bf16x2(p_lo), f2 = unpack_bf16x2(p_hi);
+      l = l * alpha + ((f0.x + f0.y) + (f2.x + f2.y));
+      return alpha;
+    };
+
     for (int t = 0; t < ntiles; ++t, ++it) {
       const int stage = it % NS;
       const uint32_t phase = (it / NS) & 1;
       const int tok0 = (j0 + t) * kGqaTile;
-      const int valid = min(kGqaTile, L - tok0);
+      const int valid = min(kGqaTile, L - tok0);  // tokens in the cache (V rows to keep)
       if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag)) {
         if (lane == 0) {
           raise_error(p.err_flags, kErrTimeout);
@@ -276,25 +312,10 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
         }
       }
 
-      // Online softmax in base 2. Columns of this thread: tokens 2t4, 2t4+1 (+8).
-      const bool v00 = 2 * t4 < valid, v01 = 2 * t4 + 1 < valid;
-      const bool v10 = 2 * t4 + 8 < valid, v11 = 2 * t4 + 9 < valid;
       uint32_t pa[4];
       {
-        const float x0 = v00 ? s[0][0] * scale_log2 : -CUDART_INF_F;
-        const float x1 = v01 ? s[0][1] * scale_log2 : -CUDART_INF_F;
-        const float x2 = v10 ? s[1][0] * scale_log2 : -CUDART_INF_F;
-        const float x3 = v11 ? s[1][1] * scale_log2 : -CUDART_INF_F;
-        float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float mn = fmaxf(m0, mx);
-        const float alpha = ex2_approx(m0 - mn);
-        m0 = mn;
-        pa[0] = pack_bf16x2(ex2_approx(x0 - mn), ex2_approx(x1 - mn));
-        pa[2] = pack_bf16x2(ex2_approx(x2 - mn), ex2_approx(x3 - mn));
-        const float2 f0 = unpack_bf16x2(pa[0]), f2 = unpack_bf16x2(pa[2]);
-        l0 = l0 * alpha + ((f0.x + f0.y) + (f2.x + f2.y));
+        const float alpha = row_step(s[0][0], s[0][1], s[1][0], s[1][1],
+                                     CAUSAL ? min(valid, lim_a - tok0) : valid, m0, l0, pa[0], pa[2]);
 #pragma unroll
         for (int nt = 0; nt < 16; ++nt) {
           o[nt][0] *= alpha;
@@ -302,20 +323,8 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
         }
       }
       if (ROWS16) {
-        const float x0 = v00 ? s[0][2] * scale_log2 : -CUDART_INF_F;
-        const float x1 = v01 ? s[0][3] * scale_log2 : -CUDART_INF_F;
-        const float x2 = v10 ? s[1][2] * scale_log2 : -CUDART_INF_F;
-        const float x3 = v11 ? s[1][3] * scale_log2 : -CUDART_INF_F;
-        float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float mn = fmaxf(m1, mx);
-        const float alpha = ex2_approx(m1 - mn);
-        m1 = mn;
-        pa[1] = pack_bf16x2(ex2_approx(x0 - mn), ex2_approx(x1 - mn));
-        pa[3] = pack_bf16x2(ex2_approx(x2 - mn), ex2_approx(x3 - mn));
-        const float2 f1 = unpack_bf16x2(pa[1]), f3 = unpack_bf16x2(pa[3]);
-        l1 = l1 * alpha + ((f1.x + f1.y) + (f3.x + f3.y));
+        const float alpha = row_step(s[0][2], s[0][3], s[1][2], s[1][3],
+                                     CAUSAL ? min(valid, lim_b - tok0) : valid, m1, l1, pa[1], pa[3]);
 #pragma unroll
         for (int nt = 0; nt < 16; ++nt) {
           o[nt][2] *= alpha;
@@ -325,9 +334,11 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
         pa[1] = pa[3] = 0u;
       }
 
-      // O += P V. Masked token rows of V are zeroed in registers so that NaN
-      // in unused slots cannot reach the output (0 * NaN = NaN).
+      // O += P V. Token rows of V past the cache end are zeroed in registers so
+      // that NaN in unused slots cannot reach the output (0 * NaN = NaN).
       {
+        const bool v00 = 2 * t4 < valid, v01 = 2 * t4 + 1 < valid;
+        const bool v10 = 2 * t4 + 8 < valid, v11 = 2 * t4 + 9 < valid;
         const uint32_t m01 = (v00 ? 0x0000ffffu : 0u) | (v01 ? 0xffff0000u : 0u);
         const uint32_t m89 = (v10 ? 0x0000ffffu : 0u) | (v11 ? 0xffff0000u : 0u);
         const int tok = (lane & 7) + (((lane >> 3) & 1) << 3);
@@ -362,28 +373,30 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
     if (bad && lane == 0) raise_error(p.err_flags, kErrBadPage);
 #pragma unroll
     for (int half = 0; half < (ROWS16 ? 2 : 1); ++half) {
-      const int r = gid + 8 * half;
-      if (r >= g) continue;
+      const int r = half ? rb : ra;
+      if (r >= R) continue;
       const float l = half ? l1 : l0;
       const float m = half ? m1 : m0;
-      // A piece that met a bad page is written as zeros (its data is stale).
-      const float inv = 1.f / l;
-      const float lse2 = bad ? -CUDART_INF_F : m + log2f(l);
+      // A piece that met a bad page, or a row that saw no token, is written as
+      // zeros with lse = -inf (weight 0 in the merge).
+      const bool none = bad || !(l > 0.f);
+      const float inv = none ? 0.f : 1.f / l;
+      const float lse2 = none ? -CUDART_INF_F : m + log2f(l);
       if (!partial) {
-        const int64_t orow = int64_t(b) * p.Hq + head0 + r;
+        const int64_t orow = qrow_index(r);
         uint32_t* dst = reinterpret_cast<uint32_t*>(p.out + orow * kGqaHeadDim);
 #pragma unroll
         for (int nt = 0; nt < 16; ++nt)
           dst[nt * 4 + t4] =
-              bad ? 0u : pack_bf16x2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
+              none ? 0u : pack_bf16x2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
         if (p.lse && t4 == 0) p.lse[orow] = lse2 * 0.69314718055994531f;
       } else {
-        const int64_t wrow = ((int64_t(c) * 2 + slot) * HPC + w) * g + r;
+        const int64_t wrow = ((int64_t(c) * 2 + slot) * HPC + w) * R + r;
         float2* dst = reinterpret_cast<float2*>(p.ws_o + wrow * kGqaHeadDim);
 #pragma unroll
         for (int nt = 0; nt < 16; ++nt)
-          dst[nt * 4 + t4] = bad ? make_float2(0.f, 0.f)
-                                 : make_float2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
+          dst[nt * 4 + t4] = none ? make_float2(0.f, 0.f)
+                                  : make_float2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
         if (t4 == 0) p.ws_lse[wrow] = bad ? CUDART_NAN_F : lse2;
       }
     }
@@ -393,11 +406,12 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
   // Sequences with no tiles (empty or invalid length): zeros, lse = -inf.
   for (int b = c; b < B; b += G) {
     if (prefix[b + 1] != prefix[b]) continue;
-    uint4* dst = reinterpret_cast<uint4*>(p.out + int64_t(b) * p.Hq * kGqaHeadDim);
-    const int n16 = p.Hq * kGqaHeadDim * 2 / 16;
-    for (int i = tid; i < n16; i += HPC * 32) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+    const int64_t rows = int64_t(p.q_len) * p.Hq;
+    uint4* dst = reinterpret_cast<uint4*>(p.out + int64_t(b) * rows * kGqaHeadDim);
+    const int64_t n16 = rows * kGqaHeadDim * 2 / 16;
+    for (int64_t i = tid; i < n16; i += HPC * 32) dst[i] = make_uint4(0u, 0u, 0u, 0u);
     if (p.lse)
-      for (int i = tid; i < p.Hq; i += HPC * 32) p.lse[int64_t(b) * p.Hq + i] = -CUDART_INF_F;
+      for (int64_t i = tid; i < rows; i += HPC * 32) p.lse[int64_t(b) * rows + i] = -CUDART_INF_F;
   }
 }
 
@@ -413,10 +427,12 @@ __device__ __forceinline__ int cta_of_tile(int64_t x, int64_t W, int G) {
 __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ GqaParams p,
                                                         int G) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = int64_t(blockIdx.x) * 4 + warp;
-  if (row >= int64_t(p.B) * p.Hq) return;
-  const int b = int(row / p.Hq), hq = int(row % p.Hq);
-  const int kvh = hq / p.g, hg = kvh / p.hpc, w = kvh % p.hpc, r = hq % p.g;
+  const int64_t row = int64_t(blockIdx.x) * 4 + warp;  // (b, query token i, head)
+  if (row >= int64_t(p.B) * p.q_len * p.Hq) return;
+  const int b = int(row / (int64_t(p.q_len) * p.Hq));
+  const int i = int((row / p.Hq) % p.q_len), hq = int(row % p.Hq);
+  const int kvh = hq / p.g, hg = kvh / p.hpc, w = kvh % p.hpc;
+  const int R = p.g * p.q_len, r = i * p.g + hq % p.g;  // row of the m16 tile
   const int* prefix = p.ws_prefix;
   const int n = prefix[b + 1] - prefix[b];
   if (n == 0) return;
@@ -431,7 +447,7 @@ __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ 
     const int64_t s_c = int64_t(c) * W / G, e_c = int64_t(c + 1) * W / G;
     if (s_c == e_c) continue;
     const int slot = (c == c_lo && U0 > s_c) ? 1 : 0;
-    const float l = p.ws_lse[((int64_t(c) * 2 + slot) * p.hpc + w) * p.g + r];
+    const float l = p.ws_lse[((int64_t(c) * 2 + slot) * p.hpc + w) * R + r];
     bad |= isnan(l);
     M = fmaxf(M, l);
   }
@@ -442,7 +458,7 @@ __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ 
       const int64_t s_c = int64_t(c) * W / G, e_c = int64_t(c + 1) * W / G;
       if (s_c == e_c) continue;
       const int slot = (c == c_lo && U0 > s_c) ? 1 : 0;
-      const int64_t wrow = ((int64_t(c) * 2 + slot) * p.hpc + w) * p.g + r;
+      const int64_t wrow = ((int64_t(c) * 2 + slot) * p.hpc + w) * R + r;
       const float wgt = exp2f(p.ws_lse[wrow] - M);
       const float4 v = reinterpret_cast<const float4*>(p.ws_o + wrow * kGqaHeadDim)[lane];
       acc.x += wgt * v.x;
@@ -464,34 +480,34 @@ __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ 
 constexpr int kMaxDevices = 64;
 
 // Raise the dynamic shared-memory limit of one kernel instance, once per device.
-template <int HPC, bool R16>
+template <int HPC, bool R16, bool C>
 cudaError_t configure(int device) {
   static bool done[kMaxDevices] = {};
   if (device >= 0 && device < kMaxDevices && done[device]) return cudaSuccess;
-  const cudaError_t e = cudaFuncSetAttribute(gqa_decode_kernel<HPC, R16>,
+  const cudaError_t e = cudaFuncSetAttribute(gqa_decode_kernel<HPC, R16, C>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              int(GqaCfg<HPC>::kSmemBytes));
   if (e == cudaSuccess && device >= 0 && device < kMaxDevices) done[device] = true;
   return e;
 }
 
-template <int HPC, bool R16>
+template <int HPC, bool R16, bool C>
 cudaError_t launch_attn(const GqaParams& p, int grid, cudaStream_t stream) {
   using Cfg = GqaCfg<HPC>;
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
-  if ((e = configure<HPC, R16>(device)) != cudaSuccess) return e;
-  gqa_decode_kernel<HPC, R16><<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(p);
+  if ((e = configure<HPC, R16, C>(device)) != cudaSuccess) return e;
+  gqa_decode_kernel<HPC, R16, C><<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 
-template <int HPC, bool R16>
+template <int HPC, bool R16, bool C>
 int occupancy(int device) {
   using Cfg = GqaCfg<HPC>;
-  if (configure<HPC, R16>(device) != cudaSuccess) return 0;
+  if (configure<HPC, R16, C>(device) != cudaSuccess) return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_decode_kernel<HPC, R16>, Cfg::kThreads,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_decode_kernel<HPC, R16, C>, Cfg::kThreads,
                                                     Cfg::kSmemBytes) != cudaSuccess)
     return 0;
   return n;
@@ -506,39 +522,54 @@ int gqa_heads_per_cta(int Hkv) {
   return 1;
 }
 
-int gqa_ctas_per_sm(int hpc, bool rows16, int device) {
-  switch (hpc * 2 + (rows16 ? 1 : 0)) {
-    case 2: return occupancy<1, false>(device);
-    case 3: return occupancy<1, true>(device);
-    case 4: return occupancy<2, false>(device);
-    case 5: return occupancy<2, true>(device);
-    case 8: return occupancy<4, false>(device);
-    case 9: return occupancy<4, true>(device);
-    case 16: return occupancy<8, false>(device);
-    case 17: return occupancy<8, true>(device);
-    default: return 0;
+namespace {
+
+// The kernel instance for (heads per CTA, 16 rows, causal rows).
+template <template <int, bool, bool> class F, typename... A>
+auto dispatch(int hpc, bool r16, bool causal, A... a) -> decltype(F<1, false, false>::run(a...)) {
+  using R = decltype(F<1, false, false>::run(a...));
+  const int k = (hpc * 2 + (r16 ? 1 : 0)) * 2 + (causal ? 1 : 0);
+  switch (k) {
+#define ZL_CASE(H, S, C) \
+  case (H * 2 + S) * 2 + C: return F<H, bool(S), bool(C)>::run(a...);
+    ZL_CASE(1, 0, 0) ZL_CASE(1, 0, 1) ZL_CASE(1, 1, 0) ZL_CASE(1, 1, 1)
+    ZL_CASE(2, 0, 0) ZL_CASE(2, 0, 1) ZL_CASE(2, 1, 0) ZL_CASE(2, 1, 1)
+    ZL_CASE(4, 0, 0) ZL_CASE(4, 0, 1) ZL_CASE(4, 1, 0) ZL_CASE(4, 1, 1)
+    ZL_CASE(8, 0, 0) ZL_CASE(8, 0, 1) ZL_CASE(8, 1, 0) ZL_CASE(8, 1, 1)
+#undef ZL_CASE
+    default: return R();
   }
+}
+
+template <int HPC, bool R16, bool C>
+struct Occupancy {
+  static int run(int device) { return occupancy<HPC, R16, C>(device); }
+};
+
+template <int HPC, bool R16, bool C>
+struct Launch {
+  static cudaError_t run(const GqaParams* p, int grid, cudaStream_t stream) {
+    return launch_attn<HPC, R16, C>(*p, grid, stream);
+  }
+};
+
+}  // namespace
+
+int gqa_ctas_per_sm(int hpc, bool rows16, bool causal, int device) {
+  return dispatch<Occupancy>(hpc, rows16, causal, device);
 }
 
 cudaError_t gqa_decode_launch(const GqaParams& p, int grid, cudaStream_t stream,
                               cudaEvent_t attn_begin, cudaEvent_t attn_end) {
   cudaError_t e = cudaSuccess;
   if (attn_begin && (e = cudaEventRecord(attn_begin, stream)) != cudaSuccess) return e;
-  const bool r16 = p.g > 8;
-  switch (p.hpc * 2 + (r16 ? 1 : 0)) {
-    case 2: e = launch_attn<1, false>(p, grid, stream); break;
-    case 3: e = launch_attn<1, true>(p, grid, stream); break;
-    case 4: e = launch_attn<2, false>(p, grid, stream); break;
-    case 5: e = launch_attn<2, true>(p, grid, stream); break;
-    case 8: e = launch_attn<4, false>(p, grid, stream); break;
-    case 9: e = launch_attn<4, true>(p, grid, stream); break;
-    case 16: e = launch_attn<8, false>(p, grid, stream); break;
-    case 17: e = launch_attn<8, true>(p, grid, stream); break;
-    default: return cudaErrorInvalidValue;
-  }
+  const bool r16 = p.g * p.q_len > 8;
+  const bool known = p.hpc == 1 || p.hpc == 2 || p.hpc == 4 || p.hpc == 8;
+  if (!known) return cudaErrorInvalidValue;
+  e = dispatch<Launch>(p.hpc, r16, p.q_len > 1, &p, grid, stream);
   if (e != cudaSuccess) return e;
   if (attn_end && (e = cudaEventRecord(attn_end, stream)) != cudaSuccess) return e;
-  const int64_t rows = int64_t(p.B) * p.Hq;
+  const int64_t rows = int64_t(p.B) * p.q_len * p.Hq;
   gqa_merge_kernel<<<int((rows + 3) / 4), 128, 0, stream>>>(p, grid);
   return cudaGetLastError();
 }

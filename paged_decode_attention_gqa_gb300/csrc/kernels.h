@@ -16,17 +16,17 @@ constexpr int kMaxBatch = 4096;  // sequences per call (prefix table lives in sm
 struct GqaParams {
   CUtensorMap tmap_k;  // 4-D {D, page_size, Hkv, num_pages}, box {64, 16, HPC, 1}, 128B swizzle
   CUtensorMap tmap_v;  // same geometry over the V pool
-  const __nv_bfloat16* q;  // [B, Hq, 128]
-  __nv_bfloat16* out;      // [B, Hq, 128]
-  float* lse;              // [B, Hq] natural log, or nullptr
+  const __nv_bfloat16* q;  // [B, q_len, Hq, 128]
+  __nv_bfloat16* out;      // [B, q_len, Hq, 128]
+  float* lse;              // [B, q_len, Hq] natural log, or nullptr
   const int32_t* block_table;
   const int32_t* seq_lens;
   int64_t bt_stride;
   int32_t* ws_prefix;  // [B + 1] tile prefix sums, written by CTA 0
-  float* ws_o;         // [G][2][HPC][g][128] normalised partial outputs
-  float* ws_lse;       // [G][2][HPC][g] base-2 lse of the partials (NaN = bad piece)
+  float* ws_o;         // [G][2][HPC][g * q_len][128] normalised partial outputs
+  float* ws_lse;       // [G][2][HPC][g * q_len] base-2 lse of the partials (NaN = bad piece)
   uint32_t* err_flags; // or nullptr
-  int B, Hq, Hkv, g, page_size, num_pages;
+  int B, q_len, Hq, Hkv, g, page_size, num_pages;
   int hpc;             // kv heads per CTA
   int nhg;             // Hkv / hpc head groups
   float scale_log2;    // scale * log2(e)
@@ -63,7 +63,7 @@ cudaError_t mla_decode_launch(const MlaParams& p, int clusters, cudaStream_t str
 // kv heads handled by one CTA for this Hkv (largest of 8, 4, 2, 1 dividing it).
 int gqa_heads_per_cta(int Hkv);
 // CTAs of the attention kernel that fit on one SM (0 on error).
-int gqa_ctas_per_sm(int hpc, bool rows16, int device);
+int gqa_ctas_per_sm(int hpc, bool rows16, bool causal, int device);
 // Launches the attention kernel on `grid` CTAs, then the merge kernel.
 cudaError_t gqa_decode_launch(const GqaParams& p, int grid, cudaStream_t stream,
                               cudaEvent_t attn_begin, cudaEvent_t attn_end);

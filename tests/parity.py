@@ -71,7 +71,8 @@ def assert_close(got, ref, what=""):
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (what, got.shape, ref.shape)
     both_inf = np.isinf(ref) & (got == ref)
-    diff = np.where(both_inf, 0.0, np.abs(got - ref))
+    with np.errstate(invalid="ignore"):  # inf - inf where both are -inf (masked below)
+        diff = np.where(both_inf, 0.0, np.abs(got - ref))
     bound = ATOL + RTOL * np.abs(np.where(both_inf, 0.0, ref))
     bad = ~(diff <= bound)
     if bad.any():

@@ -56,7 +56,9 @@ def _params(**over):
     (dict(token_stride=100), zl.ERR_INVALID_ARG),  # not a multiple of 8 elements
     (dict(D_qk=64, D_v=64), zl.ERR_UNSUPPORTED),
     (dict(Hq=8 * 32), zl.ERR_UNSUPPORTED),         # group of 32 heads
-    (dict(q_len=2), zl.ERR_UNSUPPORTED),
+    (dict(q_len=5), zl.ERR_UNSUPPORTED),           # 4 heads x 5 tokens > 16 rows
+    (dict(Hq=8 * 16, q_len=2), zl.ERR_UNSUPPORTED),
+    (dict(q_len=0), zl.ERR_INVALID_ARG),
     (dict(page_size=8), zl.ERR_UNSUPPORTED),
     (dict(B=5000), zl.ERR_UNSUPPORTED),
 ])

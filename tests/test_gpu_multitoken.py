@@ -1,0 +1,114 @@
+"""Multi-token decode queries (q_len > 1: speculative / multi-token-prediction
+steps) on the GPU against the oracle, element by element.
+
+Query token i of a sequence with L cached tokens (the q_len new ones included)
+sees tokens t < L - q_len + 1 + i; the oracle's causal pin fixes that reading.
+"""
+import numpy as np
+import pytest
+import torch
+
+import paged_decode_attention_gqa_gb300 as zl
+from paged_decode_attention_gqa_gb300 import workloads as wl
+from parity import assert_close, device_inputs, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def _parity(w, **kw):
+    g = run_gpu(w, **kw)
+    ref, ref_lse, st = run_oracle(w)
+    assert st == 0
+    assert int(g.err.item()) == 0
+    assert_close(g.out64(), ref, f"{w.name} out")
+    assert_close(g.lse64(), ref_lse, f"{w.name} lse")
+    assert not torch.isnan(g.out.float()).any()
+    return g
+
+
+@pytest.mark.parametrize("Hq,Hkv,q_len", [
+    (32, 8, 2), (32, 8, 3), (32, 8, 4),      # Llama-3 group of 4: 8, 12, 16 rows
+    (16, 8, 2), (16, 8, 5), (16, 8, 8),      # group of 2
+    (8, 8, 7), (8, 8, 16),                   # MHA: one head, up to 16 tokens
+    (10, 2, 3),                              # group of 5: 15 rows
+    (64, 8, 2),                              # group of 8: 16 rows
+])
+def test_group_and_q_len(Hq, Hkv, q_len):
+    w = wl.random_case(700 + 31 * Hq + 7 * Hkv + q_len, B=5, Hq=Hq, Hkv=Hkv, max_len=260,
+                       q_len=q_len)
+    _parity(w)
+
+
+@pytest.mark.parametrize("q_len", [2, 4])
+def test_short_contexts(q_len):
+    """L = 0, L < q_len (rows that see nothing give zeros and lse = -inf), L = q_len,
+    and lengths at the tile edges."""
+    lens = [0, 1, q_len - 1, q_len, q_len + 1, 15, 16, 17, 33]
+    w = wl.random_case(800 + q_len, B=len(lens), Hq=32, Hkv=8, lens=lens, q_len=q_len)
+    g = _parity(w)
+    out = g.out.float().cpu()
+    for b, L in enumerate(lens):
+        for i in range(q_len):
+            if L - q_len + 1 + i <= 0:
+                assert torch.all(out[b, i] == 0)
+                assert torch.all(torch.isneginf(g.lse[b, i].cpu()))
+
+
+@pytest.mark.parametrize("num_ctas", [1, 3, 64, 151, 1000])
+def test_any_split(num_ctas):
+    w = wl.random_case(810, B=6, Hq=32, Hkv=8, max_len=600, q_len=3)
+    _parity(w, num_ctas=num_ctas)
+
+
+@pytest.mark.parametrize("P", [16, 64])
+def test_page_sizes_and_hnd(P):
+    for layout in ("NHD", "HND"):
+        w = wl.random_case(820 + P, B=4, Hq=16, Hkv=4, page_size=P, max_len=5 * P, q_len=4,
+                           layout=layout)
+        _parity(w)
+
+
+def test_last_row_equals_single_token_call():
+    """The last of q_len query tokens sees the whole cache: the same row as a
+    q_len = 1 call with that query, bit for bit (rows of the tensor-core tile
+    are independent, and the split is the same)."""
+    w = wl.random_case(830, B=5, Hq=32, Hkv=8, max_len=400, q_len=4)
+    g = run_gpu(w)
+    w1 = wl.random_case(830, B=5, Hq=32, Hkv=8, max_len=400, q_len=1)
+    w1.q = w.q[:, -1:].contiguous()
+    g1 = run_gpu(w1)
+    assert torch.equal(g.out[:, -1:].view(torch.int16), g1.out.view(torch.int16))
+    assert torch.equal(g.lse[:, -1:], g1.lse)
+
+
+def test_bad_first_page_zeroes_every_row():
+    w = wl.random_case(840, B=3, Hq=32, Hkv=8, lens=[40, 50, 60], q_len=3)
+    d = device_inputs(w)
+    bt = d["bt"].clone()
+    bt[1, 0] = w.num_pages + 5
+    g = run_gpu(w, d, block_table=bt)
+    assert int(g.err.item()) & zl.DEVERR_BAD_PAGE
+    ref, ref_lse, st = run_oracle(w, block_table=bt.cpu().numpy())
+    assert st & 1
+    assert_close(g.out64(), ref, "out")
+    assert_close(g.lse64(), ref_lse, "lse")
+    assert torch.all(g.out[1].float() == 0)
+
+
+def test_full_size_llama3_8b_mtp_sampled():
+    """Llama-3-8B decode shape at batch 64 with 4 query tokens per sequence,
+    sampled rows against the oracle at full context lengths."""
+    w = wl.random_case(850, B=64, Hq=32, Hkv=8, max_len=4096, q_len=4, pool_factor=1.1)
+    g = run_gpu(w)
+    rng = np.random.default_rng(5)
+    bs = rng.choice(w.B, size=6, replace=False)
+    sub_lens = w.seq_lens[bs]
+    ws = wl.build_workload("sampled", 0, B=len(bs), Hq=32, Hkv=8, D_qk=128,
+                           page_size=w.page_size, seq_lens=sub_lens,
+                           block_table=w.block_table[bs], num_pages=w.num_pages, scale=w.scale,
+                           q_len=4, values=False)
+    ws.q, ws.k_pool, ws.v_pool = w.q[bs].contiguous(), w.k_pool, w.v_pool
+    ref, ref_lse, st = run_oracle(ws)
+    assert st == 0
+    assert_close(g.out64()[bs], ref, "sampled out")
+    assert_close(g.lse64()[bs], ref_lse, "sampled lse")
