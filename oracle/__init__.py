@@ -19,7 +19,8 @@ the standard scaled-dot-product attention; zl_oracle.c writes it out.
 Pins (tests/test_oracle_pins.py): torch's fp64 scaled_dot_product_attention on
 gathered dense K/V, scipy's softmax and logsumexp on closed-form one-hot
 cases, single-token / constant-V / zero-query closed forms, token permutation,
-page remapping, split-and-merge, GQA head mapping, MLA column sharing.
+page remapping, split-and-merge, GQA head mapping, MLA column sharing; the KV
+append against a numpy fancy-index gather of the written slots.
 """
 
 from __future__ import annotations
@@ -80,6 +81,10 @@ class Oracle:
             ctypes.c_double, i64, i64, f64p, f64p, f64p]
         lib.zl_oracle_lse_merge.restype = None
         lib.zl_oracle_lse_merge.argtypes = [f64p, f64p, c_int, c_int, f64p, f64p]
+        lib.zl_oracle_kv_append.restype = c_int
+        lib.zl_oracle_kv_append.argtypes = [
+            u16p, u16p, u16p, u16p, i64, i64, i64, i32p, i64, i32p,
+            c_int, c_int, c_int, c_int, c_int, c_int, c_int]
         lib.zl_oracle_max_threads.restype = c_int
         lib.zl_oracle_max_threads.argtypes = []
         self._lib = lib
@@ -146,6 +151,34 @@ class Oracle:
             int(t_begin), int(t_end), _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double),
             _ptr(w, ctypes.c_double) if w is not None else ctypes.cast(None, f64p))
         return out, float(lse[0]), (w[:n] if w is not None else None), int(st)
+
+    def kv_append(self, k_new, v_new, k_pool, v_pool, strides, block_table, seq_lens, *,
+                  page_size, num_pages):
+        """Write the new tokens into copies of the pools; returns (k_pool', v_pool', status).
+
+        k_new  uint16 [B, q_len, Hkv, D_k]; v_new uint16 [B, q_len, Hkv, D_v] or None (MLA)
+        k_pool, v_pool  uint16 pools (any shape; strides in elements as for decode_attn);
+                        v_pool None for MLA. The inputs are not modified.
+        """
+        k_new = np.ascontiguousarray(k_new, dtype=np.uint16)
+        B, q_len, Hkv, D_k = k_new.shape
+        v_new = None if v_new is None else np.ascontiguousarray(v_new, dtype=np.uint16)
+        D_v = D_k if v_new is None else v_new.shape[3]
+        k_out = np.array(np.asarray(k_pool).view(np.uint16), copy=True, order="C")
+        v_out = None if v_pool is None else np.array(np.asarray(v_pool).view(np.uint16),
+                                                     copy=True, order="C")
+        bt = np.ascontiguousarray(block_table, dtype=np.int32)
+        sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        assert bt.ndim == 2 and bt.shape[0] == B and sl.shape == (B,)
+        u16p = ctypes.POINTER(ctypes.c_uint16)
+        none = ctypes.cast(None, u16p)
+        st = self._lib.zl_oracle_kv_append(
+            _ptr(k_new, ctypes.c_uint16), _ptr(v_new, ctypes.c_uint16) if v_new is not None else none,
+            _ptr(k_out, ctypes.c_uint16), _ptr(v_out, ctypes.c_uint16) if v_out is not None else none,
+            int(strides[0]), int(strides[1]), int(strides[2]), _ptr(bt, ctypes.c_int32),
+            bt.shape[1], _ptr(sl, ctypes.c_int32), B, q_len, Hkv, D_k, int(D_v), int(page_size),
+            int(num_pages))
+        return k_out, v_out, int(st)
 
     def lse_merge(self, parts, lses):
         """Merge S normalised partials ``parts`` [S, D] with their ``lses`` [S]."""

@@ -231,6 +231,56 @@ void zl_oracle_lse_merge(const double* parts, const double* lses, int S, int D, 
   *lse_out = M + log(sum_c);
 }
 
+/*
+ * Paged KV append: store the q_len new tokens of every sequence in their page
+ * slots, the step that precedes decode attention. The new K and V rows are
+ * what the fused QKV projection produces ("ZhiLight: Zhihu's CUDA Inference
+ * Engine ...", section "Dual streams, host all-reduce and the memory model":
+ * fused kernels for qkv; "ZhiLight：知乎开源的高性能 LLM 推理加速引擎", section
+ * "3. 自研 Fusion Kernel": QKV fusion). The pages do not spell the append out;
+ * the plain reading used here: seq_lens[b] counts the tokens after the
+ * append, so new token i (< q_len) is logical position t = L_b - q_len + i and
+ * goes to slot t mod P of physical page block_table[b, t / P], kv head kh.
+ *
+ *   k_new   bf16 bits [B, q_len, Hkv, D_k], contiguous
+ *   v_new   bf16 bits [B, q_len, Hkv, D_v], or NULL (MLA: the latent row only)
+ *   k_pool, v_pool   pools addressed as in zl_oracle_decode_attn (updated in place)
+ * Errors, per sequence: L_b < q_len or L_b > max_pages * P -> nothing of b is
+ * written, bit 2; per token: a page id outside [0, num_pages) -> that token is
+ * not written, bit 1. Returns the OR of the bits.
+ */
+int zl_oracle_kv_append(const uint16_t* k_new, const uint16_t* v_new, uint16_t* k_pool,
+                        uint16_t* v_pool, int64_t page_stride, int64_t token_stride,
+                        int64_t head_stride, const int32_t* block_table, int64_t bt_stride,
+                        const int32_t* seq_lens, int B, int q_len, int Hkv, int D_k, int D_v,
+                        int page_size, int num_pages) {
+  int status = 0;
+  int64_t capacity = bt_stride * (int64_t)page_size;
+  for (int b = 0; b < B; ++b) {
+    int64_t L = seq_lens[b];
+    if (L < q_len || L > capacity) {
+      status |= ZL_ORACLE_BAD_LEN;
+      continue;
+    }
+    for (int i = 0; i < q_len; ++i) {
+      int64_t t = L - q_len + i;
+      int64_t page = block_table[(int64_t)b * bt_stride + t / page_size];
+      if (page < 0 || page >= num_pages) {
+        status |= ZL_ORACLE_BAD_PAGE;
+        continue;
+      }
+      for (int kh = 0; kh < Hkv; ++kh) {
+        int64_t dst = pool_row(page, t % page_size, kh, page_stride, token_stride, head_stride);
+        int64_t src_row = ((int64_t)b * q_len + i) * Hkv + kh;
+        for (int d = 0; d < D_k; ++d) k_pool[dst + d] = k_new[src_row * D_k + d];
+        if (v_new)
+          for (int d = 0; d < D_v; ++d) v_pool[dst + d] = v_new[src_row * D_v + d];
+      }
+    }
+  }
+  return status;
+}
+
 /* Threads the OpenMP runtime would use by default (1 without OpenMP). */
 int zl_oracle_max_threads(void) {
 #ifdef _OPENMP

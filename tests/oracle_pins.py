@@ -384,9 +384,84 @@ def pin_degenerate(oracle):
     assert st & 2 and np.all(out[0] == 0) and np.all(lse[0] == -np.inf)
 
 
+def _append_inputs(case, q_len):
+    """New-token rows of a PagedCase and its pools with those rows overwritten by
+    junk (the state before the append). Pure numpy indexing."""
+    knew = np.stack([case.k[b][L - q_len:] for b, L in enumerate(case.lens)])
+    vnew = None if case.mla else np.stack([np.ascontiguousarray(case.v[b][L - q_len:])
+                                           for b, L in enumerate(case.lens)])
+    junk = np.uint16(0x7F81)                      # a NaN pattern that no input holds
+    kb = case.k_pool.copy()
+    vb = None if case.mla else case.v_pool.copy()
+    for b, L in enumerate(case.lens):
+        for t in range(L - q_len, L):
+            page, slot = case.table[b, t // case.P], t % case.P
+            for arr in (kb, vb):
+                if arr is None:
+                    continue
+                if case.layout == "NHD":
+                    arr[page, slot] = junk
+                else:
+                    arr[page, :, slot] = junk
+    return bf16_bits(knew), None if vnew is None else bf16_bits(vnew), kb, vb
+
+
+def pin_kv_append(oracle):
+    """Appending the last q_len tokens of every sequence to pools that lack them
+    gives, bit for bit, the pools built directly from the dense K/V (every other
+    element untouched), for both layouts and for the latent-only (MLA) pool."""
+    rng = np.random.default_rng(26)
+    for q_len, layout, mla in ((1, "NHD", False), (3, "NHD", False), (2, "HND", False),
+                               (4, "NHD", True)):
+        lens = [20, 9, 33, 5]
+        case = PagedCase(rng, lens, 4, 2, 16, 8, q_len=q_len, layout=layout, mla=mla,
+                         D_v=8 if mla else None)
+        knew, vnew, kb, vb = _append_inputs(case, q_len)
+        assert not np.array_equal(kb, case.k_pool)
+        ko, vo, st = oracle.kv_append(knew, vnew, kb, vb, case.strides, case.table,
+                                      np.array(lens, dtype=np.int32), page_size=case.P,
+                                      num_pages=case.num_pages)
+        assert st == 0
+        assert np.array_equal(ko, case.k_pool), ("K pool", q_len, layout)
+        if mla:
+            assert vo is None
+        else:
+            assert np.array_equal(vo, case.v_pool), ("V pool", q_len, layout)
+
+
+def pin_kv_append_errors(oracle):
+    """A sequence shorter than q_len writes nothing (bit 2); a bad page id skips
+    only its token (bit 1); the other sequences are appended as usual."""
+    rng = np.random.default_rng(27)
+    q_len = 3
+    case = PagedCase(rng, [12, 19, 30], 2, 2, 8, 4, q_len=q_len)
+    knew, vnew, kb, vb = _append_inputs(case, q_len)
+    lens = np.array(case.lens, dtype=np.int32)
+    short = lens.copy()
+    short[0] = 2
+    ko, vo, st = oracle.kv_append(knew, vnew, kb, vb, case.strides, case.table, short,
+                                  page_size=4, num_pages=case.num_pages)
+    assert st == 2
+    own0 = case.table[0, :3]
+    assert np.array_equal(ko[own0], kb[own0]) and np.array_equal(vo[own0], vb[own0])
+    rest = np.setdiff1d(np.arange(case.num_pages), own0)
+    assert np.array_equal(ko[rest], case.k_pool[rest])
+    table = case.table.copy()
+    last = (case.lens[2] - 1) // 4
+    good_page = table[2, last]
+    table[2, last] = -1                   # the page of sequence 2's newest tokens
+    ko, vo, st = oracle.kv_append(knew, vnew, kb, vb, case.strides, table, lens, page_size=4,
+                                  num_pages=case.num_pages)
+    assert st == 1
+    assert np.array_equal(ko[good_page], kb[good_page])
+    others = np.setdiff1d(np.arange(case.num_pages), [good_page])
+    assert np.array_equal(ko[others], case.k_pool[others])
+    assert np.array_equal(vo[others], case.v_pool[others])
+
+
 ALL_PINS = [
     pin_sdpa_dense, pin_gqa_head_mapping, pin_softmax_onehot, pin_large_scores,
     pin_single_token, pin_constant_v, pin_zero_query, pin_token_permutation, pin_page_remap,
     pin_layout, pin_split_merge, pin_mla, pin_mla_absorption, pin_multi_token_causal,
-    pin_degenerate,
+    pin_degenerate, pin_kv_append, pin_kv_append_errors,
 ]

@@ -36,6 +36,18 @@ MUTANTS = [
     ("wrong_v_page_index", "int32_t page = bt_row[t / page_size];\n"
                            "    const uint16_t* v_row",
      "int32_t page = bt_row[(t / page_size) / 2];\n    const uint16_t* v_row"),
+    # KV append (every variant keeps its writes inside the pools)
+    ("append_reversed_tokens", "int64_t t = L - q_len + i;", "int64_t t = L - 1 - i;"),
+    ("append_wrong_slot",
+     "pool_row(page, t % page_size, kh, page_stride, token_stride, head_stride);\n"
+     "        int64_t src_row",
+     "pool_row(page, (t + 1) % page_size, kh, page_stride, token_stride, head_stride);\n"
+     "        int64_t src_row"),
+    ("append_head_swap", "int64_t src_row = ((int64_t)b * q_len + i) * Hkv + kh;",
+     "int64_t src_row = ((int64_t)b * q_len + i) * Hkv + (Hkv - 1 - kh);"),
+    ("append_v_from_k", "v_pool[dst + d] = v_new[src_row * D_v + d];",
+     "v_pool[dst + d] = k_new[src_row * D_v + d];"),
+    ("append_bad_page_silent", "status |= ZL_ORACLE_BAD_PAGE;\n        continue;", "continue;"),
 ]
 
 
