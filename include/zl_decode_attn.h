@@ -170,6 +170,45 @@ zl_status zl_decode_attn_mla_workspace_size(const zl_decode_attn_params* params,
 #define ZL_NOALLOC_WORKSPACE_BYTES (8u << 20)
 zl_status zl_decode_attn_noalloc(const zl_decode_attn_params* params, zl_stream_t stream);
 
+/*
+ * Paged KV append: store the q_len new tokens of every sequence (the K and V
+ * rows the fused QKV projection produced; "ZhiLight: Zhihu's CUDA Inference
+ * Engine ...", section "Dual streams, host all-reduce and the memory model",
+ * lists fused kernels for qkv beside the decode attention) in their page
+ * slots, before zl_decode_attn / zl_decode_attn_mla reads them. seq_lens[b]
+ * counts the tokens after the append, so new token i (< q_len) of sequence b
+ * is logical position t = seq_lens[b] - q_len + i: slot t % page_size of
+ * physical page block_table[b, t / page_size]. The pages assign no pages; the
+ * caller's block table must already map position t.
+ *   - Pools, strides, block table and seq_lens mean exactly what they mean in
+ *     zl_decode_attn_params (the same buffers can be passed to both calls).
+ *     v_pool = NULL and v_new = NULL for a latent-only (MLA) pool.
+ *   - k_new: bf16 [B, q_len, Hkv, D_k], v_new: bf16 [B, q_len, Hkv, D_v],
+ *     contiguous, 16-byte aligned; D_k, D_v multiples of 8, <= 1024 (D_v <= D_k
+ *     is not required: each pool row is as wide as its own new row).
+ *   - Device data errors: seq_lens[b] < q_len or > block_table_stride *
+ *     page_size writes nothing of sequence b (ZL_DEVERR_BAD_SEQ_LEN); a page
+ *     id outside [0, num_pages) skips that token (ZL_DEVERR_BAD_PAGE).
+ *   - Every written element is a copy: the result is bit-exact.
+ *   - The writes are ordinary stores on the given stream; a decode call
+ *     enqueued after it on the same stream sees them.
+ */
+typedef struct {
+  size_t struct_size; /* sizeof(zl_kv_append_params) */
+  const void* k_new;
+  const void* v_new;
+  void* k_pool;
+  void* v_pool;
+  int64_t page_stride, token_stride, head_stride;
+  const int32_t* block_table;
+  int64_t block_table_stride;
+  const int32_t* seq_lens;
+  int32_t B, q_len, Hkv, D_k, D_v, page_size, num_pages;
+  uint32_t* err_flags; /* optional, as in zl_decode_attn_params */
+} zl_kv_append_params;
+
+zl_status zl_kv_append(const zl_kv_append_params* params, zl_stream_t stream);
+
 /* Static description of a status code. */
 const char* zl_status_string(zl_status status);
 

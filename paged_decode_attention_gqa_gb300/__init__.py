@@ -24,9 +24,9 @@ import torch
 from ._build import LIB_PATH, build  # noqa: F401  (build() is the public build step)
 
 __all__ = [
-    "ZlError", "Params", "lib", "decode_attn", "decode_attn_mla", "workspace_size",
-    "workspace_size_mla", "call", "call_noalloc", "build", "LIB_PATH", "DEVERR_BAD_PAGE", "DEVERR_BAD_SEQ_LEN",
-    "DEVERR_TIMEOUT", "HEADER", "declared_symbols",
+    "ZlError", "Params", "AppendParams", "lib", "decode_attn", "decode_attn_mla", "kv_append",
+    "workspace_size", "workspace_size_mla", "call", "call_noalloc", "build", "LIB_PATH",
+    "DEVERR_BAD_PAGE", "DEVERR_BAD_SEQ_LEN", "DEVERR_TIMEOUT", "HEADER", "declared_symbols",
 ]
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
@@ -76,6 +76,31 @@ class Params(ctypes.Structure):
     ]
 
 
+class AppendParams(ctypes.Structure):
+    """Mirror of zl_kv_append_params."""
+    _fields_ = [
+        ("struct_size", ctypes.c_size_t),
+        ("k_new", ctypes.c_void_p),
+        ("v_new", ctypes.c_void_p),
+        ("k_pool", ctypes.c_void_p),
+        ("v_pool", ctypes.c_void_p),
+        ("page_stride", ctypes.c_int64),
+        ("token_stride", ctypes.c_int64),
+        ("head_stride", ctypes.c_int64),
+        ("block_table", ctypes.c_void_p),
+        ("block_table_stride", ctypes.c_int64),
+        ("seq_lens", ctypes.c_void_p),
+        ("B", ctypes.c_int32),
+        ("q_len", ctypes.c_int32),
+        ("Hkv", ctypes.c_int32),
+        ("D_k", ctypes.c_int32),
+        ("D_v", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("num_pages", ctypes.c_int32),
+        ("err_flags", ctypes.c_void_p),
+    ]
+
+
 _lib = None
 _lib_lock = threading.Lock()
 
@@ -99,6 +124,8 @@ def lib():
                 fn = getattr(handle, name)
                 fn.restype = ctypes.c_int
                 fn.argtypes = [P, ctypes.POINTER(ctypes.c_size_t)]
+            handle.zl_kv_append.restype = ctypes.c_int
+            handle.zl_kv_append.argtypes = [ctypes.POINTER(AppendParams), ctypes.c_void_p]
             handle.zl_status_string.restype = ctypes.c_char_p
             handle.zl_status_string.argtypes = [ctypes.c_int]
             _lib = handle
@@ -254,3 +281,47 @@ def decode_attn_mla(q, kv_pool, block_table, seq_lens, *, page_size, scale, D_v=
                 scale=scale, Hkv=1, D_v=D_v, out=out, lse=lse, workspace=workspace,
                 err_flags=err_flags, num_ctas=num_ctas, max_seq_len=max_seq_len, layout="NHD",
                 stream=stream, events=events)
+
+
+def make_append_params(k_new, v_new, k_pool, v_pool, block_table, seq_lens, *, page_size,
+                       layout="NHD", err_flags=None) -> AppendParams:
+    B, q_len, Hkv, D_k = k_new.shape
+    ps, ts, hs = _pool_strides(k_pool, layout)
+    if (v_pool is None) != (v_new is None):
+        raise ValueError("v_new and v_pool are given together (both None for a latent-only pool)")
+    if v_pool is not None and _pool_strides(v_pool, layout) != (ps, ts, hs):
+        raise ValueError("K and V pools must share strides")
+    if not k_new.is_contiguous() or (v_new is not None and not v_new.is_contiguous()):
+        raise ValueError("k_new and v_new must be contiguous")
+    if k_pool.stride(3) != 1 or block_table.stride(1) != 1:
+        raise ValueError("pool rows and block_table rows must be contiguous")
+    p = AppendParams()
+    p.struct_size = ctypes.sizeof(AppendParams)
+    p.k_new, p.v_new, p.k_pool, p.v_pool = _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool)
+    p.page_stride, p.token_stride, p.head_stride = ps, ts, hs
+    p.block_table = _ptr(block_table)
+    p.block_table_stride = block_table.stride(0)
+    p.seq_lens = _ptr(seq_lens)
+    p.B, p.q_len, p.Hkv, p.D_k = B, q_len, Hkv, D_k
+    p.D_v = 0 if v_new is None else v_new.shape[3]
+    p.page_size = page_size
+    p.num_pages = k_pool.shape[0]
+    p.err_flags = _ptr(err_flags)
+    return p
+
+
+def kv_append(k_new, v_new, k_pool, v_pool, block_table, seq_lens, *, page_size, layout="NHD",
+              err_flags=None, stream=None):
+    """Paged KV append (zl_kv_append): new token i of sequence b goes to logical
+    position seq_lens[b] - q_len + i of its cache, in place.
+
+    k_new [B, q_len, Hkv, D_k] bf16, v_new [B, q_len, Hkv, D_v] bf16 or None
+    (latent-only pool, v_pool None); pools, block_table and seq_lens as for
+    decode_attn (seq_lens count the new tokens).
+    """
+    p = make_append_params(k_new, v_new, k_pool, v_pool, block_table, seq_lens,
+                           page_size=page_size, layout=layout, err_flags=err_flags)
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    _check(lib().zl_kv_append(ctypes.byref(p), ctypes.c_void_p(stream.cuda_stream)),
+           "zl_kv_append")

@@ -118,6 +118,14 @@ def _normal_bf16(seed: int, key: int, shape, scale_channels=None, factor=8.0) ->
     return flat.view(*shape)
 
 
+def new_token_rows(seed: int, B: int, q_len: int, Hkv: int, D_k: int, D_v: int | None = None):
+    """The new tokens' K and V rows for a KV append, bf16 N(0,1):
+    k_new [B, q_len, Hkv, D_k] and v_new [B, q_len, Hkv, D_v] (None when D_v is None)."""
+    k_new = _normal_bf16(seed, 11, (B, q_len, Hkv, D_k))
+    v_new = None if D_v is None else _normal_bf16(seed, 12, (B, q_len, Hkv, D_v))
+    return k_new, v_new
+
+
 def _poison_pool(pool_nhd: torch.Tensor, used_pages: np.ndarray, tails) -> None:
     """NaN into unreferenced pages and tail slots (pool in [page, slot, head, dim])."""
     nan = torch.tensor(BF16_NAN, dtype=torch.int16).view(torch.bfloat16)
@@ -217,9 +225,11 @@ def tiny_gqa(seed=1001, layout="NHD", poison=True, values=True) -> Workload:
                           scale=1.0 / math.sqrt(128), layout=layout, poison=poison, values=values)
 
 
-def llama3_8b_decode(seed=1002, layout="NHD", poison=True, B=64, values=True) -> Workload:
+def llama3_8b_decode(seed=1002, layout="NHD", poison=True, B=64, values=True,
+                     q_len=1) -> Workload:
     """Llama-3-8B attention shape: 64 seqs, 32 query / 8 KV heads, D 128,
-    lengths U[512, 4096], page 16, pool 1.25x, 4 of 128 K channels scaled x8."""
+    lengths U[512, 4096], page 16, pool 1.25x, 4 of 128 K channels scaled x8.
+    q_len > 1: that many new query tokens per sequence (speculative decode)."""
     rng = _structure_rng(seed)
     lens = rng.integers(512, 4096, size=B, endpoint=True).astype(np.int32)
     pages = int(((lens + 15) // 16).sum())
@@ -230,7 +240,7 @@ def llama3_8b_decode(seed=1002, layout="NHD", poison=True, B=64, values=True) ->
                           seq_lens=lens, block_table=table, num_pages=num_pages,
                           scale=1.0 / math.sqrt(128), layout=layout, k_scale_channels=channels,
                           poison=poison, notes={"k_scaled_channels": channels.tolist()},
-                          values=values)
+                          values=values, q_len=q_len)
 
 
 def llama70b_prefix_decode(seed=1003, layout="NHD", poison=True, sigma=1.0, values=True) -> Workload:

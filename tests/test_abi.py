@@ -105,3 +105,41 @@ def _mla_params(**over):
 def test_mla_host_validation(over, code):
     p = _mla_params(**over)
     assert zl.lib().zl_decode_attn_mla(ctypes.byref(p), None) == code
+
+
+def _append_params(**over):
+    """A valid-looking zl_kv_append parameter block with fake aligned pointers."""
+    p = zl.AppendParams()
+    p.struct_size = ctypes.sizeof(zl.AppendParams)
+    fake = 1 << 20
+    p.k_new = p.v_new = p.k_pool = p.v_pool = p.block_table = p.seq_lens = fake
+    p.page_stride, p.token_stride, p.head_stride = 16 * 8 * 128, 8 * 128, 128
+    p.block_table_stride = 8
+    p.B, p.q_len, p.Hkv, p.D_k, p.D_v, p.page_size, p.num_pages = 4, 1, 8, 128, 128, 16, 64
+    for k, v in over.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("over", [
+    dict(struct_size=8), dict(B=0), dict(q_len=0), dict(Hkv=0), dict(page_size=0),
+    dict(num_pages=0), dict(block_table_stride=0), dict(D_k=12), dict(D_k=2048), dict(D_v=4),
+    dict(k_new=None), dict(k_pool=None), dict(block_table=None), dict(seq_lens=None),
+    dict(v_new=None),                        # V pool without new V rows
+    dict(v_pool=None),                       # new V rows without a V pool
+    dict(k_new=(1 << 20) + 8),               # misaligned
+    dict(seq_lens=(1 << 20) + 2),
+    dict(token_stride=100), dict(head_stride=0),
+])
+def test_append_host_validation(over):
+    p = _append_params(**over)
+    assert zl.lib().zl_kv_append(ctypes.byref(p), None) == zl.ERR_INVALID_ARG
+
+
+def test_append_null_params_and_no_cpu_fallback():
+    assert zl.lib().zl_kv_append(None, None) == zl.ERR_INVALID_ARG
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    for over in (dict(), dict(v_new=None, v_pool=None, D_k=576, D_v=0)):
+        p = _append_params(**over)
+        assert zl.lib().zl_kv_append(ctypes.byref(p), None) == zl.ERR_CUDA
