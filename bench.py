@@ -77,17 +77,24 @@ def kv_bytes(w):
 def io_bytes(w):
     """Q read + out written + block table and seq_lens read (per launch)."""
     pages = int(((w.seq_lens.astype(np.int64) + w.page_size - 1) // w.page_size).sum())
-    return w.B * w.Hq * (w.D_qk + w.D_v) * 2 + pages * 4 + w.B * 4
+    return w.B * w.q_len * w.Hq * (w.D_qk + w.D_v) * 2 + pages * 4 + w.B * 4
 
 
-def metric_name(workload):
+def metric_name(workload, q_len=1):
+    if q_len != 1:
+        return f"decode-attn KV read GB/s ({workload}, {q_len} query tokens)"
     return METRIC if workload == WORKLOAD else f"decode-attn KV read GB/s ({workload})"
 
 
-def make_workload(name, batch=None):
+def make_workload(name, batch=None, q_len=1):
     from paged_decode_attention_gqa_gb300 import workloads
     fn = workloads.WORKLOADS[name]
-    return fn(B=batch) if batch else fn()
+    kw = {}
+    if batch:
+        kw["B"] = batch
+    if q_len != 1:
+        kw["q_len"] = q_len
+    return fn(**kw)
 
 
 class ClockSampler:
@@ -181,7 +188,7 @@ def run_reference(args, world, rank, budget_s=120.0):
     if rank != 0:
         return
     from paged_decode_attention_gqa_gb300 import workloads
-    w = make_workload(args.workload, args.batch)
+    w = make_workload(args.workload, args.batch, args.q_len)
     import oracle
     orc = oracle.load()
     threads = cpu_cores()
@@ -210,7 +217,7 @@ def run_reference(args, world, rank, budget_s=120.0):
     sample = (f"first {n} of {w.B} sequences per step (all heads), "
               f"{int(w.seq_lens[:n].sum())} tokens")
     line = {
-        "impl": "reference", "metric": metric_name(args.workload), "value": gbs, "unit": UNIT, "n_gpus": world,
+        "impl": "reference", "metric": metric_name(args.workload, args.q_len), "value": gbs, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": config_of(w, world),
@@ -246,19 +253,20 @@ def run_ours(args, world, rank, local):
         dist.barrier()
     zl.lib()
 
-    w = make_workload(args.workload, args.batch)
+    w = make_workload(args.workload, args.batch, args.q_len)
     kind = "mla" if w.mla else "gqa"
     q, k = w.q.to(dev), w.k_pool.to(dev)
     v = None if w.mla else w.v_pool.to(dev)
     bt = torch.from_numpy(w.block_table).to(dev)
     sl = torch.from_numpy(w.seq_lens).to(dev)
-    out = torch.empty(w.B, 1, w.Hq, w.D_v, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty(w.B, 1, w.Hq, dtype=torch.float32, device=dev)
+    out = torch.empty(w.B, w.q_len, w.Hq, w.D_v, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(w.B, w.q_len, w.Hq, dtype=torch.float32, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     p = zl.make_params(q, k, v, bt, sl, out, page_size=w.page_size, scale=w.scale, Hkv=w.Hkv,
-                       D_v=w.D_v, lse=lse, err_flags=err, max_seq_len=w.max_seq_len)
+                       D_v=w.D_v, lse=lse, err_flags=err, max_seq_len=w.max_seq_len,
+                       single_launch=args.single_launch and not w.mla)
     need = zl.workspace_size_mla(p) if w.mla else zl.workspace_size(p)
-    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
     p.workspace, p.workspace_bytes = ws.data_ptr(), ws.numel()
     stream = torch.cuda.current_stream()
     # Small working sets are flushed from L2 between steps (a 2x L2 write).
@@ -277,18 +285,6 @@ def run_ours(args, world, rank, local):
     assert int(err.item()) == 0, f"device error flags {int(err.item())}"
 
     # ---- timed region: K steps, CUDA events on the launching stream, clocks sampled
-    n_ev = min(args.steps, 1000)
-    every = max(1, args.steps // n_ev)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(n_ev)]
-    # torch only reports elapsed time for events it has recorded itself; record
-    # each once here, the library re-records them around the attention kernel.
-    for a, b in evs:
-        a.record(stream)
-        b.record(stream)
-    # whole-call events (attention + merge), excluding any L2 flush
-    call_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(n_ev)]
     sampler = ClockSampler(local)
     if not args.no_clocks:
         sampler.start()
@@ -298,33 +294,46 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_begin.record(stream)
-    used = 0
-    for i in range(args.steps):
-        if i % every == 0 and used < n_ev:
-            p.attn_begin, p.attn_end = evs[used][0].cuda_event, evs[used][1].cuda_event
-            if flush is not None:
-                flush.zero_()
-            call_evs[used][0].record(stream)
-            zl.call(p, mla=w.mla, stream=stream)
-            call_evs[used][1].record(stream)
-            used += 1
-        else:
-            p.attn_begin = p.attn_end = None
-            step()
+    for _ in range(args.steps):
+        step()
     t_end.record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
     ms = t_begin.elapsed_time(t_end) / args.steps
-    p.attn_begin = p.attn_end = None
-    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in evs[:used])
-    call_ms = statistics.mean(a.elapsed_time(b) for a, b in call_evs[:used])
     if world > 1:
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
-    launches = args.steps * (2 if kind == "gqa" else 1)   # attention (+ merge)
+    # attention + merge: one launch with ZL_DECODE_SINGLE_LAUNCH, else two (MLA: two)
+    launches = args.steps * (1 if (kind == "gqa" and args.single_launch) else 2)
     if flush is not None:
         launches += args.steps                              # the L2 flush memset
+
+    # ---- per-kernel timing, after the timed region: the library records
+    # events around the attention kernel alone, the bench around the call.
+    # (Events between the two launches would keep the merge from starting
+    # early, so the headline steps above carry none.)
+    n_ev = max(10, min(args.steps, 1000))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n_ev)]
+    # torch only reports elapsed time for events it has recorded itself; record
+    # each once here, the library re-records them around the attention kernel.
+    for a, b in evs:
+        a.record(stream)
+        b.record(stream)
+    call_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(n_ev)]
+    for i in range(n_ev):
+        p.attn_begin, p.attn_end = evs[i][0].cuda_event, evs[i][1].cuda_event
+        if flush is not None:
+            flush.zero_()
+        call_evs[i][0].record(stream)
+        zl.call(p, mla=w.mla, stream=stream)
+        call_evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    p.attn_begin = p.attn_end = None
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    call_ms = statistics.mean(a.elapsed_time(b) for a, b in call_evs)
 
     # ---- end to end through the public API: host inputs in, host result out
     e2e = None
@@ -349,7 +358,8 @@ def run_ours(args, world, rank, local):
                                    out=out, workspace=ws, max_seq_len=w.max_seq_len)
             else:
                 zl.decode_attn(q, k, v, bt, sl, page_size=w.page_size, scale=w.scale, out=out,
-                               workspace=ws, max_seq_len=w.max_seq_len)
+                               workspace=ws, max_seq_len=w.max_seq_len,
+                               single_launch=args.single_launch)
             pin_out.copy_(out, non_blocking=True)
         torch.cuda.synchronize()
         e2e_s = (time.perf_counter() - t0) / e2e_steps
@@ -374,7 +384,7 @@ def run_ours(args, world, rank, local):
         cpu = {"value": kvb / cpu_s / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"the whole workload per call, {cpu_calls} calls (median)"}
     line = {
-        "metric": metric_name(args.workload),
+        "metric": metric_name(args.workload, args.q_len),
         "value": kvb * world / (ms * 1e-3) / 1e9,
         "unit": UNIT,
         "n_gpus": world,
@@ -389,7 +399,9 @@ def run_ours(args, world, rank, local):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": config_of(w, world),
+        "config": dict(config_of(w, world), split_merge=(
+            "in the attention kernel (single launch)" if kind == "gqa" and args.single_launch
+            else "second launch" + (" (programmatic dependent launch)" if kind == "gqa" else ""))),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "kernel": f"{kind}_decode_kernel", "attn_us_per_launch": attn_ms * 1e3,
@@ -419,6 +431,10 @@ def main():
                     help="workload to time (the bench line is the default one; others are "
                          "for per-workload tables and profiling)")
     ap.add_argument("--batch", type=int, default=None, help="override the batch size")
+    ap.add_argument("--single-launch", action="store_true",
+                    help="GQA: merge split-KV partials inside the attention kernel")
+    ap.add_argument("--q-len", type=int, default=1,
+                    help="query tokens per sequence (llama3_8b_decode only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")

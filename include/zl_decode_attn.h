@@ -100,7 +100,14 @@ typedef struct {
   float scale; /* softmax scale, e.g. 1/sqrt(D) */
 
   /* Caller-owned device scratch of at least zl_decode_attn_workspace_size()
-     bytes, 256-byte aligned. Contents need no initialisation. */
+     bytes, 256-byte aligned.
+     zl_decode_attn with ZL_DECODE_SINGLE_LAUNCH: zero-fill it once before
+     its first use (e.g. with cudaMemsetAsync). It starts with one arrival
+     counter per (sequence, kv head) that the in-kernel merge counts up and
+     returns to zero, so every call leaves it ready for the next; counters
+     left by a call that stopped on a device error are recognised and
+     ignored. Writing other data into it (another entry point, another use)
+     needs a new zero fill. Otherwise: contents need no initialisation. */
   void* workspace;
   size_t workspace_bytes;
 
@@ -113,9 +120,20 @@ typedef struct {
   int32_t num_ctas;
 
   /* Optional profiling events recorded on the stream immediately before and
-     after the attention kernel (not the merge); NULL to skip. */
+     after the attention kernel (not the split-KV merge when that is a second
+     launch); NULL to skip. */
   zl_event_t attn_begin, attn_end;
+
+  /* ZL_DECODE_* bits; 0 for the defaults. */
+  uint32_t flags;
 } zl_decode_attn_params;
+
+/* zl_decode_attn: merge the split-KV partials inside the attention kernel
+   (the last CTA to finish a piece of a (sequence, kv head) merges it, in a
+   fixed order), so the call is one launch. Without it the merge is a second,
+   programmatically dependent launch. Both give bit-identical results.
+   zl_decode_attn_mla accepts no flags. */
+#define ZL_DECODE_SINGLE_LAUNCH 1u
 
 /*
  * GQA / MHA / MQA decode over separate K and V pools.
@@ -162,10 +180,11 @@ zl_status zl_decode_attn_mla_workspace_size(const zl_decode_attn_params* params,
  *   - The first call on each device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
  *   - Calls allocate nothing: no cudaMalloc, cudaFree or allocating library
- *     routine. All calls share the one array, which keeps the last call's
- *     contents; nothing in it needs clearing (each launch writes what it later
- *     reads). Calls that overlap on the GPU (other streams, other threads)
- *     race on it: serialise them.
+ *     routine. All calls share the one array, which starts zero-filled and
+ *     keeps the last call's contents; every call leaves its arrival counters
+ *     at zero, as the workspace contract of zl_decode_attn asks, so it never
+ *     needs clearing. Calls that overlap on the GPU (other streams, other
+ *     threads) race on it: serialise them.
  */
 #define ZL_NOALLOC_WORKSPACE_BYTES (8u << 20)
 zl_status zl_decode_attn_noalloc(const zl_decode_attn_params* params, zl_stream_t stream);

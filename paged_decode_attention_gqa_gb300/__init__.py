@@ -33,6 +33,7 @@ HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))
                       "zl_decode_attn.h")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA = range(5)
+SINGLE_LAUNCH = 1  # ZL_DECODE_SINGLE_LAUNCH
 DEVERR_BAD_PAGE, DEVERR_BAD_SEQ_LEN, DEVERR_TIMEOUT = 1, 2, 4
 
 
@@ -73,6 +74,7 @@ class Params(ctypes.Structure):
         ("num_ctas", ctypes.c_int32),
         ("attn_begin", ctypes.c_void_p),
         ("attn_end", ctypes.c_void_p),
+        ("flags", ctypes.c_uint32),
     ]
 
 
@@ -161,7 +163,7 @@ def _pool_strides(pool: torch.Tensor, layout: str):
 
 def make_params(q, k_pool, v_pool, block_table, seq_lens, out, *, page_size, scale, Hkv,
                 D_v, lse=None, workspace=None, err_flags=None, num_ctas=0, max_seq_len=0,
-                layout="NHD", events=None) -> Params:
+                layout="NHD", events=None, single_launch=False) -> Params:
     B, q_len, Hq, D_qk = q.shape
     ps, ts, hs = _pool_strides(k_pool, layout)
     if v_pool is not None and _pool_strides(v_pool, layout) != (ps, ts, hs):
@@ -187,8 +189,11 @@ def make_params(q, k_pool, v_pool, block_table, seq_lens, out, *, page_size, sca
         p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     p.err_flags = _ptr(err_flags)
     p.num_ctas = int(num_ctas)
+    p.flags = SINGLE_LAUNCH if single_launch else 0
     if events is not None:
         p.attn_begin, p.attn_end = events[0].cuda_event, events[1].cuda_event
+    # The struct holds raw device pointers: keep the tensors alive with it.
+    p.tensors = (q, k_pool, v_pool, block_table, seq_lens, out, lse, workspace, err_flags, events)
     return p
 
 
@@ -209,12 +214,14 @@ def workspace_size_mla(params: Params) -> int:
 _ws_cache: dict = {}
 
 
-def _workspace(device, nbytes):
-    """A cached device byte buffer of at least nbytes (256-byte aligned by torch)."""
-    key = (device.type, device.index)
+def _workspace(device, nbytes, kind):
+    """A cached, zero-filled device byte buffer of at least nbytes per (device,
+    entry point). GQA calls leave their counters at zero, so the buffer stays
+    valid for the next GQA call; MLA calls get a buffer of their own."""
+    key = (device.type, device.index, kind)
     buf = _ws_cache.get(key)
     if buf is None or buf.numel() < nbytes:
-        buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
         _ws_cache[key] = buf
     return buf
 
@@ -238,15 +245,16 @@ def call(params: Params, *, mla: bool, stream=None):
 
 
 def _run(q, k_pool, v_pool, block_table, seq_lens, *, mla, page_size, scale, Hkv, D_v, out, lse,
-         workspace, err_flags, num_ctas, max_seq_len, layout, stream, events):
+         workspace, err_flags, num_ctas, max_seq_len, layout, stream, events, single_launch=False):
     if out is None:
         out = torch.empty(q.shape[:3] + (D_v,), dtype=torch.bfloat16, device=q.device)
     p = make_params(q, k_pool, v_pool, block_table, seq_lens, out, page_size=page_size,
                     scale=scale, Hkv=Hkv, D_v=D_v, lse=lse, err_flags=err_flags,
-                    num_ctas=num_ctas, max_seq_len=max_seq_len, layout=layout, events=events)
+                    num_ctas=num_ctas, max_seq_len=max_seq_len, layout=layout, events=events,
+                    single_launch=single_launch)
     need = workspace_size_mla(p) if mla else workspace_size(p)
     if workspace is None:
-        workspace = _workspace(q.device, need)
+        workspace = _workspace(q.device, need, "mla" if mla else "gqa")
     p.workspace = workspace.data_ptr()
     p.workspace_bytes = workspace.numel() * workspace.element_size()
     call(p, mla=mla, stream=stream)
@@ -255,18 +263,21 @@ def _run(q, k_pool, v_pool, block_table, seq_lens, *, mla, page_size, scale, Hkv
 
 def decode_attn(q, k_pool, v_pool, block_table, seq_lens, *, page_size, scale, out=None, lse=None,
                 workspace=None, err_flags=None, num_ctas=0, max_seq_len=0, layout="NHD",
-                stream=None, events=None):
+                stream=None, events=None, single_launch=False):
     """GQA/MHA/MQA paged decode attention (zl_decode_attn).
 
-    q [B, 1, Hq, 128] bf16; k_pool, v_pool [pages, page_size, Hkv, 128] (layout
-    "NHD") or [pages, Hkv, page_size, 128] ("HND") bf16; block_table int32
-    [B, max_pages]; seq_lens int32 [B]. Returns out [B, 1, Hq, 128] bf16.
+    q [B, q_len, Hq, 128] bf16; k_pool, v_pool [pages, page_size, Hkv, 128]
+    (layout "NHD") or [pages, Hkv, page_size, 128] ("HND") bf16; block_table
+    int32 [B, max_pages]; seq_lens int32 [B]. Returns out [B, q_len, Hq, 128]
+    bf16. single_launch: merge split-KV partials inside the attention kernel
+    (ZL_DECODE_SINGLE_LAUNCH; the workspace must then start zeroed, which the
+    cached default workspace is).
     """
     Hkv = k_pool.shape[2] if layout == "NHD" else k_pool.shape[1]
     return _run(q, k_pool, v_pool, block_table, seq_lens, mla=False, page_size=page_size,
                 scale=scale, Hkv=Hkv, D_v=q.shape[3], out=out, lse=lse, workspace=workspace,
                 err_flags=err_flags, num_ctas=num_ctas, max_seq_len=max_seq_len, layout=layout,
-                stream=stream, events=events)
+                stream=stream, events=events, single_launch=single_launch)
 
 
 def decode_attn_mla(q, kv_pool, block_table, seq_lens, *, page_size, scale, D_v=512, out=None,
@@ -307,6 +318,7 @@ def make_append_params(k_new, v_new, k_pool, v_pool, block_table, seq_lens, *, p
     p.page_size = page_size
     p.num_pages = k_pool.shape[0]
     p.err_flags = _ptr(err_flags)
+    p.tensors = (k_new, v_new, k_pool, v_pool, block_table, seq_lens, err_flags)
     return p
 
 

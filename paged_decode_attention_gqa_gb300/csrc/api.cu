@@ -5,6 +5,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -34,6 +35,16 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
+// A different nonzero tag for every GQA call in this process: the in-kernel
+// split merge counts arrivals per tag, so counters left behind by a call that
+// stopped early (a device error) are ignored by the next call.
+uint32_t next_epoch() {
+  static std::atomic<uint32_t> counter{0};
+  uint32_t e = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+  if (e == 0) e = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+  return e;
+}
+
 struct DeviceInfo {
   int device = -1;
   int sms = 0;
@@ -58,7 +69,8 @@ zl_status current_device(DeviceInfo* info) {
 // ------------------------------------------------------------------ GQA plan
 struct GqaPlan {
   int hpc = 0, nhg = 0, g = 0, grid = 0;
-  size_t off_lse = 0, off_o = 0, bytes = 0;
+  bool fused = false;
+  size_t off_prefix = 0, off_lse = 0, off_o = 0, bytes = 0;
 };
 
 zl_status gqa_validate_shape(const zl_decode_attn_params* a) {
@@ -68,6 +80,8 @@ zl_status gqa_validate_shape(const zl_decode_attn_params* a) {
       a->num_ctas < 0 || a->max_seq_len < 0)
     return ZL_ERR_INVALID_ARG;
   if (a->Hq % a->Hkv != 0) return ZL_ERR_INVALID_ARG;
+  if (a->flags & ~uint32_t(ZL_DECODE_SINGLE_LAUNCH)) return ZL_ERR_INVALID_ARG;
+  if (a->num_ctas > 65535) return ZL_ERR_UNSUPPORTED;  // the tile cut needs G^2 < 2^32
   if (!(a->scale > 0.f) || !std::isfinite(a->scale)) return ZL_ERR_INVALID_ARG;
   if (a->D_qk != zl::kGqaHeadDim || a->D_v != zl::kGqaHeadDim) return ZL_ERR_UNSUPPORTED;
   if (a->Hq / a->Hkv * a->q_len > 16) return ZL_ERR_UNSUPPORTED;  // (query, head) rows per tile
@@ -82,12 +96,14 @@ zl_status gqa_plan(const zl_decode_attn_params* a, GqaPlan* plan) {
   DeviceInfo dev;
   if ((st = current_device(&dev)) != ZL_OK) return st;
   plan->g = a->Hq / a->Hkv;
+  plan->fused = (a->flags & ZL_DECODE_SINGLE_LAUNCH) != 0;
   plan->hpc = zl::gqa_heads_per_cta(a->Hkv);
   plan->nhg = a->Hkv / plan->hpc;
   int grid = a->num_ctas;
   if (grid == 0) {
     const int per_sm =
-        zl::gqa_ctas_per_sm(plan->hpc, plan->g * a->q_len > 8, a->q_len > 1, dev.device);
+        zl::gqa_ctas_per_sm(plan->hpc, plan->g * a->q_len > 8, a->q_len > 1, plan->fused,
+                            dev.device);
     if (per_sm < 1) return ZL_ERR_CUDA;
     grid = dev.sms * per_sm;
     if (a->max_seq_len > 0) {
@@ -99,7 +115,10 @@ zl_status gqa_plan(const zl_decode_attn_params* a, GqaPlan* plan) {
   }
   plan->grid = grid;
   const size_t rows = size_t(grid) * 2 * plan->hpc * plan->g * a->q_len;  // partial slots
-  plan->off_lse = round_up(size_t(a->B + 1) * sizeof(int32_t), 256);
+  // [0, off_prefix): one arrival counter (8 bytes) per (sequence, kv head);
+  // [off_prefix, off_lse): the tile prefix sums the merge kernel reads.
+  plan->off_prefix = round_up(size_t(a->B) * a->Hkv * sizeof(unsigned long long), 256);
+  plan->off_lse = plan->off_prefix + round_up(size_t(a->B + 1) * sizeof(int32_t), 256);
   plan->off_o = plan->off_lse + round_up(rows * sizeof(float), 256);
   plan->bytes = plan->off_o + rows * zl::kGqaHeadDim * sizeof(float);
   return ZL_OK;
@@ -119,6 +138,8 @@ zl_status mla_validate_shape(const zl_decode_attn_params* a) {
     return ZL_ERR_INVALID_ARG;
   if (!(a->scale > 0.f) || !std::isfinite(a->scale)) return ZL_ERR_INVALID_ARG;
   if (a->Hkv != 1) return ZL_ERR_INVALID_ARG;
+  if (a->flags & ~uint32_t(ZL_DECODE_SINGLE_LAUNCH)) return ZL_ERR_INVALID_ARG;
+  if (a->flags) return ZL_ERR_UNSUPPORTED;  // MLA always merges in a second launch
   if (a->D_qk != zl::kMlaDqk || a->D_v != zl::kMlaDv) return ZL_ERR_UNSUPPORTED;
   if (a->Hq != zl::kMlaHeads) return ZL_ERR_UNSUPPORTED;
   if (a->q_len != 1) return ZL_ERR_UNSUPPORTED;
@@ -224,10 +245,12 @@ zl_status zl_decode_attn(const zl_decode_attn_params* a, zl_stream_t stream) {
   p.seq_lens = a->seq_lens;
   p.bt_stride = a->block_table_stride;
   char* ws = static_cast<char*>(a->workspace);
-  p.ws_prefix = reinterpret_cast<int32_t*>(ws);
+  p.ws_count = reinterpret_cast<unsigned long long*>(ws);
+  p.ws_prefix = reinterpret_cast<int32_t*>(ws + plan.off_prefix);
   p.ws_lse = reinterpret_cast<float*>(ws + plan.off_lse);
   p.ws_o = reinterpret_cast<float*>(ws + plan.off_o);
   p.err_flags = a->err_flags;
+  p.epoch = next_epoch();
   p.B = a->B;
   p.q_len = a->q_len;
   p.Hq = a->Hq;
@@ -239,7 +262,8 @@ zl_status zl_decode_attn(const zl_decode_attn_params* a, zl_stream_t stream) {
   p.nhg = plan.nhg;
   p.scale_log2 = float(double(a->scale) * kLog2e);
 
-  const cudaError_t e = zl::gqa_decode_launch(p, plan.grid, reinterpret_cast<cudaStream_t>(stream),
+  const cudaError_t e = zl::gqa_decode_launch(p, plan.grid, plan.fused,
+                                              reinterpret_cast<cudaStream_t>(stream),
                                               reinterpret_cast<cudaEvent_t>(a->attn_begin),
                                               reinterpret_cast<cudaEvent_t>(a->attn_end));
   return e == cudaSuccess ? ZL_OK : ZL_ERR_CUDA;

@@ -7,8 +7,11 @@
 // flash_decoding family named under "技术架构：五层模块化设计" on the
 // "ZhiLight：知乎开源的高性能 LLM 推理加速引擎" page). A CTA whose range covers a
 // whole unit writes the final output; a unit cut between CTAs leaves one
-// normalised partial (o, lse) per CTA in the workspace, and the merge kernel
-// combines them by log-sum-exp in CTA order. The cut depends only on
+// normalised partial (o, lse) per CTA in the workspace. Each consumer warp
+// that writes a partial then counts its arrival on the (sequence, kv head)
+// counter; the warp that arrives last combines all the partials of its rows
+// by log-sum-exp, always in CTA order, so the result does not depend on
+// which CTA finished last: one launch, deterministic. The cut depends only on
 // seq_lens and G, so results are bit-identical under page remapping.
 //
 // Per tile (16 tokens x HPC kv heads), the producer issues four TMA loads (K
@@ -34,6 +37,7 @@ namespace {
 constexpr uint32_t kErrBadPage = 1u;
 constexpr uint32_t kErrBadLen = 2u;
 constexpr uint32_t kErrTimeout = 4u;
+constexpr int kMergeRows = 4;  // rows merged together by the split merge
 
 template <int HPC>
 struct GqaCfg {
@@ -42,8 +46,9 @@ struct GqaCfg {
   static constexpr int kStages = HPC == 8 ? 3 : HPC == 4 ? 4 : HPC == 2 ? 6 : 8;
   static constexpr int kThreads = (HPC + 1) * 32;
   // 1 KB alignment slack + stages + barriers + per-stage flags + abort flag + prefix table
-  static constexpr size_t kSmemBytes =
-      1024 + size_t(kStages) * kStageBytes + kStages * 16 + kStages * 4 + 16 + (kMaxBatch + 1) * 4;
+  // + split-piece records (2 per consumer warp)
+  static constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStageBytes + kStages * 16 +
+                                       kStages * 4 + 16 + (kMaxBatch + 1) * 4 + HPC * 2 * 4;
 };
 
 __device__ __forceinline__ void raise_error(uint32_t* flags, uint32_t bits) {
@@ -62,7 +67,169 @@ __device__ __forceinline__ int locate_seq(const int* prefix, int B, int nhg, int
   return lo;
 }
 
-template <int HPC, bool ROWS16, bool CAUSAL>
+// First tile of CTA cc's range when W tiles are cut into G ranges
+// [floor(cc W / G), floor((cc+1) W / G)), from Wq = W / G and Wr = W % G:
+// floor(cc W / G) = cc Wq + floor(cc Wr / G), and cc Wr < G^2 < 2^32 (G is
+// at most 65535), so no 64-bit division is needed.
+struct TileCut {
+  int64_t Wq;
+  uint32_t Wr, G;
+  __device__ __forceinline__ int64_t start(int cc) const {
+    return int64_t(cc) * Wq + int64_t((uint32_t(cc) * Wr) / G);
+  }
+};
+
+// 64-bit compare-and-swap with acquire-release semantics at GPU scope: the
+// arriving warp's partial rows (ordered before it by __syncwarp) are released
+// with its arrival, and the last arrival acquires everyone else's.
+__device__ __forceinline__ unsigned long long cas_acq_rel(unsigned long long* addr,
+                                                          unsigned long long cmp,
+                                                          unsigned long long val) {
+  unsigned long long old;
+  asm volatile("atom.acq_rel.gpu.global.cas.b64 %0, [%1], %2, %3;"
+               : "=l"(old)
+               : "l"(addr), "l"(cmp), "l"(val)
+               : "memory");
+  return old;
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed(const unsigned long long* addr) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed(unsigned long long* addr, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(addr), "l"(v) : "memory");
+}
+
+// Count one arrival on a split unit's counter (epoch << 32 | count; a word
+// from another epoch counts as 0, so a call that stopped early cannot confuse
+// the next one). Returns true for the last of `pieces` arrivals, which also
+// puts the word back to 0. The first CAS guesses the usual state of a unit's
+// first arrival (a zero word), so that arrival costs one round trip. The CAS
+// retries only while other CTAs update the same word; the bound is a guard,
+// never reached by a correct schedule.
+__device__ __forceinline__ bool arrive_last(unsigned long long* word, uint32_t epoch, int pieces,
+                                            uint32_t* err_flags) {
+  unsigned long long old = 0ull;
+  for (int tries = 0; tries < (1 << 20); ++tries) {
+    const uint32_t cnt = uint32_t(old >> 32) == epoch ? uint32_t(old) : 0u;
+    const unsigned long long want = (static_cast<unsigned long long>(epoch) << 32) | (cnt + 1u);
+    const unsigned long long seen = cas_acq_rel(word, old, want);
+    if (seen == old) {
+      if (int(cnt + 1u) < pieces) return false;
+      st_relaxed(word, 0ull);
+      return true;
+    }
+    old = seen;
+  }
+  raise_error(err_flags, kErrTimeout);
+  return false;
+}
+
+// The CTAs holding pieces of a split unit (first tile U0, n tiles) that CTA c
+// takes part in: c_lo owns tile U0, c_hi the last tile, c lies between them.
+// Returns how many of them have a non-empty range (one piece each).
+__device__ __forceinline__ int split_cta_span(const TileCut& cut, int64_t U0, int n, int c,
+                                              int& c_lo, int& c_hi) {
+  int pieces = 1;
+  c_lo = c_hi = c;
+  while (cut.start(c_lo) > U0) {
+    --c_lo;
+    pieces += cut.start(c_lo) < cut.start(c_lo + 1) ? 1 : 0;
+  }
+  while (cut.start(c_hi + 1) < U0 + n) {
+    ++c_hi;
+    pieces += cut.start(c_hi) < cut.start(c_hi + 1) ? 1 : 0;
+  }
+  return pieces;
+}
+
+// Log-sum-exp merge of the R rows of kv head w (of CTA head group hg) over the
+// pieces of a split unit, by the warp whose arrival was the last (single
+// launch) or by the merge kernel: a running max and rescaled sums per row,
+// always in CTA order, so the result does not depend on who merges. Rows go in blocks of kMergeRows and pieces in
+// batches of kMergePieces: a lane loads every row's lse and its own 4 columns
+// of every row of a batch at once, so a batch costs one round trip to L2.
+// Merging the same pieces with any batch size gives the same bits.
+template <int kMergePieces>
+__device__ __forceinline__ void merge_split_rows(const GqaParams& p, const TileCut& cut,
+                                                 int64_t U0, int c_lo, int c_hi, int b, int w,
+                                                 int head0, int R, int lane) {
+  const int hpc = p.hpc;
+  const int g = p.g;
+  for (int r0 = 0; r0 < R; r0 += kMergeRows) {
+    float mx[kMergeRows], den[kMergeRows];
+    float4 acc[kMergeRows];
+    bool badp = false;
+#pragma unroll
+    for (int k = 0; k < kMergeRows; ++k) {
+      mx[k] = -CUDART_INF_F;
+      den[k] = 0.f;
+      acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int cb = c_lo; cb <= c_hi; cb += kMergePieces) {
+      float lv[kMergePieces][kMergeRows];
+      float4 ov[kMergePieces][kMergeRows];
+      bool use[kMergePieces];
+#pragma unroll
+      for (int q = 0; q < kMergePieces; ++q) {
+        const int cc = cb + q;
+        const int64_t s_cc = cut.start(cc);
+        use[q] = cc <= c_hi && s_cc < cut.start(cc + 1);
+        const int sl = (cc == c_lo && U0 > s_cc) ? 1 : 0;
+        const int64_t base = ((int64_t(cc) * 2 + sl) * hpc + w) * R + r0;
+#pragma unroll
+        for (int k = 0; k < kMergeRows; ++k) {
+          if (use[q] && r0 + k < R) {
+            lv[q][k] = __ldcg(p.ws_lse + base + k);
+            ov[q][k] =
+                __ldcg(reinterpret_cast<const float4*>(p.ws_o + (base + k) * kGqaHeadDim) + lane);
+          }
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < kMergePieces; ++q) {
+#pragma unroll
+        for (int k = 0; k < kMergeRows; ++k) {
+          if (use[q] && r0 + k < R) {
+            badp |= isnan(lv[q][k]);
+            const float mn = fmaxf(mx[k], lv[q][k]);
+            if (mn != -CUDART_INF_F && !isnan(lv[q][k])) {
+              const float a = ex2_approx(mx[k] - mn), wgt = ex2_approx(lv[q][k] - mn);
+              den[k] = den[k] * a + wgt;
+              acc[k].x = acc[k].x * a + wgt * ov[q][k].x;
+              acc[k].y = acc[k].y * a + wgt * ov[q][k].y;
+              acc[k].z = acc[k].z * a + wgt * ov[q][k].z;
+              acc[k].w = acc[k].w * a + wgt * ov[q][k].w;
+              mx[k] = mn;
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kMergeRows; ++k) {
+      const int r = r0 + k;
+      if (r < R) {
+        const bool none = badp || !(den[k] > 0.f);
+        const float inv = none ? 0.f : 1.f / den[k];
+        const int64_t orow = (int64_t(b) * p.q_len + r / g) * p.Hq + head0 + r % g;
+        uint2 packed = make_uint2(0u, 0u);  // a bad piece (NaN lse) zeroes the row
+        if (!none) {
+          packed.x = pack_bf16x2(acc[k].x * inv, acc[k].y * inv);
+          packed.y = pack_bf16x2(acc[k].z * inv, acc[k].w * inv);
+        }
+        reinterpret_cast<uint2*>(p.out + orow * kGqaHeadDim)[lane] = packed;
+        if (p.lse && lane == 0)
+          p.lse[orow] = none ? -CUDART_INF_F : (mx[k] + log2f(den[k])) * 0.69314718055994531f;
+      }
+    }
+  }
+}
+
+template <int HPC, bool ROWS16, bool CAUSAL, bool FUSED>
 __global__ void __launch_bounds__(GqaCfg<HPC>::kThreads, 1)
 gqa_decode_kernel(const __grid_constant__ GqaParams p) {
   using Cfg = GqaCfg<HPC>;
@@ -76,6 +243,7 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
   int* stage_bad = reinterpret_cast<int*>(empty + NS);
   volatile int* abort_flag = stage_bad + NS;
   int* prefix = stage_bad + NS + 4;
+  int* split_rec = prefix + kMaxBatch + 1;  // [HPC][2]: b | hg << 12 of a split piece, or -1
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int B = p.B;
@@ -127,15 +295,20 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
   }
   __syncthreads();
 
-  if (blockIdx.x == 0) {
-    for (int b = tid; b <= B; b += Cfg::kThreads) p.ws_prefix[b] = prefix[b];
+  if constexpr (!FUSED) {
+    // The merge kernel reads the tile counts, and may be scheduled early:
+    // it waits for this whole grid to finish before reading anything.
+    if (blockIdx.x == 0)
+      for (int b = tid; b <= B; b += Cfg::kThreads) p.ws_prefix[b] = prefix[b];
+    griddep_launch_dependents();
   }
 
   const int G = gridDim.x, c = blockIdx.x;
   const int nhg = p.nhg;
   const int64_t W = int64_t(nhg) * prefix[B];
-  const int64_t s_c = int64_t(c) * W / G;
-  const int64_t e_c = int64_t(c + 1) * W / G;
+  const TileCut cut{W / G, uint32_t(W % G), uint32_t(G)};
+  const int64_t s_c = cut.start(c);
+  const int64_t e_c = cut.start(c + 1);
 
   if (warp == HPC) {
     // ------------------------------------------------------------ producer
@@ -209,6 +382,7 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
   const float scale_log2 = p.scale_log2;
   int it = 0;
   int64_t idx = s_c;
+  if (lane == 0) split_rec[2 * w] = split_rec[2 * w + 1] = -1;
   while (idx < e_c) {
     const int b = locate_seq(prefix, B, nhg, idx);
     const int n = prefix[b + 1] - prefix[b];
@@ -400,7 +574,41 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
         if (t4 == 0) p.ws_lse[wrow] = bad ? CUDART_NAN_F : lse2;
       }
     }
+    // A split piece is merged after the CTA's range is done (its partner
+    // pieces finish about then too); only its (b, hg) is kept meanwhile.
+    if (FUSED && partial && lane == 0) split_rec[2 * w + slot] = b | (hg << 12);
     idx = piece_end;
+  }
+  // This warp's split pieces (at most two: the range's first and last) are
+  // written; count both arrivals at once (lane sl takes record sl; the CAS
+  // releases the rows the warp wrote before __syncwarp), then merge the units
+  // this warp completed. Without FUSED the merge kernel does it.
+  if constexpr (FUSED) {
+  __syncwarp();
+  int job = -1;
+  if (lane < 2) {
+    const int rec = split_rec[2 * w + lane];
+    if (rec >= 0) {
+      const int b = rec & 4095, hg = rec >> 12;
+      const int n = prefix[b + 1] - prefix[b];
+      int c_lo, c_hi;
+      const int pieces = split_cta_span(cut, int64_t(nhg) * prefix[b] + int64_t(hg) * n, n, c,
+                                        c_lo, c_hi);
+      if (arrive_last(p.ws_count + int64_t(b) * p.Hkv + hg * HPC + w, p.epoch, pieces,
+                      p.err_flags))
+        job = rec;
+    }
+  }
+  for (int sl = 0; sl < 2; ++sl) {
+    const int rec = __shfl_sync(0xffffffffu, job, sl);
+    if (rec < 0) continue;
+    const int b = rec & 4095, hg = rec >> 12;
+    const int n = prefix[b + 1] - prefix[b];
+    const int64_t U0 = int64_t(nhg) * prefix[b] + int64_t(hg) * n;
+    int c_lo, c_hi;
+    split_cta_span(cut, U0, n, c, c_lo, c_hi);
+    merge_split_rows<4>(p, cut, U0, c_lo, c_hi, b, w, (hg * HPC + w) * g, g * p.q_len, lane);
+  }
   }
 
   // Sequences with no tiles (empty or invalid length): zeros, lse = -inf.
@@ -415,24 +623,26 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
   }
 }
 
-// CTA that owns global tile x when W tiles are cut into G ranges
-// [floor(c W / G), floor((c+1) W / G)).
+
+// CTA that owns global tile x when W tiles are cut into G ranges.
 __device__ __forceinline__ int cta_of_tile(int64_t x, int64_t W, int G) {
   return int(((x + 1) * G + W - 1) / W) - 1;
 }
 
-// One warp per (sequence, query head): log-sum-exp merge of the partials of
-// a unit that was cut between CTAs, in CTA order. Units that one CTA finished
-// were written by the attention kernel and are skipped here.
+// Split-KV merge as its own launch (when the attention kernel runs without
+// FUSED): one warp per (sequence, kv head) that was cut between CTAs, with
+// the same arithmetic as the in-kernel merge, so both give the same bits.
+// Launched as a programmatic dependent of the attention kernel: it may start
+// early and waits here until that grid has finished and its writes are
+// visible.
 __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ GqaParams p,
                                                         int G) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = int64_t(blockIdx.x) * 4 + warp;  // (b, query token i, head)
-  if (row >= int64_t(p.B) * p.q_len * p.Hq) return;
-  const int b = int(row / (int64_t(p.q_len) * p.Hq));
-  const int i = int((row / p.Hq) % p.q_len), hq = int(row % p.Hq);
-  const int kvh = hq / p.g, hg = kvh / p.hpc, w = kvh % p.hpc;
-  const int R = p.g * p.q_len, r = i * p.g + hq % p.g;  // row of the m16 tile
+  griddep_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t unit = int64_t(blockIdx.x) * 4 + (threadIdx.x >> 5);  // b * Hkv + kv head
+  if (unit >= int64_t(p.B) * p.Hkv) return;
+  const int b = int(unit / p.Hkv), kvh = int(unit % p.Hkv);
+  const int hg = kvh / p.hpc, w = kvh % p.hpc;
   const int* prefix = p.ws_prefix;
   const int n = prefix[b + 1] - prefix[b];
   if (n == 0) return;
@@ -440,74 +650,41 @@ __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ 
   const int64_t U0 = int64_t(p.nhg) * prefix[b] + int64_t(hg) * n;
   const int c_lo = cta_of_tile(U0, W, G), c_hi = cta_of_tile(U0 + n - 1, W, G);
   if (c_lo == c_hi) return;
-
-  float M = -CUDART_INF_F;
-  bool bad = false;
-  for (int c = c_lo; c <= c_hi; ++c) {
-    const int64_t s_c = int64_t(c) * W / G, e_c = int64_t(c + 1) * W / G;
-    if (s_c == e_c) continue;
-    const int slot = (c == c_lo && U0 > s_c) ? 1 : 0;
-    const float l = p.ws_lse[((int64_t(c) * 2 + slot) * p.hpc + w) * R + r];
-    bad |= isnan(l);
-    M = fmaxf(M, l);
-  }
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float den = 0.f;
-  if (!bad) {
-    for (int c = c_lo; c <= c_hi; ++c) {
-      const int64_t s_c = int64_t(c) * W / G, e_c = int64_t(c + 1) * W / G;
-      if (s_c == e_c) continue;
-      const int slot = (c == c_lo && U0 > s_c) ? 1 : 0;
-      const int64_t wrow = ((int64_t(c) * 2 + slot) * p.hpc + w) * R + r;
-      const float wgt = exp2f(p.ws_lse[wrow] - M);
-      const float4 v = reinterpret_cast<const float4*>(p.ws_o + wrow * kGqaHeadDim)[lane];
-      acc.x += wgt * v.x;
-      acc.y += wgt * v.y;
-      acc.z += wgt * v.z;
-      acc.w += wgt * v.w;
-      den += wgt;
-    }
-  }
-  const float inv = bad ? 0.f : 1.f / den;
-  uint2 packed;
-  packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-  packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-  reinterpret_cast<uint2*>(p.out + row * kGqaHeadDim)[lane] = packed;
-  if (p.lse && lane == 0)
-    p.lse[row] = bad ? -CUDART_INF_F : (M + log2f(den)) * 0.69314718055994531f;
+  const TileCut cut{W / G, uint32_t(W % G), uint32_t(G)};
+  merge_split_rows<2>(p, cut, U0, c_lo, c_hi, b, w, kvh * p.g, p.g * p.q_len, lane);
 }
 
 constexpr int kMaxDevices = 64;
 
 // Raise the dynamic shared-memory limit of one kernel instance, once per device.
-template <int HPC, bool R16, bool C>
+template <int HPC, bool R16, bool C, bool U>
 cudaError_t configure(int device) {
   static bool done[kMaxDevices] = {};
   if (device >= 0 && device < kMaxDevices && done[device]) return cudaSuccess;
-  const cudaError_t e = cudaFuncSetAttribute(gqa_decode_kernel<HPC, R16, C>,
+  const cudaError_t e = cudaFuncSetAttribute(gqa_decode_kernel<HPC, R16, C, U>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              int(GqaCfg<HPC>::kSmemBytes));
   if (e == cudaSuccess && device >= 0 && device < kMaxDevices) done[device] = true;
   return e;
 }
 
-template <int HPC, bool R16, bool C>
+template <int HPC, bool R16, bool C, bool U>
 cudaError_t launch_attn(const GqaParams& p, int grid, cudaStream_t stream) {
   using Cfg = GqaCfg<HPC>;
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
-  if ((e = configure<HPC, R16, C>(device)) != cudaSuccess) return e;
-  gqa_decode_kernel<HPC, R16, C><<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(p);
+  if ((e = configure<HPC, R16, C, U>(device)) != cudaSuccess) return e;
+  gqa_decode_kernel<HPC, R16, C, U><<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 
-template <int HPC, bool R16, bool C>
+template <int HPC, bool R16, bool C, bool U>
 int occupancy(int device) {
   using Cfg = GqaCfg<HPC>;
-  if (configure<HPC, R16, C>(device) != cudaSuccess) return 0;
+  if (configure<HPC, R16, C, U>(device) != cudaSuccess) return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_decode_kernel<HPC, R16, C>, Cfg::kThreads,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_decode_kernel<HPC, R16, C, U>, Cfg::kThreads,
                                                     Cfg::kSmemBytes) != cudaSuccess)
     return 0;
   return n;
@@ -524,54 +701,68 @@ int gqa_heads_per_cta(int Hkv) {
 
 namespace {
 
-// The kernel instance for (heads per CTA, 16 rows, causal rows).
-template <template <int, bool, bool> class F, typename... A>
-auto dispatch(int hpc, bool r16, bool causal, A... a) -> decltype(F<1, false, false>::run(a...)) {
-  using R = decltype(F<1, false, false>::run(a...));
-  const int k = (hpc * 2 + (r16 ? 1 : 0)) * 2 + (causal ? 1 : 0);
+// The kernel instance for (heads per CTA, 16 rows, causal rows, fused merge).
+template <template <int, bool, bool, bool> class F, typename... A>
+auto dispatch(int hpc, bool r16, bool causal, bool fused, A... a)
+    -> decltype(F<1, false, false, false>::run(a...)) {
+  using R = decltype(F<1, false, false, false>::run(a...));
+  const int k = ((hpc * 2 + (r16 ? 1 : 0)) * 2 + (causal ? 1 : 0)) * 2 + (fused ? 1 : 0);
   switch (k) {
-#define ZL_CASE(H, S, C) \
-  case (H * 2 + S) * 2 + C: return F<H, bool(S), bool(C)>::run(a...);
-    ZL_CASE(1, 0, 0) ZL_CASE(1, 0, 1) ZL_CASE(1, 1, 0) ZL_CASE(1, 1, 1)
-    ZL_CASE(2, 0, 0) ZL_CASE(2, 0, 1) ZL_CASE(2, 1, 0) ZL_CASE(2, 1, 1)
-    ZL_CASE(4, 0, 0) ZL_CASE(4, 0, 1) ZL_CASE(4, 1, 0) ZL_CASE(4, 1, 1)
-    ZL_CASE(8, 0, 0) ZL_CASE(8, 0, 1) ZL_CASE(8, 1, 0) ZL_CASE(8, 1, 1)
+#define ZL_CASE(H, S, C, U) \
+  case ((H * 2 + S) * 2 + C) * 2 + U: return F<H, bool(S), bool(C), bool(U)>::run(a...);
+#define ZL_CASES(H)                                                              \
+  ZL_CASE(H, 0, 0, 0) ZL_CASE(H, 0, 0, 1) ZL_CASE(H, 0, 1, 0) ZL_CASE(H, 0, 1, 1) \
+  ZL_CASE(H, 1, 0, 0) ZL_CASE(H, 1, 0, 1) ZL_CASE(H, 1, 1, 0) ZL_CASE(H, 1, 1, 1)
+    ZL_CASES(1) ZL_CASES(2) ZL_CASES(4) ZL_CASES(8)
+#undef ZL_CASES
 #undef ZL_CASE
     default: return R();
   }
 }
 
-template <int HPC, bool R16, bool C>
+template <int HPC, bool R16, bool C, bool U>
 struct Occupancy {
-  static int run(int device) { return occupancy<HPC, R16, C>(device); }
+  static int run(int device) { return occupancy<HPC, R16, C, U>(device); }
 };
 
-template <int HPC, bool R16, bool C>
+template <int HPC, bool R16, bool C, bool U>
 struct Launch {
   static cudaError_t run(const GqaParams* p, int grid, cudaStream_t stream) {
-    return launch_attn<HPC, R16, C>(*p, grid, stream);
+    return launch_attn<HPC, R16, C, U>(*p, grid, stream);
   }
 };
 
 }  // namespace
 
-int gqa_ctas_per_sm(int hpc, bool rows16, bool causal, int device) {
-  return dispatch<Occupancy>(hpc, rows16, causal, device);
+int gqa_ctas_per_sm(int hpc, bool rows16, bool causal, bool fused, int device) {
+  return dispatch<Occupancy>(hpc, rows16, causal, fused, device);
 }
 
-cudaError_t gqa_decode_launch(const GqaParams& p, int grid, cudaStream_t stream,
+cudaError_t gqa_decode_launch(const GqaParams& p, int grid, bool fused, cudaStream_t stream,
                               cudaEvent_t attn_begin, cudaEvent_t attn_end) {
   cudaError_t e = cudaSuccess;
   if (attn_begin && (e = cudaEventRecord(attn_begin, stream)) != cudaSuccess) return e;
   const bool r16 = p.g * p.q_len > 8;
   const bool known = p.hpc == 1 || p.hpc == 2 || p.hpc == 4 || p.hpc == 8;
   if (!known) return cudaErrorInvalidValue;
-  e = dispatch<Launch>(p.hpc, r16, p.q_len > 1, &p, grid, stream);
+  e = dispatch<Launch>(p.hpc, r16, p.q_len > 1, fused, &p, grid, stream);
   if (e != cudaSuccess) return e;
   if (attn_end && (e = cudaEventRecord(attn_end, stream)) != cudaSuccess) return e;
-  const int64_t rows = int64_t(p.B) * p.q_len * p.Hq;
-  gqa_merge_kernel<<<int((rows + 3) / 4), 128, 0, stream>>>(p, grid);
-  return cudaGetLastError();
+  if (fused) return cudaSuccess;
+  // The merge as a programmatic dependent launch: its CTAs may become resident
+  // before the attention grid ends and wait in griddepcontrol.wait.
+  const int64_t units = int64_t(p.B) * p.Hkv;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned((units + 3) / 4));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gqa_merge_kernel, p, grid);
 }
 
 }  // namespace zl

@@ -12,7 +12,7 @@ constexpr int kGqaTile = 16;     // tokens per pipeline stage of the GQA kernel
 constexpr int kGqaHeadDim = 128; // D_qk = D_v
 constexpr int kMaxBatch = 4096;  // sequences per call (prefix table lives in smem)
 
-// Everything the GQA attention kernel and its merge kernel read.
+// Everything the GQA attention kernel reads.
 struct GqaParams {
   CUtensorMap tmap_k;  // 4-D {D, page_size, Hkv, num_pages}, box {64, 16, HPC, 1}, 128B swizzle
   CUtensorMap tmap_v;  // same geometry over the V pool
@@ -22,10 +22,12 @@ struct GqaParams {
   const int32_t* block_table;
   const int32_t* seq_lens;
   int64_t bt_stride;
-  int32_t* ws_prefix;  // [B + 1] tile prefix sums, written by CTA 0
+  unsigned long long* ws_count;  // [B * Hkv] arrivals per split unit: epoch << 32 | count
+  int32_t* ws_prefix;  // [B + 1] tile prefix sums, written by CTA 0 for the merge kernel
   float* ws_o;         // [G][2][HPC][g * q_len][128] normalised partial outputs
   float* ws_lse;       // [G][2][HPC][g * q_len] base-2 lse of the partials (NaN = bad piece)
   uint32_t* err_flags; // or nullptr
+  uint32_t epoch;      // nonzero, different for every host call
   int B, q_len, Hq, Hkv, g, page_size, num_pages;
   int hpc;             // kv heads per CTA
   int nhg;             // Hkv / hpc head groups
@@ -63,9 +65,11 @@ cudaError_t mla_decode_launch(const MlaParams& p, int clusters, cudaStream_t str
 // kv heads handled by one CTA for this Hkv (largest of 8, 4, 2, 1 dividing it).
 int gqa_heads_per_cta(int Hkv);
 // CTAs of the attention kernel that fit on one SM (0 on error).
-int gqa_ctas_per_sm(int hpc, bool rows16, bool causal, int device);
-// Launches the attention kernel on `grid` CTAs, then the merge kernel.
-cudaError_t gqa_decode_launch(const GqaParams& p, int grid, cudaStream_t stream,
+int gqa_ctas_per_sm(int hpc, bool rows16, bool causal, bool fused, int device);
+// Launches the attention kernel on `grid` CTAs. fused: split units are merged
+// inside it (one launch); otherwise a merge kernel follows as a programmatic
+// dependent launch.
+cudaError_t gqa_decode_launch(const GqaParams& p, int grid, bool fused, cudaStream_t stream,
                               cudaEvent_t attn_begin, cudaEvent_t attn_end);
 
 }  // namespace zl

@@ -317,6 +317,14 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint32_t a, ui
 namespace zl {
 
 // Non-blocking probe of an mbarrier phase.
+// Programmatic dependent launch: let the next kernel in the stream start
+// (launch_dependents), and wait until the kernel this one depends on has
+// finished and its memory is visible (wait; returns at once without one).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t done;
   asm volatile(

@@ -59,6 +59,7 @@ def _params(**over):
     (dict(q_len=5), zl.ERR_UNSUPPORTED),           # 4 heads x 5 tokens > 16 rows
     (dict(Hq=8 * 16, q_len=2), zl.ERR_UNSUPPORTED),
     (dict(q_len=0), zl.ERR_INVALID_ARG),
+    (dict(flags=2), zl.ERR_INVALID_ARG),           # unknown flag bit
     (dict(page_size=8), zl.ERR_UNSUPPORTED),
     (dict(B=5000), zl.ERR_UNSUPPORTED),
 ])
@@ -101,6 +102,8 @@ def _mla_params(**over):
     (dict(page_size=32), zl.ERR_UNSUPPORTED),
     (dict(q_len=2), zl.ERR_UNSUPPORTED),
     (dict(B=3000), zl.ERR_UNSUPPORTED),
+    (dict(flags=zl.SINGLE_LAUNCH), zl.ERR_UNSUPPORTED),
+    (dict(flags=4), zl.ERR_INVALID_ARG),
 ])
 def test_mla_host_validation(over, code):
     p = _mla_params(**over)

@@ -30,7 +30,7 @@ def test_noalloc_matches_workspace_entry_point_twice():
     ref_out = torch.empty(w.B, 1, w.Hq, w.D_v, dtype=torch.bfloat16, device="cuda")
     ref_lse = torch.empty(w.B, 1, w.Hq, dtype=torch.float32, device="cuda")
     p = _params(w, d, ref_out, ref_lse)
-    ws = torch.empty(zl.workspace_size(p), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(zl.workspace_size(p), dtype=torch.uint8, device="cuda")
     p.workspace, p.workspace_bytes = ws.data_ptr(), ws.numel()
     stream = torch.cuda.current_stream()
     assert zl.lib().zl_decode_attn(ctypes.byref(p), ctypes.c_void_p(stream.cuda_stream)) == zl.OK
