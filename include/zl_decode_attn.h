@@ -101,13 +101,16 @@ typedef struct {
 
   /* Caller-owned device scratch of at least zl_decode_attn_workspace_size()
      bytes, 256-byte aligned.
-     zl_decode_attn with ZL_DECODE_SINGLE_LAUNCH: zero-fill it once before
-     its first use (e.g. with cudaMemsetAsync). It starts with one arrival
-     counter per (sequence, kv head) that the in-kernel merge counts up and
-     returns to zero, so every call leaves it ready for the next; counters
-     left by a call that stopped on a device error are recognised and
-     ignored. Writing other data into it (another entry point, another use)
-     needs a new zero fill. Otherwise: contents need no initialisation. */
+     zl_decode_attn with ZL_DECODE_SINGLE_LAUNCH: its first 8 * B * Hkv bytes
+     are one arrival counter per (sequence, kv head), which must be zero
+     before the call (zero-fill them, e.g. with cudaMemsetAsync). The
+     in-kernel merge counts them up and returns each one it used to zero, so
+     a call leaves them ready for the next call of the same or smaller
+     B * Hkv; counters left by a call that stopped on a device error are
+     recognised (each call tags its counts) and ignored. Anything else
+     written into that range (a call without the flag, a call with a larger
+     B * Hkv, other data) needs a new zero fill of it first.
+     Otherwise: contents need no initialisation. */
   void* workspace;
   size_t workspace_bytes;
 

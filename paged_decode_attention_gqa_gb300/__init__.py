@@ -214,15 +214,21 @@ def workspace_size_mla(params: Params) -> int:
 _ws_cache: dict = {}
 
 
-def _workspace(device, nbytes, kind):
-    """A cached, zero-filled device byte buffer of at least nbytes per (device,
-    entry point). GQA calls leave their counters at zero, so the buffer stays
-    valid for the next GQA call; MLA calls get a buffer of their own."""
+def _workspace(device, nbytes, kind, counters=0):
+    """A cached device byte buffer of at least nbytes per (device, kind).
+
+    ``counters``: the call needs that many leading bytes at zero (the arrival
+    counters of a single-launch GQA call). They are zeroed again whenever the
+    previous user of the buffer may have written there: a call of another
+    shape (its partials may sit where this call counts) or a fresh buffer.
+    Calls of one shape leave the counters at zero themselves."""
     key = (device.type, device.index, kind)
-    buf = _ws_cache.get(key)
+    buf, last = _ws_cache.get(key, (None, None))
     if buf is None or buf.numel() < nbytes:
-        buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
-        _ws_cache[key] = buf
+        buf, last = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device), None
+    if counters and last != (nbytes, counters):
+        buf[:counters].zero_()
+    _ws_cache[key] = (buf, (nbytes, counters) if counters else None)
     return buf
 
 
@@ -254,7 +260,9 @@ def _run(q, k_pool, v_pool, block_table, seq_lens, *, mla, page_size, scale, Hkv
                     single_launch=single_launch)
     need = workspace_size_mla(p) if mla else workspace_size(p)
     if workspace is None:
-        workspace = _workspace(q.device, need, "mla" if mla else "gqa")
+        counters = 8 * q.shape[0] * Hkv if single_launch else 0
+        workspace = _workspace(q.device, need,
+                               "mla" if mla else ("gqa1" if single_launch else "gqa"), counters)
     p.workspace = workspace.data_ptr()
     p.workspace_bytes = workspace.numel() * workspace.element_size()
     call(p, mla=mla, stream=stream)
@@ -270,8 +278,8 @@ def decode_attn(q, k_pool, v_pool, block_table, seq_lens, *, page_size, scale, o
     (layout "NHD") or [pages, Hkv, page_size, 128] ("HND") bf16; block_table
     int32 [B, max_pages]; seq_lens int32 [B]. Returns out [B, q_len, Hq, 128]
     bf16. single_launch: merge split-KV partials inside the attention kernel
-    (ZL_DECODE_SINGLE_LAUNCH; the workspace must then start zeroed, which the
-    cached default workspace is).
+    (ZL_DECODE_SINGLE_LAUNCH; a caller's workspace must then hold zeroed
+    arrival counters, see the header; the default cached one is kept so).
     """
     Hkv = k_pool.shape[2] if layout == "NHD" else k_pool.shape[1]
     return _run(q, k_pool, v_pool, block_table, seq_lens, mla=False, page_size=page_size,

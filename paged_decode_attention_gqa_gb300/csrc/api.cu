@@ -37,11 +37,22 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // A different nonzero tag for every GQA call in this process: the in-kernel
 // split merge counts arrivals per tag, so counters left behind by a call that
-// stopped early (a device error) are ignored by the next call.
+// stopped early (a device error) are ignored by the next call. The call
+// number goes through an invertible 32-bit mix (odd multiplier, xor-shifts),
+// so consecutive tags are far apart and unlike small integers or float bits
+// that other data may have left in the buffer.
 uint32_t next_epoch() {
   static std::atomic<uint32_t> counter{0};
-  uint32_t e = counter.fetch_add(1, std::memory_order_relaxed) + 1;
-  if (e == 0) e = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+  uint32_t e = 0;
+  while (e == 0) {
+    uint32_t x = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+    x ^= x >> 16;
+    x *= 0x7feb352du;
+    x ^= x >> 15;
+    x *= 0x846ca68bu;
+    x ^= x >> 16;
+    e = x;
+  }
   return e;
 }
 
