@@ -138,6 +138,15 @@ typedef struct {
    zl_decode_attn_mla accepts no flags. */
 #define ZL_DECODE_SINGLE_LAUNCH 1u
 
+/* Test hook for failure detection, not for production calls: the attention
+   kernel first waits on a word that nothing ever sets, so its bounded wait
+   (about 50 ms) runs out; every CTA then stops, the call reports
+   ZL_DEVERR_TIMEOUT in *err_flags, and out / lse are left undefined. The
+   context stays usable and the next call without the hook computes normally.
+   This is how a stalled pipeline is reported, made to happen on purpose
+   without a fault. zl_decode_attn only. */
+#define ZL_DECODE_TEST_STALL 0x80000000u
+
 /*
  * GQA / MHA / MQA decode over separate K and V pools.
  *   Supported: D_qk = D_v = 128; Hq % Hkv == 0; 1 <= (Hq/Hkv) * q_len <= 16

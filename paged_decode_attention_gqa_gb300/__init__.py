@@ -34,6 +34,7 @@ HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA = range(5)
 SINGLE_LAUNCH = 1  # ZL_DECODE_SINGLE_LAUNCH
+TEST_STALL = 0x80000000  # ZL_DECODE_TEST_STALL (failure-detection test hook)
 DEVERR_BAD_PAGE, DEVERR_BAD_SEQ_LEN, DEVERR_TIMEOUT = 1, 2, 4
 
 

@@ -91,7 +91,8 @@ zl_status gqa_validate_shape(const zl_decode_attn_params* a) {
       a->num_ctas < 0 || a->max_seq_len < 0)
     return ZL_ERR_INVALID_ARG;
   if (a->Hq % a->Hkv != 0) return ZL_ERR_INVALID_ARG;
-  if (a->flags & ~uint32_t(ZL_DECODE_SINGLE_LAUNCH)) return ZL_ERR_INVALID_ARG;
+  if (a->flags & ~uint32_t(ZL_DECODE_SINGLE_LAUNCH | ZL_DECODE_TEST_STALL))
+    return ZL_ERR_INVALID_ARG;
   if (a->num_ctas > 65535) return ZL_ERR_UNSUPPORTED;  // the tile cut needs G^2 < 2^32
   if (!(a->scale > 0.f) || !std::isfinite(a->scale)) return ZL_ERR_INVALID_ARG;
   if (a->D_qk != zl::kGqaHeadDim || a->D_v != zl::kGqaHeadDim) return ZL_ERR_UNSUPPORTED;
@@ -149,8 +150,9 @@ zl_status mla_validate_shape(const zl_decode_attn_params* a) {
     return ZL_ERR_INVALID_ARG;
   if (!(a->scale > 0.f) || !std::isfinite(a->scale)) return ZL_ERR_INVALID_ARG;
   if (a->Hkv != 1) return ZL_ERR_INVALID_ARG;
-  if (a->flags & ~uint32_t(ZL_DECODE_SINGLE_LAUNCH)) return ZL_ERR_INVALID_ARG;
-  if (a->flags) return ZL_ERR_UNSUPPORTED;  // MLA always merges in a second launch
+  if (a->flags & ~uint32_t(ZL_DECODE_SINGLE_LAUNCH | ZL_DECODE_TEST_STALL))
+    return ZL_ERR_INVALID_ARG;
+  if (a->flags) return ZL_ERR_UNSUPPORTED;  // neither flag exists for MLA
   if (a->D_qk != zl::kMlaDqk || a->D_v != zl::kMlaDv) return ZL_ERR_UNSUPPORTED;
   if (a->Hq != zl::kMlaHeads) return ZL_ERR_UNSUPPORTED;
   if (a->q_len != 1) return ZL_ERR_UNSUPPORTED;
@@ -262,6 +264,7 @@ zl_status zl_decode_attn(const zl_decode_attn_params* a, zl_stream_t stream) {
   p.ws_o = reinterpret_cast<float*>(ws + plan.off_o);
   p.err_flags = a->err_flags;
   p.epoch = next_epoch();
+  p.test_stall = (a->flags & ZL_DECODE_TEST_STALL) ? 1 : 0;
   p.B = a->B;
   p.q_len = a->q_len;
   p.Hq = a->Hq;

@@ -38,6 +38,7 @@ constexpr uint32_t kErrBadPage = 1u;
 constexpr uint32_t kErrBadLen = 2u;
 constexpr uint32_t kErrTimeout = 4u;
 constexpr int kMergeRows = 4;  // rows merged together by the split merge
+constexpr uint64_t kTestStallNs = 50ull * 1000 * 1000;  // bound of the test-hook wait
 
 template <int HPC>
 struct GqaCfg {
@@ -312,6 +313,20 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
 
   if (warp == HPC) {
     // ------------------------------------------------------------ producer
+    if (p.test_stall) {
+      // Failure-detection test hook: wait on a word nothing sets until the
+      // bound runs out, then stop the CTA the way a stalled pipeline does.
+      __shared__ int never_set;
+      if (lane == 0) {
+        never_set = 0;
+        if (!flag_wait(&never_set, kTestStallNs)) {
+          raise_error(p.err_flags, kErrTimeout);
+          *abort_flag = 1;
+        }
+      }
+      __syncwarp();
+      return;
+    }
     int it = 0;
     bool aborted = false;
     for (int64_t base = s_c; base < e_c && !aborted; base += 32) {

@@ -28,6 +28,7 @@ struct GqaParams {
   float* ws_lse;       // [G][2][HPC][g * q_len] base-2 lse of the partials (NaN = bad piece)
   uint32_t* err_flags; // or nullptr
   uint32_t epoch;      // nonzero, different for every host call
+  int test_stall;      // failure-detection test hook: stall the producer until its wait runs out
   int B, q_len, Hq, Hkv, g, page_size, num_pages;
   int hpc;             // kv heads per CTA
   int nhg;             // Hkv / hpc head groups

@@ -166,6 +166,9 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
 
   if (blockIdx.x == 0)
     for (int b = tid; b <= B; b += kThreads) p.ws_prefix[b] = prefix[b];
+  // The merge kernel may be scheduled from here on; it waits for this whole
+  // grid to finish before it reads anything.
+  griddep_launch_dependents();
 
   const int64_t W = prefix[B];
   const int64_t s_c = int64_t(cid) * W / NC;
@@ -567,9 +570,11 @@ __device__ __forceinline__ int cluster_of_tile(int64_t x, int64_t W, int NC) {
 }
 
 // One warp per (sequence, head): log-sum-exp merge of the partials of a
-// sequence cut between clusters, in cluster order.
+// sequence cut between clusters, in cluster order. A programmatic dependent
+// launch of the attention kernel: it waits here until that grid is done.
 __global__ void __launch_bounds__(128) mla_merge_kernel(const __grid_constant__ MlaParams p,
                                                         int NC) {
+  griddep_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = int64_t(blockIdx.x) * 4 + warp;
   if (row >= int64_t(p.B) * kRows) return;
@@ -649,8 +654,17 @@ cudaError_t mla_decode_launch(const MlaParams& p, int clusters, cudaStream_t str
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (attn_end && (e = cudaEventRecord(attn_end, stream)) != cudaSuccess) return e;
   const int64_t rows = int64_t(p.B) * kRows;
-  mla_merge_kernel<<<int((rows + 3) / 4), 128, 0, stream>>>(p, clusters);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned((rows + 3) / 4));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_merge_kernel, p, clusters);
 }
 
 }  // namespace zl

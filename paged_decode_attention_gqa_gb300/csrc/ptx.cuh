@@ -70,6 +70,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// Wait until *flag != 0 or timeout_ns have passed; false on timeout.
+__device__ __forceinline__ bool flag_wait(const volatile int* flag, uint64_t timeout_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (*flag) return true;
+    if ((i & 63u) == 63u && globaltimer_ns() - t0 > timeout_ns) return false;
+  }
+}
+
 // ---------------------------------------------------------------- TMA
 // 4-D tiled bulk tensor load global -> shared, completion counted in bytes on
 // the mbarrier. Coordinates are in elements, innermost first.

@@ -60,6 +60,7 @@ def _params(**over):
     (dict(Hq=8 * 16, q_len=2), zl.ERR_UNSUPPORTED),
     (dict(q_len=0), zl.ERR_INVALID_ARG),
     (dict(flags=2), zl.ERR_INVALID_ARG),           # unknown flag bit
+    (dict(flags=zl.TEST_STALL | 4), zl.ERR_INVALID_ARG),
     (dict(page_size=8), zl.ERR_UNSUPPORTED),
     (dict(B=5000), zl.ERR_UNSUPPORTED),
 ])
@@ -103,6 +104,7 @@ def _mla_params(**over):
     (dict(q_len=2), zl.ERR_UNSUPPORTED),
     (dict(B=3000), zl.ERR_UNSUPPORTED),
     (dict(flags=zl.SINGLE_LAUNCH), zl.ERR_UNSUPPORTED),
+    (dict(flags=zl.TEST_STALL), zl.ERR_UNSUPPORTED),
     (dict(flags=4), zl.ERR_INVALID_ARG),
 ])
 def test_mla_host_validation(over, code):

@@ -183,3 +183,30 @@ def test_llama70b_prefix_full():
 
 def test_long_context_full():
     _parity(wl.long_context_decode())
+
+
+def test_cuda_graph_capture_of_the_default_path():
+    """The default call (attention kernel + merge kernel as a programmatic
+    dependent launch) captures into a CUDA graph; replays give the eager bits."""
+    w = wl.random_case(509, B=8, Hq=32, Hkv=8, max_len=2500)
+    d = device_inputs(w)
+    out = torch.empty(w.B, 1, w.Hq, 128, dtype=torch.bfloat16, device="cuda")
+    p = zl.make_params(d["q"], d["k"], d["v"], d["bt"], d["sl"], out, page_size=16,
+                       scale=w.scale, Hkv=8, D_v=128)
+    ws = torch.zeros(zl.workspace_size(p), dtype=torch.uint8, device="cuda")
+    p.workspace, p.workspace_bytes = ws.data_ptr(), ws.numel()
+    zl.call(p, mla=False)
+    torch.cuda.synchronize()
+    eager = out.clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        zl.call(p, mla=False, stream=s)
+    for _ in range(4):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    ref, _, _ = run_oracle(w)
+    assert_close(out.float().cpu().numpy().astype(np.float64), ref, "graph replay")
