@@ -16,6 +16,7 @@ replicas (the path has no exchange step).
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -235,7 +236,8 @@ def config_of(w, world):
             "seq_len": f"{int(lens.min())}..{int(lens.max())} (sum {int(lens.sum())})",
             "q_len": w.q_len, "kv_bytes_per_step": kv_bytes(w), "seed": w.seed,
             "l2": ("no flush: KV working set per step exceeds the 129 MB L2"
-                   if kv_bytes(w) > 4 * 129e6 else "L2 flushed between steps"),
+                   if kv_bytes(w) > 4 * 129e6 else "L2 flushed between steps (a 2 x L2 write, outside"
+                   " the per-step events)"),
             "parallelism": f"replicas x{world}"}
 
 
@@ -274,10 +276,29 @@ def run_ours(args, world, rank, local):
     if kv_bytes(w) <= 4 * 129e6:
         flush = torch.empty(int(2 * 129e6) // 4, dtype=torch.int32, device=dev)
 
+    # --with-append: each step first writes the q_len new tokens' K/V rows into
+    # their page slots (zl_kv_append), then attends, as a decode step does.
+    ap = None
+    if args.with_append:
+        from paged_decode_attention_gqa_gb300 import workloads as _wl
+        k_new, v_new = _wl.new_token_rows(w.seed, w.B, w.q_len, w.Hkv, w.D_qk,
+                                          None if w.mla else w.D_v)
+        k_new = k_new.to(dev)
+        v_new = None if v_new is None else v_new.to(dev)
+        ap = zl.make_append_params(k_new, v_new, k, v, bt, sl, page_size=w.page_size,
+                                   layout=w.layout, err_flags=err)
+    stream_ptr = ctypes.c_void_p(stream.cuda_stream)
+
+    def call():
+        if ap is not None:
+            rc = zl.lib().zl_kv_append(ctypes.byref(ap), stream_ptr)
+            assert rc == zl.OK, rc
+        zl.call(p, mla=w.mla, stream=stream)
+
     def step():
         if flush is not None:
             flush.zero_()
-        zl.call(p, mla=w.mla, stream=stream)
+        call()
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -293,19 +314,34 @@ def run_ours(args, world, rank, local):
         dist.barrier()
     torch.cuda.synchronize()
     t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # With an L2 flush between steps, each step's call is timed on its own
+    # (events after the flush, around the call) and the flush is left out.
+    step_evs = ([(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(args.steps)] if flush is not None else None)
     t_begin.record(stream)
-    for _ in range(args.steps):
-        step()
+    for i in range(args.steps):
+        if flush is None:
+            call()
+        else:
+            flush.zero_()
+            step_evs[i][0].record(stream)
+            call()
+            step_evs[i][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
-    ms = t_begin.elapsed_time(t_end) / args.steps
+    if flush is None:
+        ms = t_begin.elapsed_time(t_end) / args.steps
+    else:
+        ms = sum(a.elapsed_time(b) for a, b in step_evs) / args.steps
     if world > 1:
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
     # attention + merge: one launch with ZL_DECODE_SINGLE_LAUNCH, else two (MLA: two)
     launches = args.steps * (1 if (kind == "gqa" and args.single_launch) else 2)
+    if ap is not None:
+        launches += args.steps                              # the KV append
     if flush is not None:
         launches += args.steps                              # the L2 flush memset
 
@@ -328,12 +364,30 @@ def run_ours(args, world, rank, local):
         if flush is not None:
             flush.zero_()
         call_evs[i][0].record(stream)
-        zl.call(p, mla=w.mla, stream=stream)
+        call()
         call_evs[i][1].record(stream)
     torch.cuda.synchronize()
     p.attn_begin = p.attn_end = None
     attn_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
     call_ms = statistics.mean(a.elapsed_time(b) for a, b in call_evs)
+    append = None
+    if ap is not None:
+        app_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(n_ev)]
+        for a, b in app_evs:
+            if flush is not None:
+                flush.zero_()
+            a.record(stream)
+            zl.lib().zl_kv_append(ctypes.byref(ap), stream_ptr)
+            b.record(stream)
+        torch.cuda.synchronize()
+        app_ms = statistics.mean(a.elapsed_time(b) for a, b in app_evs)
+        # new rows read once, written once into the pools
+        app_bytes = 2 * w.B * w.q_len * w.Hkv * (w.D_qk + (0 if w.mla else w.D_v)) * 2
+        append = {"us_per_launch": app_ms * 1e3, "bytes_per_launch": app_bytes,
+                  "GBs": app_bytes / (app_ms * 1e-3) / 1e9,
+                  "note": "zl_kv_append alone, L2 flushed first when the step flushes"}
+    assert int(err.item()) == 0, f"device error flags {int(err.item())}"
 
     # ---- end to end through the public API: host inputs in, host result out
     e2e = None
@@ -401,7 +455,8 @@ def run_ours(args, world, rank, local):
         "data": "synthetic",
         "config": dict(config_of(w, world), split_merge=(
             "in the attention kernel (single launch)" if kind == "gqa" and args.single_launch
-            else "second launch" + (" (programmatic dependent launch)" if kind == "gqa" else ""))),
+            else "second launch (programmatic dependent launch)"),
+            step="kv append + attention" if ap is not None else "attention"),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "kernel": f"{kind}_decode_kernel", "attn_us_per_launch": attn_ms * 1e3,
@@ -410,6 +465,7 @@ def run_ours(args, world, rank, local):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,
+        "kv_append": append,
         "clocks": clocks,
     }
     if w.mla:
@@ -431,6 +487,8 @@ def main():
                     help="workload to time (the bench line is the default one; others are "
                          "for per-workload tables and profiling)")
     ap.add_argument("--batch", type=int, default=None, help="override the batch size")
+    ap.add_argument("--with-append", action="store_true",
+                    help="each step writes the new tokens' K/V (zl_kv_append) before attending")
     ap.add_argument("--single-launch", action="store_true",
                     help="GQA: merge split-KV partials inside the attention kernel")
     ap.add_argument("--q-len", type=int, default=1,

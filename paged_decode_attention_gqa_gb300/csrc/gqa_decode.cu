@@ -157,10 +157,11 @@ __device__ __forceinline__ int split_cta_span(const TileCut& cut, int64_t U0, in
 template <int kMergePieces>
 __device__ __forceinline__ void merge_split_rows(const GqaParams& p, const TileCut& cut,
                                                  int64_t U0, int c_lo, int c_hi, int b, int w,
-                                                 int head0, int R, int lane) {
+                                                 int head0, int R, int r_begin, int r_end,
+                                                 int lane) {
   const int hpc = p.hpc;
   const int g = p.g;
-  for (int r0 = 0; r0 < R; r0 += kMergeRows) {
+  for (int r0 = r_begin; r0 < r_end; r0 += kMergeRows) {
     float mx[kMergeRows], den[kMergeRows];
     float4 acc[kMergeRows];
     bool badp = false;
@@ -262,6 +263,10 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
     tma_prefetch_desc(&p.tmap_k);
     tma_prefetch_desc(&p.tmap_v);
   }
+  // Launched as a programmatic dependent of whatever kernel precedes it on the
+  // stream (e.g. the KV append): everything above overlaps that kernel's tail;
+  // nothing in global memory is read or written before it has finished.
+  griddep_wait();
 
   // Tiles per sequence and their exclusive prefix sum (warp 0).
   if (warp == 0) {
@@ -622,7 +627,8 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
     const int64_t U0 = int64_t(nhg) * prefix[b] + int64_t(hg) * n;
     int c_lo, c_hi;
     split_cta_span(cut, U0, n, c, c_lo, c_hi);
-    merge_split_rows<4>(p, cut, U0, c_lo, c_hi, b, w, (hg * HPC + w) * g, g * p.q_len, lane);
+    merge_split_rows<4>(p, cut, U0, c_lo, c_hi, b, w, (hg * HPC + w) * g, g * p.q_len, 0,
+                        g * p.q_len, lane);
   }
   }
 
@@ -645,17 +651,22 @@ __device__ __forceinline__ int cta_of_tile(int64_t x, int64_t W, int G) {
 }
 
 // Split-KV merge as its own launch (when the attention kernel runs without
-// FUSED): one warp per (sequence, kv head) that was cut between CTAs, with
-// the same arithmetic as the in-kernel merge, so both give the same bits.
+// FUSED): one warp per block of kMergeRows rows of a (sequence, kv head) that
+// was cut between CTAs, with the same arithmetic as the in-kernel merge, so
+// both give the same bits.
 // Launched as a programmatic dependent of the attention kernel: it may start
 // early and waits here until that grid has finished and its writes are
 // visible.
 __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ GqaParams p,
                                                         int G) {
   griddep_wait();
+  griddep_launch_dependents();  // the next call's kernels may start their prologue
   const int lane = threadIdx.x & 31;
-  const int64_t unit = int64_t(blockIdx.x) * 4 + (threadIdx.x >> 5);  // b * Hkv + kv head
-  if (unit >= int64_t(p.B) * p.Hkv) return;
+  const int R = p.g * p.q_len, nrb = (R + kMergeRows - 1) / kMergeRows;
+  const int64_t item = int64_t(blockIdx.x) * 4 + (threadIdx.x >> 5);
+  if (item >= int64_t(p.B) * p.Hkv * nrb) return;
+  const int64_t unit = item / nrb;  // b * Hkv + kv head
+  const int r0 = int(item % nrb) * kMergeRows;
   const int b = int(unit / p.Hkv), kvh = int(unit % p.Hkv);
   const int hg = kvh / p.hpc, w = kvh % p.hpc;
   const int* prefix = p.ws_prefix;
@@ -666,7 +677,8 @@ __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ 
   const int c_lo = cta_of_tile(U0, W, G), c_hi = cta_of_tile(U0 + n - 1, W, G);
   if (c_lo == c_hi) return;
   const TileCut cut{W / G, uint32_t(W % G), uint32_t(G)};
-  merge_split_rows<2>(p, cut, U0, c_lo, c_hi, b, w, kvh * p.g, p.g * p.q_len, lane);
+  merge_split_rows<2>(p, cut, U0, c_lo, c_hi, b, w, kvh * p.g, R, r0, min(R, r0 + kMergeRows),
+                      lane);
 }
 
 constexpr int kMaxDevices = 64;
@@ -690,8 +702,17 @@ cudaError_t launch_attn(const GqaParams& p, int grid, cudaStream_t stream) {
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
   if ((e = configure<HPC, R16, C, U>(device)) != cudaSuccess) return e;
-  gqa_decode_kernel<HPC, R16, C, U><<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(Cfg::kThreads);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gqa_decode_kernel<HPC, R16, C, U>, p);
 }
 
 template <int HPC, bool R16, bool C, bool U>
@@ -766,9 +787,9 @@ cudaError_t gqa_decode_launch(const GqaParams& p, int grid, bool fused, cudaStre
   if (fused) return cudaSuccess;
   // The merge as a programmatic dependent launch: its CTAs may become resident
   // before the attention grid ends and wait in griddepcontrol.wait.
-  const int64_t units = int64_t(p.B) * p.Hkv;
+  const int64_t items = int64_t(p.B) * p.Hkv * ((p.g * p.q_len + kMergeRows - 1) / kMergeRows);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned((units + 3) / 4));
+  cfg.gridDim = dim3(unsigned((items + 3) / 4));
   cfg.blockDim = dim3(128);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;

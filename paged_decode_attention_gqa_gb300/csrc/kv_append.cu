@@ -12,6 +12,7 @@
 // 16 + 16 chunks are one pass of the warp). Pure copies, so bit-exact.
 #include "../../include/zl_decode_attn.h"
 #include "kernels.h"
+#include "ptx.cuh"
 
 #include <cstring>
 
@@ -33,6 +34,9 @@ struct AppendParams {
 };
 
 __global__ void __launch_bounds__(256) kv_append_kernel(const __grid_constant__ AppendParams p) {
+  // The attention kernels that follow are programmatic dependents: let them
+  // start their prologue now (they wait for this grid before reading memory).
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
   for (int64_t row = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); row < p.rows;

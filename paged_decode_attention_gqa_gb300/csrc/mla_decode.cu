@@ -120,6 +120,10 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // Launched as a programmatic dependent of the kernel before it on the
+  // stream: wait for it before touching global memory, and before taking
+  // TMEM (a kernel still running on this SM may need its own).
+  griddep_wait();
   if (warp == 1) {
     tmem_alloc(sbase + kOffMisc, kTmemCols);
     tmem_relinquish();
@@ -575,6 +579,7 @@ __device__ __forceinline__ int cluster_of_tile(int64_t x, int64_t W, int NC) {
 __global__ void __launch_bounds__(128) mla_merge_kernel(const __grid_constant__ MlaParams p,
                                                         int NC) {
   griddep_wait();
+  griddep_launch_dependents();  // the next call's kernels may start their prologue
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = int64_t(blockIdx.x) * 4 + warp;
   if (row >= int64_t(p.B) * kRows) return;
@@ -650,8 +655,19 @@ cudaError_t mla_decode_launch(const MlaParams& p, int clusters, cudaStream_t str
     configured[device] = true;
   }
   if (attn_begin && (e = cudaEventRecord(attn_begin, stream)) != cudaSuccess) return e;
-  mla_decode_kernel<<<2 * clusters, kThreads, kSmemBytes, stream>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(2 * clusters));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if ((e = cudaLaunchKernelEx(&cfg, mla_decode_kernel, p)) != cudaSuccess) return e;
+  }
   if (attn_end && (e = cudaEventRecord(attn_end, stream)) != cudaSuccess) return e;
   const int64_t rows = int64_t(p.B) * kRows;
   cudaLaunchConfig_t cfg = {};
