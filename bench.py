@@ -264,9 +264,14 @@ def run_ours(args, world, rank, local):
     out = torch.empty(w.B, w.q_len, w.Hq, w.D_v, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(w.B, w.q_len, w.Hq, dtype=torch.float32, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
+    npref = 0
+    if args.shared_prefix:
+        npref = int(w.notes.get("shared_prefix_tokens", 0)) // w.page_size
+        assert npref > 0, "--shared-prefix needs a workload with a shared prefix"
     p = zl.make_params(q, k, v, bt, sl, out, page_size=w.page_size, scale=w.scale, Hkv=w.Hkv,
                        D_v=w.D_v, lse=lse, err_flags=err, max_seq_len=w.max_seq_len,
-                       single_launch=args.single_launch and not w.mla)
+                       single_launch=args.single_launch and not w.mla,
+                       shared_prefix_pages=npref)
     need = zl.workspace_size_mla(p) if w.mla else zl.workspace_size(p)
     ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
     p.workspace, p.workspace_bytes = ws.data_ptr(), ws.numel()
@@ -338,7 +343,8 @@ def run_ours(args, world, rank, local):
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
-    # attention + merge: one launch with ZL_DECODE_SINGLE_LAUNCH, else two (MLA: two)
+    # attention + merge: one launch with ZL_DECODE_SINGLE_LAUNCH, else two (MLA and
+    # shared-prefix calls: two)
     launches = args.steps * (1 if (kind == "gqa" and args.single_launch) else 2)
     if ap is not None:
         launches += args.steps                              # the KV append
@@ -413,7 +419,7 @@ def run_ours(args, world, rank, local):
             else:
                 zl.decode_attn(q, k, v, bt, sl, page_size=w.page_size, scale=w.scale, out=out,
                                workspace=ws, max_seq_len=w.max_seq_len,
-                               single_launch=args.single_launch)
+                               single_launch=args.single_launch, shared_prefix_pages=npref)
             pin_out.copy_(out, non_blocking=True)
         torch.cuda.synchronize()
         e2e_s = (time.perf_counter() - t0) / e2e_steps
@@ -456,7 +462,8 @@ def run_ours(args, world, rank, local):
         "config": dict(config_of(w, world), split_merge=(
             "in the attention kernel (single launch)" if kind == "gqa" and args.single_launch
             else "second launch (programmatic dependent launch)"),
-            step="kv append + attention" if ap is not None else "attention"),
+            step="kv append + attention" if ap is not None else "attention",
+            shared_prefix_pages=npref),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "kernel": f"{kind}_decode_kernel", "attn_us_per_launch": attn_ms * 1e3,
@@ -489,6 +496,8 @@ def main():
     ap.add_argument("--batch", type=int, default=None, help="override the batch size")
     ap.add_argument("--with-append", action="store_true",
                     help="each step writes the new tokens' K/V (zl_kv_append) before attending")
+    ap.add_argument("--shared-prefix", action="store_true",
+                    help="pass the workload's shared prefix pages (read once per group)")
     ap.add_argument("--single-launch", action="store_true",
                     help="GQA: merge split-KV partials inside the attention kernel")
     ap.add_argument("--q-len", type=int, default=1,

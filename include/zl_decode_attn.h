@@ -65,6 +65,7 @@ typedef enum {
 #define ZL_DEVERR_BAD_PAGE 1u    /* block_table entry outside [0, num_pages) */
 #define ZL_DEVERR_BAD_SEQ_LEN 2u /* seq_len < 0 or > block_table_stride * page_size */
 #define ZL_DEVERR_TIMEOUT 4u     /* a pipeline wait gave up after ~2 s */
+#define ZL_DEVERR_BAD_PREFIX 8u  /* shared_prefix_pages does not hold for some sequence */
 
 typedef struct {
   size_t struct_size; /* sizeof(zl_decode_attn_params), for ABI checks */
@@ -129,6 +130,16 @@ typedef struct {
 
   /* ZL_DECODE_* bits; 0 for the defaults. */
   uint32_t flags;
+
+  /* zl_decode_attn only; 0 = none. The first shared_prefix_pages entries of
+     every block-table row are the same physical pages (a cached prefix all B
+     sequences share), and every query row sees all of them
+     (seq_lens[b] - q_len + 1 >= shared_prefix_pages * page_size). Those pages
+     are then read once per group of 16 / (g * q_len) sequences instead of
+     once per sequence. The kernels check both conditions and set
+     ZL_DEVERR_BAD_PREFIX if either fails (results are then undefined). Not
+     with ZL_DECODE_SINGLE_LAUNCH. */
+  int32_t shared_prefix_pages;
 } zl_decode_attn_params;
 
 /* zl_decode_attn: merge the split-KV partials inside the attention kernel

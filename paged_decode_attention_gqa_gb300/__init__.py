@@ -35,7 +35,7 @@ HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA = range(5)
 SINGLE_LAUNCH = 1  # ZL_DECODE_SINGLE_LAUNCH
 TEST_STALL = 0x80000000  # ZL_DECODE_TEST_STALL (failure-detection test hook)
-DEVERR_BAD_PAGE, DEVERR_BAD_SEQ_LEN, DEVERR_TIMEOUT = 1, 2, 4
+DEVERR_BAD_PAGE, DEVERR_BAD_SEQ_LEN, DEVERR_TIMEOUT, DEVERR_BAD_PREFIX = 1, 2, 4, 8
 
 
 class ZlError(RuntimeError):
@@ -76,6 +76,7 @@ class Params(ctypes.Structure):
         ("attn_begin", ctypes.c_void_p),
         ("attn_end", ctypes.c_void_p),
         ("flags", ctypes.c_uint32),
+        ("shared_prefix_pages", ctypes.c_int32),
     ]
 
 
@@ -164,7 +165,8 @@ def _pool_strides(pool: torch.Tensor, layout: str):
 
 def make_params(q, k_pool, v_pool, block_table, seq_lens, out, *, page_size, scale, Hkv,
                 D_v, lse=None, workspace=None, err_flags=None, num_ctas=0, max_seq_len=0,
-                layout="NHD", events=None, single_launch=False) -> Params:
+                layout="NHD", events=None, single_launch=False,
+                shared_prefix_pages=0) -> Params:
     B, q_len, Hq, D_qk = q.shape
     ps, ts, hs = _pool_strides(k_pool, layout)
     if v_pool is not None and _pool_strides(v_pool, layout) != (ps, ts, hs):
@@ -191,6 +193,7 @@ def make_params(q, k_pool, v_pool, block_table, seq_lens, out, *, page_size, sca
     p.err_flags = _ptr(err_flags)
     p.num_ctas = int(num_ctas)
     p.flags = SINGLE_LAUNCH if single_launch else 0
+    p.shared_prefix_pages = int(shared_prefix_pages)
     if events is not None:
         p.attn_begin, p.attn_end = events[0].cuda_event, events[1].cuda_event
     # The struct holds raw device pointers: keep the tensors alive with it.
@@ -252,13 +255,14 @@ def call(params: Params, *, mla: bool, stream=None):
 
 
 def _run(q, k_pool, v_pool, block_table, seq_lens, *, mla, page_size, scale, Hkv, D_v, out, lse,
-         workspace, err_flags, num_ctas, max_seq_len, layout, stream, events, single_launch=False):
+         workspace, err_flags, num_ctas, max_seq_len, layout, stream, events, single_launch=False,
+         shared_prefix_pages=0):
     if out is None:
         out = torch.empty(q.shape[:3] + (D_v,), dtype=torch.bfloat16, device=q.device)
     p = make_params(q, k_pool, v_pool, block_table, seq_lens, out, page_size=page_size,
                     scale=scale, Hkv=Hkv, D_v=D_v, lse=lse, err_flags=err_flags,
                     num_ctas=num_ctas, max_seq_len=max_seq_len, layout=layout, events=events,
-                    single_launch=single_launch)
+                    single_launch=single_launch, shared_prefix_pages=shared_prefix_pages)
     need = workspace_size_mla(p) if mla else workspace_size(p)
     if workspace is None:
         counters = 8 * q.shape[0] * Hkv if single_launch else 0
@@ -272,7 +276,7 @@ def _run(q, k_pool, v_pool, block_table, seq_lens, *, mla, page_size, scale, Hkv
 
 def decode_attn(q, k_pool, v_pool, block_table, seq_lens, *, page_size, scale, out=None, lse=None,
                 workspace=None, err_flags=None, num_ctas=0, max_seq_len=0, layout="NHD",
-                stream=None, events=None, single_launch=False):
+                stream=None, events=None, single_launch=False, shared_prefix_pages=0):
     """GQA/MHA/MQA paged decode attention (zl_decode_attn).
 
     q [B, q_len, Hq, 128] bf16; k_pool, v_pool [pages, page_size, Hkv, 128]
@@ -281,12 +285,15 @@ def decode_attn(q, k_pool, v_pool, block_table, seq_lens, *, page_size, scale, o
     bf16. single_launch: merge split-KV partials inside the attention kernel
     (ZL_DECODE_SINGLE_LAUNCH; a caller's workspace must then hold zeroed
     arrival counters, see the header; the default cached one is kept so).
+    shared_prefix_pages: the first pages of every block-table row are the same
+    shared prefix (read once per group of sequences; see the header).
     """
     Hkv = k_pool.shape[2] if layout == "NHD" else k_pool.shape[1]
     return _run(q, k_pool, v_pool, block_table, seq_lens, mla=False, page_size=page_size,
                 scale=scale, Hkv=Hkv, D_v=q.shape[3], out=out, lse=lse, workspace=workspace,
                 err_flags=err_flags, num_ctas=num_ctas, max_seq_len=max_seq_len, layout=layout,
-                stream=stream, events=events, single_launch=single_launch)
+                stream=stream, events=events, single_launch=single_launch,
+                shared_prefix_pages=shared_prefix_pages)
 
 
 def decode_attn_mla(q, kv_pool, block_table, seq_lens, *, page_size, scale, D_v=512, out=None,

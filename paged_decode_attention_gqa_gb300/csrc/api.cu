@@ -81,7 +81,10 @@ zl_status current_device(DeviceInfo* info) {
 struct GqaPlan {
   int hpc = 0, nhg = 0, g = 0, grid = 0;
   bool fused = false;
-  size_t off_prefix = 0, off_lse = 0, off_o = 0, bytes = 0;
+  // shared-prefix calls: prefix tiles, sequences per group, groups
+  int prefix_tiles = 0, sgs = 0, ng = 0;
+  size_t off_prefix = 0, off_lse = 0, off_o = 0, off_pre_lse = 0, off_pre_o = 0;
+  size_t off_suf_lse = 0, off_suf_o = 0, bytes = 0;
 };
 
 zl_status gqa_validate_shape(const zl_decode_attn_params* a) {
@@ -99,6 +102,10 @@ zl_status gqa_validate_shape(const zl_decode_attn_params* a) {
   if (a->Hq / a->Hkv * a->q_len > 16) return ZL_ERR_UNSUPPORTED;  // (query, head) rows per tile
   if (a->page_size % zl::kGqaTile != 0 || a->page_size > 1024) return ZL_ERR_UNSUPPORTED;
   if (a->B > zl::kMaxBatch) return ZL_ERR_UNSUPPORTED;
+  if (a->shared_prefix_pages < 0 || a->shared_prefix_pages > a->block_table_stride)
+    return ZL_ERR_INVALID_ARG;
+  if (a->shared_prefix_pages > 0 && (a->flags & ZL_DECODE_SINGLE_LAUNCH))
+    return ZL_ERR_UNSUPPORTED;
   return ZL_OK;
 }
 
@@ -111,14 +118,23 @@ zl_status gqa_plan(const zl_decode_attn_params* a, GqaPlan* plan) {
   plan->fused = (a->flags & ZL_DECODE_SINGLE_LAUNCH) != 0;
   plan->hpc = zl::gqa_heads_per_cta(a->Hkv);
   plan->nhg = a->Hkv / plan->hpc;
+  const int rps = plan->g * a->q_len;
+  if (a->shared_prefix_pages > 0) {
+    plan->prefix_tiles = a->shared_prefix_pages * a->page_size / zl::kGqaTile;
+    plan->sgs = 16 / rps > 0 ? 16 / rps : 1;
+    plan->ng = (a->B + plan->sgs - 1) / plan->sgs;
+    if (plan->ng + a->B > zl::kMaxBatch) return ZL_ERR_UNSUPPORTED;  // one tile-count table
+  }
+  const int rows_per_warp = plan->prefix_tiles > 0 ? plan->sgs * rps : rps;
   int grid = a->num_ctas;
   if (grid == 0) {
     const int per_sm =
-        zl::gqa_ctas_per_sm(plan->hpc, plan->g * a->q_len > 8, a->q_len > 1, plan->fused,
-                            dev.device);
+        plan->prefix_tiles > 0
+            ? zl::gqa_shared_ctas_per_sm(plan->hpc, rows_per_warp > 8, a->q_len > 1, dev.device)
+            : zl::gqa_ctas_per_sm(plan->hpc, rps > 8, a->q_len > 1, plan->fused, dev.device);
     if (per_sm < 1) return ZL_ERR_CUDA;
     grid = dev.sms * per_sm;
-    if (a->max_seq_len > 0) {
+    if (a->max_seq_len > 0 && plan->prefix_tiles == 0) {
       // No more CTAs than tiles: B * head groups * ceil(max_seq_len / 16).
       const int64_t tiles = int64_t(a->B) * plan->nhg *
                             ((int64_t(a->max_seq_len) + zl::kGqaTile - 1) / zl::kGqaTile);
@@ -126,13 +142,24 @@ zl_status gqa_plan(const zl_decode_attn_params* a, GqaPlan* plan) {
     }
   }
   plan->grid = grid;
-  const size_t rows = size_t(grid) * 2 * plan->hpc * plan->g * a->q_len;  // partial slots
+  const size_t rows = size_t(grid) * 2 * plan->hpc * rows_per_warp;  // partial slots
+  const size_t store_rows = plan->prefix_tiles > 0 ? size_t(a->B) * a->q_len * a->Hq : 0;
   // [0, off_prefix): one arrival counter (8 bytes) per (sequence, kv head);
-  // [off_prefix, off_lse): the tile prefix sums the merge kernel reads.
+  // [off_prefix, off_lse): the tile prefix sums the merge kernel reads (one per
+  // unit: groups, then sequences); then the partials' lse and outputs; then
+  // (shared prefix) each query row's result over its prefix part and over its
+  // suffix part when one CTA had the whole unit: base-2 lse and normalised
+  // fp32 output.
   plan->off_prefix = round_up(size_t(a->B) * a->Hkv * sizeof(unsigned long long), 256);
-  plan->off_lse = plan->off_prefix + round_up(size_t(a->B + 1) * sizeof(int32_t), 256);
+  plan->off_lse =
+      plan->off_prefix + round_up(size_t(plan->ng + a->B + 1) * sizeof(int32_t), 256);
   plan->off_o = plan->off_lse + round_up(rows * sizeof(float), 256);
-  plan->bytes = plan->off_o + rows * zl::kGqaHeadDim * sizeof(float);
+  plan->off_pre_lse = plan->off_o + round_up(rows * zl::kGqaHeadDim * sizeof(float), 256);
+  plan->off_pre_o = plan->off_pre_lse + round_up(store_rows * sizeof(float), 256);
+  plan->off_suf_lse =
+      plan->off_pre_o + round_up(store_rows * zl::kGqaHeadDim * sizeof(float), 256);
+  plan->off_suf_o = plan->off_suf_lse + round_up(store_rows * sizeof(float), 256);
+  plan->bytes = plan->off_suf_o + store_rows * zl::kGqaHeadDim * sizeof(float);
   return ZL_OK;
 }
 
@@ -153,6 +180,7 @@ zl_status mla_validate_shape(const zl_decode_attn_params* a) {
   if (a->flags & ~uint32_t(ZL_DECODE_SINGLE_LAUNCH | ZL_DECODE_TEST_STALL))
     return ZL_ERR_INVALID_ARG;
   if (a->flags) return ZL_ERR_UNSUPPORTED;  // neither flag exists for MLA
+  if (a->shared_prefix_pages != 0) return ZL_ERR_UNSUPPORTED;
   if (a->D_qk != zl::kMlaDqk || a->D_v != zl::kMlaDv) return ZL_ERR_UNSUPPORTED;
   if (a->Hq != zl::kMlaHeads) return ZL_ERR_UNSUPPORTED;
   if (a->q_len != 1) return ZL_ERR_UNSUPPORTED;
@@ -275,11 +303,22 @@ zl_status zl_decode_attn(const zl_decode_attn_params* a, zl_stream_t stream) {
   p.hpc = plan.hpc;
   p.nhg = plan.nhg;
   p.scale_log2 = float(double(a->scale) * kLog2e);
+  p.prefix_tiles = plan.prefix_tiles;
+  p.sgs = plan.sgs;
+  p.ng = plan.ng;
+  p.pre_lse = reinterpret_cast<float*>(ws + plan.off_pre_lse);
+  p.pre_o = reinterpret_cast<float*>(ws + plan.off_pre_o);
+  p.suf_lse = reinterpret_cast<float*>(ws + plan.off_suf_lse);
+  p.suf_o = reinterpret_cast<float*>(ws + plan.off_suf_o);
 
-  const cudaError_t e = zl::gqa_decode_launch(p, plan.grid, plan.fused,
-                                              reinterpret_cast<cudaStream_t>(stream),
-                                              reinterpret_cast<cudaEvent_t>(a->attn_begin),
-                                              reinterpret_cast<cudaEvent_t>(a->attn_end));
+  const cudaError_t e =
+      plan.prefix_tiles > 0
+          ? zl::gqa_shared_launch(p, plan.grid, reinterpret_cast<cudaStream_t>(stream),
+                                  reinterpret_cast<cudaEvent_t>(a->attn_begin),
+                                  reinterpret_cast<cudaEvent_t>(a->attn_end))
+          : zl::gqa_decode_launch(p, plan.grid, plan.fused, reinterpret_cast<cudaStream_t>(stream),
+                                  reinterpret_cast<cudaEvent_t>(a->attn_begin),
+                                  reinterpret_cast<cudaEvent_t>(a->attn_end));
   return e == cudaSuccess ? ZL_OK : ZL_ERR_CUDA;
 }
 

@@ -1,0 +1,880 @@
+// Paged GQA decode attention for sm_103a: one persistent wave of CTAs, each a
+// TMA producer warp plus one tensor-core consumer warp per kv head.
+//
+// Work decomposition. For sequence b the context is cut into n_b tiles of 16
+// tokens. The tiles of all (sequence, kv-head-group) units are laid end to end
+// and the line is cut into G equal ranges, one per CTA ("split-KV" of the
+// flash_decoding family named under "技术架构：五层模块化设计" on the
+// "ZhiLight：知乎开源的高性能 LLM 推理加速引擎" page). A CTA whose range covers a
+// whole unit writes the final output; a unit cut between CTAs leaves one
+// normalised partial (o, lse) per CTA in the workspace. Each consumer warp
+// that writes a partial then counts its arrival on the (sequence, kv head)
+// counter; the warp that arrives last combines all the partials of its rows
+// by log-sum-exp, always in CTA order, so the result does not depend on
+// which CTA finished last: one launch, deterministic. The cut depends only on
+// seq_lens and G, so results are bit-identical under page remapping.
+//
+// Per tile (16 tokens x HPC kv heads), the producer issues four TMA loads (K
+// and V, two 64-column halves each, 128-byte swizzled) into a ring of
+// shared-memory stages guarded by mbarriers. Consumer warp w owns kv head w of
+// the group: its g query heads are the rows of an m16n8k16 tensor-core tile
+// ("fused batch attention for decoding using tensor core instructions", the
+// "ZhiLight: Zhihu's CUDA Inference Engine..." page, "Dual streams, host
+// all-reduce and the memory model"), S = Q K^T and O += P V run on mma.sync,
+// and the online softmax (running max, rescaled sum) stays in registers with
+// quad shuffles. With q_len > 1 query tokens per sequence the rows are the
+// (token, head) pairs, g * q_len <= 16 of them, each with its causal limit
+// (the CAUSAL instances; q_len = 1 runs the instances without the limit).
+#pragma once
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+#include <math_constants.h>
+
+namespace zl {
+
+namespace {
+
+constexpr uint32_t kErrBadPage = 1u;
+constexpr uint32_t kErrBadLen = 2u;
+constexpr uint32_t kErrTimeout = 4u;
+constexpr uint32_t kErrBadPrefix = 8u;
+constexpr int kMergeRows = 4;  // rows merged together by the split merge
+
+// What one launch of the attention kernel covers.
+constexpr int kModePlain = 0;   // every sequence over all of its own pages
+// Shared prefix: units (group of sgs sequences, head group) over the prefix
+// tiles, then units (sequence, head group) over each sequence's tiles past
+// the prefix, on one tile line; whole units leave fp32 results in the prefix
+// and suffix stores, and the merge kernel combines both parts of every row.
+constexpr int kModeShared = 1;
+constexpr uint64_t kTestStallNs = 50ull * 1000 * 1000;  // bound of the test-hook wait
+
+template <int HPC>
+struct GqaCfg {
+  static constexpr int kHalfBytes = HPC * kGqaTile * 64 * 2;  // one 64-column half of K or V
+  static constexpr int kStageBytes = 4 * kHalfBytes;           // K lo | K hi | V lo | V hi
+  static constexpr int kStages = HPC == 8 ? 3 : HPC == 4 ? 4 : HPC == 2 ? 6 : 8;
+  static constexpr int kThreads = (HPC + 1) * 32;
+  // 1 KB alignment slack + stages + barriers + per-stage flags + abort flag + prefix table
+  // + split-piece records (2 per consumer warp)
+  static constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStageBytes + kStages * 16 +
+                                       kStages * 4 + 16 + (kMaxBatch + 1) * 4 + HPC * 2 * 4;
+};
+
+__device__ __forceinline__ void raise_error(uint32_t* flags, uint32_t bits) {
+  if (flags) atomicOr(flags, bits);
+}
+
+// Index of the sequence whose tile range contains global tile `idx`:
+// the largest b with nhg * prefix[b] <= idx (sequences with no tiles are skipped
+// because the next prefix equals theirs).
+__device__ __forceinline__ int locate_seq(const int* prefix, int B, int nhg, int64_t idx) {
+  int lo = 0, hi = B;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (int64_t(nhg) * prefix[mid] <= idx) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// First tile of CTA cc's range when W tiles are cut into G ranges
+// [floor(cc W / G), floor((cc+1) W / G)), from Wq = W / G and Wr = W % G:
+// floor(cc W / G) = cc Wq + floor(cc Wr / G), and cc Wr < G^2 < 2^32 (G is
+// at most 65535), so no 64-bit division is needed.
+struct TileCut {
+  int64_t Wq;
+  uint32_t Wr, G;
+  __device__ __forceinline__ int64_t start(int cc) const {
+    return int64_t(cc) * Wq + int64_t((uint32_t(cc) * Wr) / G);
+  }
+};
+
+// 64-bit compare-and-swap with acquire-release semantics at GPU scope: the
+// arriving warp's partial rows (ordered before it by __syncwarp) are released
+// with its arrival, and the last arrival acquires everyone else's.
+__device__ __forceinline__ unsigned long long cas_acq_rel(unsigned long long* addr,
+                                                          unsigned long long cmp,
+                                                          unsigned long long val) {
+  unsigned long long old;
+  asm volatile("atom.acq_rel.gpu.global.cas.b64 %0, [%1], %2, %3;"
+               : "=l"(old)
+               : "l"(addr), "l"(cmp), "l"(val)
+               : "memory");
+  return old;
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed(const unsigned long long* addr) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed(unsigned long long* addr, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(addr), "l"(v) : "memory");
+}
+
+// Count one arrival on a split unit's counter (epoch << 32 | count; a word
+// from another epoch counts as 0, so a call that stopped early cannot confuse
+// the next one). Returns true for the last of `pieces` arrivals, which also
+// puts the word back to 0. The first CAS guesses the usual state of a unit's
+// first arrival (a zero word), so that arrival costs one round trip. The CAS
+// retries only while other CTAs update the same word; the bound is a guard,
+// never reached by a correct schedule.
+__device__ __forceinline__ bool arrive_last(unsigned long long* word, uint32_t epoch, int pieces,
+                                            uint32_t* err_flags) {
+  unsigned long long old = 0ull;
+  for (int tries = 0; tries < (1 << 20); ++tries) {
+    const uint32_t cnt = uint32_t(old >> 32) == epoch ? uint32_t(old) : 0u;
+    const unsigned long long want = (static_cast<unsigned long long>(epoch) << 32) | (cnt + 1u);
+    const unsigned long long seen = cas_acq_rel(word, old, want);
+    if (seen == old) {
+      if (int(cnt + 1u) < pieces) return false;
+      st_relaxed(word, 0ull);
+      return true;
+    }
+    old = seen;
+  }
+  raise_error(err_flags, kErrTimeout);
+  return false;
+}
+
+// The CTAs holding pieces of a split unit (first tile U0, n tiles) that CTA c
+// takes part in: c_lo owns tile U0, c_hi the last tile, c lies between them.
+// Returns how many of them have a non-empty range (one piece each).
+__device__ __forceinline__ int split_cta_span(const TileCut& cut, int64_t U0, int n, int c,
+                                              int& c_lo, int& c_hi) {
+  int pieces = 1;
+  c_lo = c_hi = c;
+  while (cut.start(c_lo) > U0) {
+    --c_lo;
+    pieces += cut.start(c_lo) < cut.start(c_lo + 1) ? 1 : 0;
+  }
+  while (cut.start(c_hi + 1) < U0 + n) {
+    ++c_hi;
+    pieces += cut.start(c_hi) < cut.start(c_hi + 1) ? 1 : 0;
+  }
+  return pieces;
+}
+
+// Log-sum-exp merge of the R rows of kv head w (of CTA head group hg) over the
+// pieces of a split unit, by the warp whose arrival was the last (single
+// launch) or by the merge kernel: a running max and rescaled sums per row,
+// always in CTA order, so the result does not depend on who merges. Rows go in blocks of kMergeRows and pieces in
+// batches of kMergePieces: a lane loads every row's lse and its own 4 columns
+// of every row of a batch at once, so a batch costs one round trip to L2.
+// Merging the same pieces with any batch size gives the same bits.
+// Running log-sum-exp merge of kMergeRows rows (base-2 lse): a running max,
+// the rescaled weight sum and the rescaled sum of normalised outputs. A
+// source with lse NaN (a bad page) marks the rows bad; lse -inf weighs 0.
+struct MergeAcc {
+  float mx[kMergeRows], den[kMergeRows];
+  float4 acc[kMergeRows];
+  bool bad;
+  __device__ __forceinline__ void init() {
+#pragma unroll
+    for (int k = 0; k < kMergeRows; ++k) {
+      mx[k] = -CUDART_INF_F;
+      den[k] = 0.f;
+      acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    bad = false;
+  }
+  __device__ __forceinline__ void add(int k, float l, float4 o) {
+    bad |= isnan(l);
+    const float mn = fmaxf(mx[k], l);
+    if (mn != -CUDART_INF_F && !isnan(l)) {
+      const float a = ex2_approx(mx[k] - mn), wgt = ex2_approx(l - mn);
+      den[k] = den[k] * a + wgt;
+      acc[k].x = acc[k].x * a + wgt * o.x;
+      acc[k].y = acc[k].y * a + wgt * o.y;
+      acc[k].z = acc[k].z * a + wgt * o.z;
+      acc[k].w = acc[k].w * a + wgt * o.w;
+      mx[k] = mn;
+    }
+  }
+};
+
+// Adds the partials of rows [row_off + r0, row_off + r0 + nrows) (slot stride
+// R) of the pieces of a unit (first tile U0) held by CTAs c_lo..c_hi, in CTA
+// order; pieces go in batches of kMergePieces whose loads are issued together
+// (one L2 round trip per batch).
+template <int kMergePieces>
+__device__ __forceinline__ void merge_add_pieces(MergeAcc& m, const GqaParams& p,
+                                                 const TileCut& cut, int64_t U0, int c_lo,
+                                                 int c_hi, int w, int R, int row_off, int r0,
+                                                 int nrows, int lane) {
+  for (int cb = c_lo; cb <= c_hi; cb += kMergePieces) {
+    float lv[kMergePieces][kMergeRows];
+    float4 ov[kMergePieces][kMergeRows];
+    bool use[kMergePieces];
+#pragma unroll
+    for (int q = 0; q < kMergePieces; ++q) {
+      const int cc = cb + q;
+      const int64_t s_cc = cut.start(cc);
+      use[q] = cc <= c_hi && s_cc < cut.start(cc + 1);
+      const int sl = (cc == c_lo && U0 > s_cc) ? 1 : 0;
+      const int64_t base = ((int64_t(cc) * 2 + sl) * p.hpc + w) * R + row_off + r0;
+#pragma unroll
+      for (int k = 0; k < kMergeRows; ++k) {
+        if (use[q] && k < nrows) {
+          lv[q][k] = __ldcg(p.ws_lse + base + k);
+          ov[q][k] =
+              __ldcg(reinterpret_cast<const float4*>(p.ws_o + (base + k) * kGqaHeadDim) + lane);
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kMergePieces; ++q)
+#pragma unroll
+      for (int k = 0; k < kMergeRows; ++k)
+        if (use[q] && k < nrows) m.add(k, lv[q][k], ov[q][k]);
+  }
+}
+
+// Adds rows (sequence b, tile rows r0 + k of g * q_len, head group starting at
+// head0) from an fp32 store of whole-unit results.
+__device__ __forceinline__ void merge_add_store(MergeAcc& m, const GqaParams& p,
+                                                const float* st_o, const float* st_lse, int b,
+                                                int head0, int r0, int nrows, int lane) {
+  float lv[kMergeRows];
+  float4 ov[kMergeRows];
+#pragma unroll
+  for (int k = 0; k < kMergeRows; ++k) {
+    if (k < nrows) {
+      const int r = r0 + k;
+      const int64_t orow = (int64_t(b) * p.q_len + r / p.g) * p.Hq + head0 + r % p.g;
+      lv[k] = __ldcg(st_lse + orow);
+      ov[k] = __ldcg(reinterpret_cast<const float4*>(st_o + orow * kGqaHeadDim) + lane);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kMergeRows; ++k)
+    if (k < nrows) m.add(k, lv[k], ov[k]);
+}
+
+// Writes the merged rows of sequence b as bf16 out and natural-log lse; a bad
+// source or a row with no weight gives zeros and lse = -inf.
+__device__ __forceinline__ void merge_write_out(const MergeAcc& m, const GqaParams& p, int b,
+                                                int head0, int r0, int nrows, int lane) {
+#pragma unroll
+  for (int k = 0; k < kMergeRows; ++k) {
+    if (k < nrows) {
+      const int r = r0 + k;
+      const int64_t orow = (int64_t(b) * p.q_len + r / p.g) * p.Hq + head0 + r % p.g;
+      const bool none = m.bad || !(m.den[k] > 0.f);
+      const float inv = none ? 0.f : 1.f / m.den[k];
+      uint2 packed = make_uint2(0u, 0u);
+      if (!none) {
+        packed.x = pack_bf16x2(m.acc[k].x * inv, m.acc[k].y * inv);
+        packed.y = pack_bf16x2(m.acc[k].z * inv, m.acc[k].w * inv);
+      }
+      reinterpret_cast<uint2*>(p.out + orow * kGqaHeadDim)[lane] = packed;
+      if (p.lse && lane == 0)
+        p.lse[orow] = none ? -CUDART_INF_F : (m.mx[k] + log2f(m.den[k])) * 0.69314718055994531f;
+    }
+  }
+}
+
+// A plain unit (sequence b, kv head w of the CTA group, first tile U0) cut
+// between CTAs c_lo..c_hi: merge rows [r_begin, r_end) and write them.
+template <int kMergePieces>
+__device__ __forceinline__ void merge_split_rows(const GqaParams& p, const TileCut& cut,
+                                                 int64_t U0, int c_lo, int c_hi, int b, int w,
+                                                 int head0, int R, int r_begin, int r_end,
+                                                 int lane) {
+  for (int r0 = r_begin; r0 < r_end; r0 += kMergeRows) {
+    const int nrows = min(kMergeRows, r_end - r0);
+    MergeAcc m;
+    m.init();
+    merge_add_pieces<kMergePieces>(m, p, cut, U0, c_lo, c_hi, w, R, 0, r0, nrows, lane);
+    merge_write_out(m, p, b, head0, r0, nrows, lane);
+  }
+}
+
+template <int HPC, bool ROWS16, bool CAUSAL, bool FUSED, int MODE = kModePlain>
+__global__ void __launch_bounds__(GqaCfg<HPC>::kThreads, 1)
+gqa_decode_kernel(const __grid_constant__ GqaParams p) {
+  static_assert(MODE == kModePlain || !FUSED, "the in-kernel merge is for plain launches");
+  using Cfg = GqaCfg<HPC>;
+  constexpr int NS = Cfg::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;  // 128B swizzle wants 1 KB-aligned stages
+  uint8_t* smem = smem_raw + (sbase - raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * Cfg::kStageBytes);
+  uint64_t* empty = full + NS;
+  int* stage_bad = reinterpret_cast<int*>(empty + NS);
+  volatile int* abort_flag = stage_bad + NS;
+  int* prefix = stage_bad + NS + 4;
+  int* split_rec = prefix + kMaxBatch + 1;  // [HPC][2]: b | hg << 12 of a split piece, or -1
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int B = p.B;
+  const int64_t cap = p.bt_stride * int64_t(p.page_size);
+
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), HPC);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == HPC && lane == 0) {
+    tma_prefetch_desc(&p.tmap_k);
+    tma_prefetch_desc(&p.tmap_v);
+  }
+  // Launched as a programmatic dependent of whatever kernel precedes it on the
+  // stream (e.g. the KV append): everything above overlaps that kernel's tail;
+  // nothing in global memory is read or written before it has finished.
+  griddep_wait();
+
+  // Units of this launch (one "virtual sequence" v each per head group):
+  // plain, v = sequence; shared prefix, v < ng a group of sgs sequences over
+  // the prefix tiles, v >= ng sequence v - ng over its tiles past the prefix.
+  // Their tiles and the exclusive prefix sum (warp 0).
+  const int PT = p.prefix_tiles;
+  const int NG = MODE == kModeShared ? p.ng : 0;
+  const int V = NG + B;
+  auto unit_tiles = [&](int v) -> int {
+    if (v < NG) return PT;
+    const int L = p.seq_lens[v - NG];
+    if (!(L >= 0 && int64_t(L) <= cap)) return 0;
+    const int t = (L + kGqaTile - 1) / kGqaTile - (MODE == kModeShared ? PT : 0);
+    return t > 0 ? t : 0;
+  };
+  if (warp == 0) {
+    const int per = (V + 31) / 32;
+    const int v0 = lane * per;
+    int local = 0;
+    for (int i = 0; i < per; ++i) {
+      const int v = v0 + i;
+      if (v < V) {
+        if (v >= NG && blockIdx.x == 0) {
+          const int L = p.seq_lens[v - NG];
+          if (!(L >= 0 && int64_t(L) <= cap)) raise_error(p.err_flags, kErrBadLen);
+        }
+        local += unit_tiles(v);
+      }
+    }
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += x;
+    }
+    int run = incl - local;
+    for (int i = 0; i < per; ++i) {
+      const int v = v0 + i;
+      if (v < V) {
+        prefix[v] = run;
+        run += unit_tiles(v);
+      }
+    }
+    if (lane == 31) prefix[V] = incl;
+  } else if (MODE == kModeShared && warp == 1) {
+    // The caller states that every sequence starts with the same prefix_tiles
+    // tiles of pages and that every query row sees all of them; CTA c checks
+    // sequences c, c + G, ... and flags a violation (results are then void).
+    const int ppages = PT * kGqaTile / p.page_size;
+    for (int b = blockIdx.x; b < B; b += gridDim.x) {
+      int bad = 0;
+      for (int j = lane; j < ppages; j += 32)
+        bad |= p.block_table[int64_t(b) * p.bt_stride + j] != p.block_table[j] ? 1 : 0;
+      const int L = p.seq_lens[b];
+      if (lane == 0 && (int64_t(L) > cap || L - p.q_len + 1 < PT * kGqaTile)) bad = 1;
+      if (__any_sync(0xffffffffu, bad) && lane == 0) raise_error(p.err_flags, kErrBadPrefix);
+    }
+  }
+  __syncthreads();
+
+  if constexpr (!FUSED) {
+    // The merge kernel reads the tile counts, and may be scheduled early:
+    // it waits for this whole grid to finish before reading anything.
+    if (blockIdx.x == 0)
+      for (int v = tid; v <= V; v += Cfg::kThreads) p.ws_prefix[v] = prefix[v];
+    griddep_launch_dependents();
+  }
+
+  const int G = gridDim.x, c = blockIdx.x;
+  const int nhg = p.nhg;
+  const int64_t W = int64_t(nhg) * prefix[V];
+  const TileCut cut{W / G, uint32_t(W % G), uint32_t(G)};
+  const int64_t s_c = cut.start(c);
+  const int64_t e_c = cut.start(c + 1);
+
+  if (warp == HPC) {
+    // ------------------------------------------------------------ producer
+    if (p.test_stall) {
+      // Failure-detection test hook: wait on a word nothing sets until the
+      // bound runs out, then stop the CTA the way a stalled pipeline does.
+      __shared__ int never_set;
+      if (lane == 0) {
+        never_set = 0;
+        if (!flag_wait(&never_set, kTestStallNs)) {
+          raise_error(p.err_flags, kErrTimeout);
+          *abort_flag = 1;
+        }
+      }
+      __syncwarp();
+      return;
+    }
+    int it = 0;
+    bool aborted = false;
+    for (int64_t base = s_c; base < e_c && !aborted; base += 32) {
+      // lane i resolves tile base + i: page id, slot and head group
+      const int64_t idx = base + lane;
+      int page = 0, slot = 0, hg = 0, bad = 0;
+      if (idx < e_c) {
+        const int v = locate_seq(prefix, V, nhg, idx);
+        const int n = prefix[v + 1] - prefix[v];
+        const int64_t r = idx - int64_t(nhg) * prefix[v];
+        hg = int(r / n);
+        const bool pre = v < NG;  // a prefix unit
+        const int tok0 = (MODE == kModeShared && !pre ? PT * kGqaTile : 0) + int(r % n) * kGqaTile;
+        const int trow = pre ? v * p.sgs : v - NG;  // a block-table row to read
+        slot = tok0 % p.page_size;
+        page = p.block_table[int64_t(trow) * p.bt_stride + tok0 / p.page_size];
+        bad = (page < 0 || page >= p.num_pages) ? 1 : 0;
+      }
+      const int cnt = int(min(int64_t(32), e_c - base));
+      for (int k = 0; k < cnt; ++k, ++it) {
+        const int pg = __shfl_sync(0xffffffffu, page, k);
+        const int sl = __shfl_sync(0xffffffffu, slot, k);
+        const int h = __shfl_sync(0xffffffffu, hg, k);
+        const int bd = __shfl_sync(0xffffffffu, bad, k);
+        int ok = 1;
+        if (lane == 0) {
+          const int stage = it % NS;
+          const uint32_t phase = (it / NS) & 1;
+          if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag)) {
+            raise_error(p.err_flags, kErrTimeout);
+            *abort_flag = 1;
+            ok = 0;
+          } else {
+            stage_bad[stage] = bd;
+            const uint32_t fb = smem_u32(&full[stage]);
+            if (bd) {
+              mbar_arrive(fb);  // nothing to load; the consumer discards this piece
+            } else {
+              const uint32_t dst = sbase + stage * Cfg::kStageBytes;
+              mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
+              tma_load_4d(dst, &p.tmap_k, fb, 0, sl, h * HPC, pg);
+              tma_load_4d(dst + Cfg::kHalfBytes, &p.tmap_k, fb, 64, sl, h * HPC, pg);
+              tma_load_4d(dst + 2 * Cfg::kHalfBytes, &p.tmap_v, fb, 0, sl, h * HPC, pg);
+              tma_load_4d(dst + 3 * Cfg::kHalfBytes, &p.tmap_v, fb, 64, sl, h * HPC, pg);
+            }
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          aborted = true;
+          break;
+        }
+      }
+    }
+    // Do not leave the CTA with copies in flight: wait for the last stages.
+    if (lane == 0) {
+      const int first = it > NS ? it - NS : 0;
+      for (int j = first; j < it; ++j) {
+        const volatile int never = 0;
+        mbar_wait(smem_u32(&full[j % NS]), (j / NS) & 1, &never);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int w = warp;                 // kv head within the group
+  const int gid = lane >> 2, t4 = lane & 3;
+  const int g = p.g;
+  const float scale_log2 = p.scale_log2;
+  int it = 0;
+  int64_t idx = s_c;
+  if (lane == 0) split_rec[2 * w] = split_rec[2 * w + 1] = -1;
+  while (idx < e_c) {
+    const int v = locate_seq(prefix, V, nhg, idx);
+    const int n = prefix[v + 1] - prefix[v];
+    const int64_t unit_start0 = int64_t(nhg) * prefix[v];
+    const int hg = int((idx - unit_start0) / n);
+    const int j0 = int((idx - unit_start0) % n);
+    const int64_t unit_end = unit_start0 + int64_t(hg + 1) * n;
+    const int64_t piece_end = min(e_c, unit_end);
+    const int ntiles = int(piece_end - idx);
+    const bool partial = (j0 > 0) || (piece_end < unit_end);
+    const int slot = (idx == s_c) ? 0 : 1;
+    // The unit's (first) sequence: a prefix unit covers the sgs sequences b,
+    // b + 1, ... (fewer in the last group), any other unit one sequence.
+    const bool pre = v < NG;
+    const int b = pre ? v * p.sgs : v - NG;
+    // Tokens the unit's tiles cover end at L (a prefix unit: the whole prefix).
+    const int L = pre ? PT * kGqaTile : p.seq_lens[b];
+    const int head0 = (hg * HPC + w) * g;  // first query head of this kv head
+    // m16 tile rows are (sequence b + r / rps, query token i, head head0 + j)
+    // with rps = g * q_len rows per sequence, r % rps = i * g + j; R rows per
+    // partial slot, R_act of them exist, the rest are zero. Query i sees tokens
+    // t < L - q_len + 1 + i (the new tokens are in the cache; each sees itself
+    // and what precedes it); every row sees all of a shared prefix.
+    const int rps = g * p.q_len;
+    const int R = MODE == kModeShared ? p.sgs * rps : rps;
+    const int R_act = pre ? min(p.sgs, B - b) * rps : rps;
+    const int ra = gid, rb = gid + 8;
+    const int lim_a = pre ? (1 << 30) : L - p.q_len + 1 + ra / g;
+    const int lim_b = pre ? (1 << 30) : L - p.q_len + 1 + rb / g;
+    auto qrow_index = [&](int r) -> int64_t {
+      const int rr = r % rps;
+      return (int64_t(b + r / rps) * p.q_len + rr / g) * p.Hq + head0 + rr % g;
+    };
+
+    uint32_t qa[8][4];
+    {
+      const bool r0 = ra < R_act, r1 = ROWS16 && rb < R_act;
+      const uint32_t* q0 =
+          reinterpret_cast<const uint32_t*>(p.q + (r0 ? qrow_index(ra) : 0) * kGqaHeadDim);
+      const uint32_t* q1 =
+          reinterpret_cast<const uint32_t*>(p.q + (r1 ? qrow_index(rb) : 0) * kGqaHeadDim);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const int wd = ks * 8 + t4;  // 32-bit word index of d = 16ks + 2t4
+        qa[ks][0] = r0 ? __ldg(q0 + wd) : 0u;
+        qa[ks][2] = r0 ? __ldg(q0 + wd + 4) : 0u;
+        qa[ks][1] = r1 ? __ldg(q1 + wd) : 0u;
+        qa[ks][3] = r1 ? __ldg(q1 + wd + 4) : 0u;
+      }
+    }
+
+    float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
+    float o[16][4];
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+    int bad = 0;
+
+    // One row's online-softmax step in base 2 over this thread's four scores
+    // (tokens 2t4, 2t4+1, 2t4+8, 2t4+9 of the tile; vis = visible tokens of
+    // the row in this tile). A row with nothing visible yet keeps m = -inf and
+    // contributes zeros.
+    auto row_step = [&](float sa, float sb, float sc, float sd, int vis, float& m, float& l,
+                        uint32_t& p_lo, uint32_t& p_hi) -> float {
+      const float x0 = 2 * t4 < vis ? sa * scale_log2 : -CUDART_INF_F;
+      const float x1 = 2 * t4 + 1 < vis ? sb * scale_log2 : -CUDART_INF_F;
+      const float x2 = 2 * t4 + 8 < vis ? sc * scale_log2 : -CUDART_INF_F;
+      const float x3 = 2 * t4 + 9 < vis ? sd * scale_log2 : -CUDART_INF_F;
+      float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float mn = fmaxf(m, mx);
+      const float base = mn == -CUDART_INF_F ? 0.f : mn;
+      const float alpha = ex2_approx(m - base);
+      m = mn;
+      p_lo = pack_bf16x2(ex2_approx(x0 - base), ex2_approx(x1 - base));
+      p_hi = pack_bf16x2(ex2_approx(x2 - base), ex2_approx(x3 - base));
+      const float2 f0 = unpack_bf16x2(p_lo), f2 = unpack_bf16x2(p_hi);
+      l = l * alpha + ((f0.x + f0.y) + (f2.x + f2.y));
+      return alpha;
+    };
+
+    for (int t = 0; t < ntiles; ++t, ++it) {
+      const int stage = it % NS;
+      const uint32_t phase = (it / NS) & 1;
+      const int tok0 = (MODE == kModeShared && !pre ? PT * kGqaTile : 0) + (j0 + t) * kGqaTile;
+      const int valid = min(kGqaTile, L - tok0);  // tokens in the cache (V rows to keep)
+      if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag)) {
+        if (lane == 0) {
+          raise_error(p.err_flags, kErrTimeout);
+          *abort_flag = 1;
+        }
+        return;
+      }
+      bad |= stage_bad[stage];
+      const uint32_t kbase = sbase + stage * Cfg::kStageBytes + w * (kGqaTile * 128);
+      const uint32_t vbase = kbase + 2 * Cfg::kHalfBytes;
+
+      // S = Q K^T over the 16 tokens: two n8 tiles (tokens 0-7, 8-15).
+      float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      {
+        const int tok = (lane & 7) + ((lane >> 4) << 3);
+        const uint32_t row = kbase + tok * 128;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const int chunk = ((ks & 3) << 1) + ((lane >> 3) & 1);
+          const uint32_t addr = row + (ks >> 2) * Cfg::kHalfBytes + ((chunk ^ (tok & 7)) << 4);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(addr, b0, b1, b2, b3);
+          mma_bf16_16816(s[0], qa[ks], b0, b1);
+          mma_bf16_16816(s[1], qa[ks], b2, b3);
+        }
+      }
+
+      uint32_t pa[4];
+      {
+        const float alpha = row_step(s[0][0], s[0][1], s[1][0], s[1][1],
+                                     CAUSAL ? min(valid, lim_a - tok0) : valid, m0, l0, pa[0], pa[2]);
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+          o[nt][0] *= alpha;
+          o[nt][1] *= alpha;
+        }
+      }
+      if (ROWS16) {
+        const float alpha = row_step(s[0][2], s[0][3], s[1][2], s[1][3],
+                                     CAUSAL ? min(valid, lim_b - tok0) : valid, m1, l1, pa[1], pa[3]);
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+          o[nt][2] *= alpha;
+          o[nt][3] *= alpha;
+        }
+      } else {
+        pa[1] = pa[3] = 0u;
+      }
+
+      // O += P V. Token rows of V past the cache end are zeroed in registers so
+      // that NaN in unused slots cannot reach the output (0 * NaN = NaN).
+      {
+        const bool v00 = 2 * t4 < valid, v01 = 2 * t4 + 1 < valid;
+        const bool v10 = 2 * t4 + 8 < valid, v11 = 2 * t4 + 9 < valid;
+        const uint32_t m01 = (v00 ? 0x0000ffffu : 0u) | (v01 ? 0xffff0000u : 0u);
+        const uint32_t m89 = (v10 ? 0x0000ffffu : 0u) | (v11 ? 0xffff0000u : 0u);
+        const int tok = (lane & 7) + (((lane >> 3) & 1) << 3);
+        const uint32_t row = vbase + tok * 128;
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const int chunk = ((jj & 3) << 1) + (lane >> 4);
+          const uint32_t addr = row + (jj >> 2) * Cfg::kHalfBytes + ((chunk ^ (tok & 7)) << 4);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_trans(addr, b0, b1, b2, b3);
+          if (valid < kGqaTile) {
+            b0 &= m01;
+            b1 &= m89;
+            b2 &= m01;
+            b3 &= m89;
+          }
+          mma_bf16_16816(o[2 * jj], pa, b0, b1);
+          mma_bf16_16816(o[2 * jj + 1], pa, b2, b3);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
+    }
+
+    // ---- finalize the piece
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    if (ROWS16) {
+      l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    }
+    if (bad && lane == 0) raise_error(p.err_flags, kErrBadPage);
+#pragma unroll
+    for (int half = 0; half < (ROWS16 ? 2 : 1); ++half) {
+      const int r = half ? rb : ra;
+      if (r >= R_act) continue;
+      const float l = half ? l1 : l0;
+      const float m = half ? m1 : m0;
+      // A piece that met a bad page, or a row that saw no token, is written as
+      // zeros with lse = -inf (weight 0 in the merge).
+      const bool none = bad || !(l > 0.f);
+      const float inv = none ? 0.f : 1.f / l;
+      const float lse2 = none ? -CUDART_INF_F : m + log2f(l);
+      if (!partial && MODE == kModeShared) {
+        // a whole unit: the row's result over this part (prefix or suffix),
+        // for the merge kernel to combine
+        const int64_t orow = qrow_index(r);
+        float* st_o = pre ? p.pre_o : p.suf_o;
+        float* st_lse = pre ? p.pre_lse : p.suf_lse;
+        float2* dst = reinterpret_cast<float2*>(st_o + orow * kGqaHeadDim);
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt)
+          dst[nt * 4 + t4] = none ? make_float2(0.f, 0.f)
+                                  : make_float2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
+        if (t4 == 0) st_lse[orow] = bad ? CUDART_NAN_F : lse2;
+      } else if (!partial) {
+        const int64_t orow = qrow_index(r);
+        uint32_t* dst = reinterpret_cast<uint32_t*>(p.out + orow * kGqaHeadDim);
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt)
+          dst[nt * 4 + t4] =
+              none ? 0u : pack_bf16x2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
+        if (p.lse && t4 == 0) p.lse[orow] = lse2 * 0.69314718055994531f;
+      } else {
+        const int64_t wrow = ((int64_t(c) * 2 + slot) * HPC + w) * R + r;
+        float2* dst = reinterpret_cast<float2*>(p.ws_o + wrow * kGqaHeadDim);
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt)
+          dst[nt * 4 + t4] = none ? make_float2(0.f, 0.f)
+                                  : make_float2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
+        if (t4 == 0) p.ws_lse[wrow] = bad ? CUDART_NAN_F : lse2;
+      }
+    }
+    // A split piece is merged after the CTA's range is done (its partner
+    // pieces finish about then too); only its (b, hg) is kept meanwhile.
+    if (FUSED && partial && lane == 0) split_rec[2 * w + slot] = b | (hg << 12);
+    idx = piece_end;
+  }
+  // This warp's split pieces (at most two: the range's first and last) are
+  // written; count both arrivals at once (lane sl takes record sl; the CAS
+  // releases the rows the warp wrote before __syncwarp), then merge the units
+  // this warp completed. Without FUSED the merge kernel does it.
+  if constexpr (FUSED) {
+  __syncwarp();
+  int job = -1;
+  if (lane < 2) {
+    const int rec = split_rec[2 * w + lane];
+    if (rec >= 0) {
+      const int b = rec & 4095, hg = rec >> 12;
+      const int n = prefix[b + 1] - prefix[b];
+      int c_lo, c_hi;
+      const int pieces = split_cta_span(cut, int64_t(nhg) * prefix[b] + int64_t(hg) * n, n, c,
+                                        c_lo, c_hi);
+      if (arrive_last(p.ws_count + int64_t(b) * p.Hkv + hg * HPC + w, p.epoch, pieces,
+                      p.err_flags))
+        job = rec;
+    }
+  }
+  for (int sl = 0; sl < 2; ++sl) {
+    const int rec = __shfl_sync(0xffffffffu, job, sl);
+    if (rec < 0) continue;
+    const int b = rec & 4095, hg = rec >> 12;
+    const int n = prefix[b + 1] - prefix[b];
+    const int64_t U0 = int64_t(nhg) * prefix[b] + int64_t(hg) * n;
+    int c_lo, c_hi;
+    split_cta_span(cut, U0, n, c, c_lo, c_hi);
+    merge_split_rows<4>(p, cut, U0, c_lo, c_hi, b, w, (hg * HPC + w) * g, g * p.q_len, 0,
+                        g * p.q_len, lane);
+  }
+  }
+
+  if constexpr (MODE == kModePlain) {
+    // Sequences with no tiles (empty or invalid length): zeros, lse = -inf.
+    for (int b = c; b < B; b += G) {
+      if (prefix[b + 1] != prefix[b]) continue;
+      const int64_t rows = int64_t(p.q_len) * p.Hq;
+      uint4* dst = reinterpret_cast<uint4*>(p.out + int64_t(b) * rows * kGqaHeadDim);
+      const int64_t n16 = rows * kGqaHeadDim * 2 / 16;
+      for (int64_t i = tid; i < n16; i += HPC * 32) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (p.lse)
+        for (int64_t i = tid; i < rows; i += HPC * 32)
+          p.lse[int64_t(b) * rows + i] = -CUDART_INF_F;
+    }
+  }
+}
+
+
+// CTA that owns global tile x when W tiles are cut into G ranges.
+__device__ __forceinline__ int cta_of_tile(int64_t x, int64_t W, int G) {
+  return int(((x + 1) * G + W - 1) / W) - 1;
+}
+
+// Split-KV merge as its own launch (when the attention kernel runs without
+// FUSED), one warp per block of kMergeRows rows of a (sequence, kv head), with
+// the same arithmetic as the in-kernel merge, so both give the same bits.
+// Plain: only units cut between CTAs need it. Shared prefix: every row, from
+// its prefix part (the group unit's pieces, or the prefix store when one CTA
+// had the whole unit) then its suffix part (pieces, the suffix store, or
+// nothing when the sequence ends at the prefix), always in that order.
+// Launched as a programmatic dependent of the attention kernel: it may start
+// early and waits here until that grid has finished and its writes are
+// visible.
+template <int MODE>
+__global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ GqaParams p,
+                                                        int G) {
+  griddep_wait();
+  griddep_launch_dependents();  // the next kernels may start their prologue
+  const int lane = threadIdx.x & 31;
+  const int rps = p.g * p.q_len;
+  const int nrb = (rps + kMergeRows - 1) / kMergeRows;
+  const int64_t item = int64_t(blockIdx.x) * 4 + (threadIdx.x >> 5);
+  if (item >= int64_t(p.B) * p.Hkv * nrb) return;
+  const int64_t unit = item / nrb;  // b * Hkv + kv head
+  const int r0 = int(item % nrb) * kMergeRows;
+  const int nrows = min(kMergeRows, rps - r0);
+  const int b = int(unit / p.Hkv), kvh = int(unit % p.Hkv);
+  const int hg = kvh / p.hpc, w = kvh % p.hpc;
+  const int head0 = kvh * p.g;
+  const int* prefix = p.ws_prefix;
+  const int NG = MODE == kModeShared ? p.ng : 0;
+  const int64_t W = int64_t(p.nhg) * prefix[NG + p.B];
+  const TileCut cut{W / G, uint32_t(W % G), uint32_t(G)};
+  const int vs = NG + b;  // the sequence's own unit
+  const int n = prefix[vs + 1] - prefix[vs];
+  const int64_t U0 = int64_t(p.nhg) * prefix[vs] + int64_t(hg) * n;
+  const int c_lo = n ? cta_of_tile(U0, W, G) : 0, c_hi = n ? cta_of_tile(U0 + n - 1, W, G) : 0;
+  if constexpr (MODE == kModePlain) {
+    if (n == 0 || c_lo == c_hi) return;
+    merge_split_rows<2>(p, cut, U0, c_lo, c_hi, b, w, head0, rps, r0, r0 + nrows, lane);
+  } else {
+    const int R = p.sgs * rps;  // rows of a partial slot
+    MergeAcc m;
+    m.init();
+    {
+      const int vp = b / p.sgs;  // the group's prefix unit
+      const int np = prefix[vp + 1] - prefix[vp];
+      const int64_t P0 = int64_t(p.nhg) * prefix[vp] + int64_t(hg) * np;
+      const int p_lo = cta_of_tile(P0, W, G), p_hi = cta_of_tile(P0 + np - 1, W, G);
+      if (p_lo == p_hi)
+        merge_add_store(m, p, p.pre_o, p.pre_lse, b, head0, r0, nrows, lane);
+      else
+        merge_add_pieces<2>(m, p, cut, P0, p_lo, p_hi, w, R, (b % p.sgs) * rps, r0, nrows, lane);
+    }
+    if (n > 0) {
+      if (c_lo == c_hi)
+        merge_add_store(m, p, p.suf_o, p.suf_lse, b, head0, r0, nrows, lane);
+      else
+        merge_add_pieces<2>(m, p, cut, U0, c_lo, c_hi, w, R, 0, r0, nrows, lane);
+    }
+    merge_write_out(m, p, b, head0, r0, nrows, lane);
+  }
+}
+
+constexpr int kMaxDevices = 64;
+
+// Raise the dynamic shared-memory limit of one kernel instance, once per device.
+template <int HPC, bool R16, bool C, bool U, int MODE = kModePlain>
+cudaError_t configure(int device) {
+  static bool done[kMaxDevices] = {};
+  if (device >= 0 && device < kMaxDevices && done[device]) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(gqa_decode_kernel<HPC, R16, C, U, MODE>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             int(GqaCfg<HPC>::kSmemBytes));
+  if (e == cudaSuccess && device >= 0 && device < kMaxDevices) done[device] = true;
+  return e;
+}
+
+template <int HPC, bool R16, bool C, bool U, int MODE = kModePlain>
+cudaError_t launch_attn(const GqaParams& p, int grid, cudaStream_t stream) {
+  using Cfg = GqaCfg<HPC>;
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return e;
+  if ((e = configure<HPC, R16, C, U, MODE>(device)) != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(Cfg::kThreads);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gqa_decode_kernel<HPC, R16, C, U, MODE>, p);
+}
+
+template <int HPC, bool R16, bool C, bool U, int MODE = kModePlain>
+int occupancy(int device) {
+  using Cfg = GqaCfg<HPC>;
+  // Queried once per device (it does not change), not on every call.
+  static int cached[kMaxDevices] = {};
+  if (device >= 0 && device < kMaxDevices && cached[device] > 0) return cached[device];
+  if (configure<HPC, R16, C, U, MODE>(device) != cudaSuccess) return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_decode_kernel<HPC, R16, C, U, MODE>,
+                                                    Cfg::kThreads, Cfg::kSmemBytes) != cudaSuccess)
+    return 0;
+  if (device >= 0 && device < kMaxDevices) cached[device] = n;
+  return n;
+}
+
+}  // namespace
+}  // namespace zl

@@ -28,6 +28,16 @@ struct GqaParams {
   float* ws_lse;       // [G][2][HPC][g * q_len] base-2 lse of the partials (NaN = bad piece)
   uint32_t* err_flags; // or nullptr
   uint32_t epoch;      // nonzero, different for every host call
+  // Shared-prefix decode (zero otherwise): the first prefix_tiles tiles of
+  // every sequence are the same pages. Groups of sgs sequences (ng groups)
+  // attend to them together. A unit one CTA finishes leaves each query row's
+  // result over its part in pre_* (prefix) or suf_* (the rest): fp32
+  // normalised output [B, q_len, Hq, 128] and base-2 lse [B, q_len, Hq].
+  int prefix_tiles, sgs, ng;
+  float* pre_o;
+  float* pre_lse;
+  float* suf_o;
+  float* suf_lse;
   int test_stall;      // failure-detection test hook: stall the producer until its wait runs out
   int B, q_len, Hq, Hkv, g, page_size, num_pages;
   int hpc;             // kv heads per CTA
@@ -67,6 +77,11 @@ cudaError_t mla_decode_launch(const MlaParams& p, int clusters, cudaStream_t str
 int gqa_heads_per_cta(int Hkv);
 // CTAs of the attention kernel that fit on one SM (0 on error).
 int gqa_ctas_per_sm(int hpc, bool rows16, bool causal, bool fused, int device);
+// Shared-prefix decode: CTAs per SM of its attention kernel, and its two
+// launches (attention over prefix groups and suffixes, then the merge).
+int gqa_shared_ctas_per_sm(int hpc, bool rows16, bool causal, int device);
+cudaError_t gqa_shared_launch(const GqaParams& p, int grid, cudaStream_t stream,
+                              cudaEvent_t attn_begin, cudaEvent_t attn_end);
 // Launches the attention kernel on `grid` CTAs. fused: split units are merged
 // inside it (one launch); otherwise a merge kernel follows as a programmatic
 // dependent launch.
