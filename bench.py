@@ -36,7 +36,9 @@ UNIT = "GB/s"
 WORKLOAD = "llama3_8b_decode"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 CSRC = os.path.join(ROOT, "paged_decode_attention_gqa_gb300", "csrc")
-KERNEL_SRC = {"gqa": os.path.join(CSRC, "gqa_decode.cu"), "mla": os.path.join(CSRC, "mla_decode.cu")}
+# the sources whose hash must match the one an ncu traffic figure was taken with
+KERNEL_SRC = {"gqa": [os.path.join(CSRC, "gqa_kernel.cuh"), os.path.join(CSRC, "gqa_decode.cu")],
+              "mla": [os.path.join(CSRC, "mla_decode.cu")]}
 
 
 def measured_peaks():
@@ -49,8 +51,11 @@ def measured_peaks():
 
 
 def kernel_hash(kind):
-    with open(KERNEL_SRC[kind], "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for path in KERNEL_SRC[kind]:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def traffic_per_launch(workload, kind):
