@@ -209,8 +209,32 @@ zl_status mla_plan(const zl_decode_attn_params* a, MlaPlan* plan) {
   return ZL_OK;
 }
 
+// Tensor maps this thread encoded recently, so a decode loop over the same
+// pools skips the driver call (the map is a plain 128-byte value).
+struct PoolMapKey {
+  const void* pool;
+  int64_t page_stride, token_stride, head_stride;
+  int32_t D, page_size, Hkv, num_pages, box_heads;
+  bool operator==(const PoolMapKey& o) const {
+    return pool == o.pool && page_stride == o.page_stride && token_stride == o.token_stride &&
+           head_stride == o.head_stride && D == o.D && page_size == o.page_size &&
+           Hkv == o.Hkv && num_pages == o.num_pages && box_heads == o.box_heads;
+  }
+};
+constexpr int kMapCache = 8;
+thread_local PoolMapKey t_map_keys[kMapCache];
+thread_local CUtensorMap t_maps[kMapCache];
+thread_local int t_map_used = 0, t_map_next = 0;
+
 zl_status encode_pool_map(CUtensorMap* map, const void* pool, const zl_decode_attn_params* a,
                           int box_heads) {
+  const PoolMapKey key{pool, a->page_stride, a->token_stride, a->head_stride, a->D_qk,
+                       a->page_size, a->Hkv, a->num_pages, box_heads};
+  for (int i = 0; i < t_map_used; ++i)
+    if (t_map_keys[i] == key) {
+      *map = t_maps[i];
+      return ZL_OK;
+    }
   auto encode = tensor_map_encoder();
   if (!encode) return ZL_ERR_CUDA;
   const cuuint64_t dims[4] = {cuuint64_t(a->D_qk), cuuint64_t(a->page_size), cuuint64_t(a->Hkv),
@@ -223,7 +247,12 @@ zl_status encode_pool_map(CUtensorMap* map, const void* pool, const zl_decode_at
                             dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? ZL_OK : ZL_ERR_UNSUPPORTED;
+  if (r != CUDA_SUCCESS) return ZL_ERR_UNSUPPORTED;
+  t_map_keys[t_map_next] = key;
+  t_maps[t_map_next] = *map;
+  t_map_next = (t_map_next + 1) % kMapCache;
+  if (t_map_used < kMapCache) ++t_map_used;
+  return ZL_OK;
 }
 
 zl_status validate_pointers(const zl_decode_attn_params* a, bool need_v) {
