@@ -174,14 +174,33 @@ def time_oracle(w, min_seconds=10.0, max_calls=50):
     q, k = w.bits(w.q), w.bits(w.k_pool)
     v = None if w.mla else w.bits(w.v_pool)
     times = []
+    res = None
     t_start = time.perf_counter()
     while len(times) < max_calls and (time.perf_counter() - t_start) < min_seconds:
         t0 = time.perf_counter()
-        orc.decode_attn(q, k, v, w.strides, w.block_table, w.seq_lens, Hkv=w.Hkv,
-                        page_size=w.page_size, num_pages=w.num_pages, scale=w.scale, D_v=w.D_v,
-                        num_threads=threads)
+        res = orc.decode_attn(q, k, v, w.strides, w.block_table, w.seq_lens, Hkv=w.Hkv,
+                              page_size=w.page_size, num_pages=w.num_pages, scale=w.scale,
+                              D_v=w.D_v, num_threads=threads)
         times.append(time.perf_counter() - t0)
-    return statistics.median(times), len(times), threads
+    return statistics.median(times), len(times), threads, res
+
+
+def parity_summary(out_gpu, lse_gpu, res):
+    """Element-wise errors of the measured call's output against the oracle's."""
+    ref, ref_lse, status = res
+    got = out_gpu.float().cpu().numpy().astype(np.float64)
+    diff = np.abs(got - ref)
+    big = np.abs(ref) >= 1e-2
+    ratio = diff / (1e-2 + 1e-2 * np.abs(ref))
+    lse = lse_gpu.cpu().numpy().astype(np.float64)
+    fin = np.isfinite(ref_lse)
+    return {"max_abs_err": float(diff.max()),
+            "max_rel_err": float((diff[big] / np.abs(ref[big])).max()) if big.any() else 0.0,
+            "worst_err_over_tolerance": float(ratio.max()),
+            "lse_max_abs_err": float(np.abs(lse[fin] - ref_lse[fin]).max()) if fin.any() else 0.0,
+            "within_tolerance": bool((ratio <= 1.0).all()), "oracle_status": int(status),
+            "tolerance": "|gpu - oracle| <= 1e-2 + 1e-2 |oracle| per element (bf16 out, fp64 "
+                         "oracle), the whole output of the last timed call"}
 
 
 def run_reference(args, world, rank, budget_s=120.0):
@@ -444,10 +463,13 @@ def run_ours(args, world, rank, local):
     algo = kvb + io_bytes(w)
     achieved = algo / (attn_ms * 1e-3) / 1e9
     cpu = None
+    parity = None
     if not args.no_cpu_baseline:
-        cpu_s, cpu_calls, cores = time_oracle(w)
+        cpu_s, cpu_calls, cores, res = time_oracle(w)
         cpu = {"value": kvb / cpu_s / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"the whole workload per call, {cpu_calls} calls (median)"}
+        if ap is None:  # (with the append the device pools hold the new rows)
+            parity = parity_summary(out, lse, res)
     line = {
         "metric": metric_name(args.workload, args.q_len),
         "value": kvb * world / (ms * 1e-3) / 1e9,
@@ -475,6 +497,7 @@ def run_ours(args, world, rank, local):
                      "algorithmic_bytes_per_launch": algo,
                      "traffic": traffic_per_launch(w.name, kind)},
         "cpu_baseline": cpu,
+        "parity": parity,
         "e2e": e2e,
         "gpu_launches": launches,
         "kv_append": append,
