@@ -7,12 +7,15 @@
 // flash_decoding family named under "技术架构：五层模块化设计" on the
 // "ZhiLight：知乎开源的高性能 LLM 推理加速引擎" page). A CTA whose range covers a
 // whole unit writes the final output; a unit cut between CTAs leaves one
-// normalised partial (o, lse) per CTA in the workspace. Each consumer warp
-// that writes a partial then counts its arrival on the (sequence, kv head)
-// counter; the warp that arrives last combines all the partials of its rows
-// by log-sum-exp, always in CTA order, so the result does not depend on
-// which CTA finished last: one launch, deterministic. The cut depends only on
-// seq_lens and G, so results are bit-identical under page remapping.
+// normalised partial (o, lse) per CTA in the workspace, and the merge kernel
+// that follows (a programmatic dependent launch) combines them by
+// log-sum-exp in CTA order. With FUSED the attention kernel merges instead:
+// each consumer warp that writes a partial counts its arrival on the
+// (sequence, kv head) counter and the last to arrive merges, in the same CTA
+// order, so the result does not depend on which CTA finished last. Either way
+// the cut depends only on seq_lens and G, so results are deterministic and
+// bit-identical under page remapping. MODE kModeShared adds units that cover a
+// shared prefix for a group of sequences at once (see gqa_prefix.cu).
 //
 // Per tile (16 tokens x HPC kv heads), the producer issues four TMA loads (K
 // and V, two 64-column halves each, 128-byte swizzled) into a ring of
