@@ -51,10 +51,16 @@ def measured_peaks():
 
 
 def kernel_hash(kind):
+    """Hash of the kernel sources with // comments and blank space removed, so
+    that editing a comment does not void a traffic figure but any code change
+    does."""
+    import re
     h = hashlib.sha256()
     for path in KERNEL_SRC[kind]:
-        with open(path, "rb") as f:
-            h.update(f.read())
+        with open(path, encoding="utf-8") as f:
+            text = f.read()
+        code = re.sub(r"//[^\n]*", "", text)
+        h.update("".join(code.split()).encode())
     return h.hexdigest()[:16]
 
 
