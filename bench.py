@@ -510,7 +510,7 @@ def run_ours(args, world, rank, local):
         "clocks": clocks,
     }
     if w.mla:
-        flops = 2.0 * int(w.seq_lens.astype(np.int64).sum()) * w.Hq * (w.D_qk + w.D_v)
+        flops = 2.0 * int(w.seq_lens.astype(np.int64).sum()) * w.q_len * w.Hq * (w.D_qk + w.D_v)
         line["tensor"] = {"tflops": flops / (attn_ms * 1e-3) / 1e12, "flops_per_launch": flops}
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -535,7 +535,7 @@ def main():
     ap.add_argument("--single-launch", action="store_true",
                     help="GQA: merge split-KV partials inside the attention kernel")
     ap.add_argument("--q-len", type=int, default=1,
-                    help="query tokens per sequence (llama3_8b_decode only)")
+                    help="query tokens per sequence (llama3_8b_decode, mla_decode)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")

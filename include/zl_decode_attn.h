@@ -176,7 +176,9 @@ zl_status zl_decode_attn(const zl_decode_attn_params* params, zl_stream_t stream
  * columns. The "ZhiLight：知乎开源的高性能 LLM 推理加速引擎" page lists MLA support
  * under "功能生态" and flash_mla under "技术架构：五层模块化设计".
  *   Supported: Hkv = 1, v_pool = NULL, Hq = 128, D_qk = 576, D_v = 512,
- *   page_size a multiple of 64 (<= 1024), q_len = 1, 1 <= B <= 1024.
+ *   page_size a multiple of 64 (<= 1024), q_len >= 1 with B * q_len <= 1024
+ *   (query token i attends causally, as for zl_decode_attn; each (sequence,
+ *   query token) pair is a unit of work of its own).
  *   head_stride is not used. The kernel runs on clusters of two CTAs;
  *   num_ctas (when > 0) is rounded up to an even count.
  */

@@ -183,9 +183,8 @@ zl_status mla_validate_shape(const zl_decode_attn_params* a) {
   if (a->shared_prefix_pages != 0) return ZL_ERR_UNSUPPORTED;
   if (a->D_qk != zl::kMlaDqk || a->D_v != zl::kMlaDv) return ZL_ERR_UNSUPPORTED;
   if (a->Hq != zl::kMlaHeads) return ZL_ERR_UNSUPPORTED;
-  if (a->q_len != 1) return ZL_ERR_UNSUPPORTED;
   if (a->page_size % zl::kMlaTile != 0 || a->page_size > 1024) return ZL_ERR_UNSUPPORTED;
-  if (a->B > zl::kMlaMaxBatch) return ZL_ERR_UNSUPPORTED;
+  if (int64_t(a->B) * a->q_len > zl::kMlaMaxBatch) return ZL_ERR_UNSUPPORTED;
   return ZL_OK;
 }
 
@@ -197,13 +196,15 @@ zl_status mla_plan(const zl_decode_attn_params* a, MlaPlan* plan) {
   int clusters = a->num_ctas > 0 ? (a->num_ctas + 1) / 2 : dev.sms / 2;
   if (a->num_ctas == 0 && a->max_seq_len > 0) {
     const int64_t tiles =
-        int64_t(a->B) * ((int64_t(a->max_seq_len) + zl::kMlaTile - 1) / zl::kMlaTile);
+        int64_t(a->B) * a->q_len *
+        ((int64_t(a->max_seq_len) + zl::kMlaTile - 1) / zl::kMlaTile);
     if (tiles < clusters) clusters = int(tiles < 1 ? 1 : tiles);
   }
   if (clusters < 1) clusters = 1;
   plan->clusters = clusters;
   const size_t rows = size_t(clusters) * 2 * zl::kMlaHeads;
-  plan->off_lse = round_up(size_t(a->B + 1) * sizeof(int32_t), 256);
+  // tile prefix sums per (sequence, query token) | partial lse | partial outputs
+  plan->off_lse = round_up((size_t(a->B) * a->q_len + 1) * sizeof(int32_t), 256);
   plan->off_o = plan->off_lse + round_up(rows * sizeof(float), 256);
   plan->bytes = plan->off_o + rows * zl::kMlaDv * sizeof(float);
   return ZL_OK;
@@ -396,6 +397,7 @@ zl_status zl_decode_attn_mla(const zl_decode_attn_params* a, zl_stream_t stream)
   p.ws_o = reinterpret_cast<float*>(ws + plan.off_o);
   p.err_flags = a->err_flags;
   p.B = a->B;
+  p.q_len = a->q_len;
   p.page_size = a->page_size;
   p.num_pages = a->num_pages;
   p.scale_log2 = float(double(a->scale) * kLog2e);

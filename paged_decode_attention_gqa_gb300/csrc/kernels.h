@@ -49,14 +49,14 @@ constexpr int kMlaTile = 64;       // tokens per MLA tile (page sizes are multip
 constexpr int kMlaDqk = 576;       // latent 512 + rope 64
 constexpr int kMlaDv = 512;        // V = first 512 latent columns
 constexpr int kMlaHeads = 128;     // query heads (= TMEM lanes)
-constexpr int kMlaMaxBatch = 1024; // sequences per MLA call
+constexpr int kMlaMaxBatch = 1024; // (sequence, query token) pairs per MLA call
 
 // Everything the MLA kernel and its merge kernel read.
 struct MlaParams {
   CUtensorMap tmap_kv;  // 3-D {576, page_size, num_pages}, box {64, 64, 1}, 128B swizzle
-  const __nv_bfloat16* q;  // [B, 128, 576]
-  __nv_bfloat16* out;   // [B, 128, 512]
-  float* lse;           // [B, 128] natural log, or nullptr
+  const __nv_bfloat16* q;  // [B, q_len, 128, 576]
+  __nv_bfloat16* out;   // [B, q_len, 128, 512]
+  float* lse;           // [B, q_len, 128] natural log, or nullptr
   const int32_t* block_table;
   const int32_t* seq_lens;
   int64_t bt_stride;
@@ -64,7 +64,7 @@ struct MlaParams {
   float* ws_o;          // [clusters][2][128][512] normalised partial outputs
   float* ws_lse;        // [clusters][2][128] base-2 lse of partials (NaN = bad piece)
   uint32_t* err_flags;
-  int B, page_size, num_pages;
+  int B, q_len, page_size, num_pages;
   float scale_log2;
 };
 

@@ -98,8 +98,18 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
   const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
   const int cid = blockIdx.x >> 1, NC = gridDim.x >> 1;
   const int nbox = rank == 0 ? 5 : 4;
-  const int B = p.B;
+  // The units of work are (sequence b, query token i) pairs, v = b * q_len + i:
+  // q, out and lse rows of v are contiguous, and v attends causally to the
+  // first L_b - q_len + 1 + i tokens of sequence b's pages.
+  const int B = p.B * p.q_len;
   const int64_t cap = p.bt_stride * int64_t(p.page_size);
+  // Visible tokens of unit v (0 for an invalid sequence length).
+  auto vis_len = [&](int v) -> int {
+    const int L = p.seq_lens[v / p.q_len];
+    if (!(L >= 0 && int64_t(L) <= cap)) return 0;
+    const int n = L - p.q_len + 1 + v % p.q_len;
+    return n > 0 ? n : 0;
+  };
 
   if (tid == 0) {
     mbar_init(bar(B_Q_FULL), kRows);  // softmax threads wrote this piece's Q into TMEM
@@ -139,10 +149,10 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     for (int i = 0; i < per; ++i) {
       const int b = b0 + i;
       if (b < B) {
-        const int L = p.seq_lens[b];
+        const int L = p.seq_lens[b / p.q_len];
         const bool ok = L >= 0 && int64_t(L) <= cap;
         if (!ok && blockIdx.x == 0) raise_error(p.err_flags, kErrBadLen);
-        local += ok ? (L + kTile - 1) / kTile : 0;
+        local += (vis_len(b) + kTile - 1) / kTile;
       }
     }
     int incl = local;
@@ -156,8 +166,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       const int b = b0 + i;
       if (b < B) {
         prefix[b] = run;
-        const int L = p.seq_lens[b];
-        run += (L >= 0 && int64_t(L) <= cap) ? (L + kTile - 1) / kTile : 0;
+        run += (vis_len(b) + kTile - 1) / kTile;
       }
     }
     if (lane == 31) prefix[B] = incl;
@@ -194,7 +203,8 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
             break;
           }
           const int tok0 = j * kTile;
-          const int page = p.block_table[int64_t(b) * p.bt_stride + tok0 / p.page_size];
+          const int page =
+              p.block_table[int64_t(b / p.q_len) * p.bt_stride + tok0 / p.page_size];
           if (page < 0 || page >= p.num_pages) {
             mbar_arrive(bar(B_KV_FULL0 + s));  // nothing loaded; the piece is discarded
           } else {
@@ -395,8 +405,8 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       const int ntiles = int(pend - idx);
       const bool partial = (j0 > 0) || (pend < prefix[b + 1]);
       const int slot = (idx == s_c) ? 0 : 1;
-      const int L = p.seq_lens[b];
-      const int32_t* bt_row = p.block_table + int64_t(b) * p.bt_stride;
+      const int L = vis_len(b);
+      const int32_t* bt_row = p.block_table + int64_t(b / p.q_len) * p.bt_stride;
       float m_used = -CUDART_INF_F, l = 0.f;
       int bad = 0;
       int page_cur = bt_row[(j0 * kTile) / p.page_size];
@@ -582,12 +592,12 @@ __global__ void __launch_bounds__(128) mla_merge_kernel(const __grid_constant__ 
   griddep_launch_dependents();  // the next call's kernels may start their prologue
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = int64_t(blockIdx.x) * 4 + warp;
-  if (row >= int64_t(p.B) * kRows) return;
+  if (row >= int64_t(p.B) * p.q_len * kRows) return;
   const int b = int(row / kRows), h = int(row % kRows);
   const int* prefix = p.ws_prefix;
   const int n = prefix[b + 1] - prefix[b];
   if (n == 0) return;
-  const int64_t W = prefix[p.B];
+  const int64_t W = prefix[p.B * p.q_len];
   const int64_t U0 = prefix[b];
   const int c_lo = cluster_of_tile(U0, W, NC), c_hi = cluster_of_tile(U0 + n - 1, W, NC);
   if (c_lo == c_hi) return;
@@ -669,7 +679,7 @@ cudaError_t mla_decode_launch(const MlaParams& p, int clusters, cudaStream_t str
     if ((e = cudaLaunchKernelEx(&cfg, mla_decode_kernel, p)) != cudaSuccess) return e;
   }
   if (attn_end && (e = cudaEventRecord(attn_end, stream)) != cudaSuccess) return e;
-  const int64_t rows = int64_t(p.B) * kRows;
+  const int64_t rows = int64_t(p.B) * p.q_len * kRows;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned((rows + 3) / 4));
   cfg.blockDim = dim3(128);

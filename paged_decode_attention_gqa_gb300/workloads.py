@@ -276,10 +276,11 @@ def long_context_decode(seed=1004, layout="NHD", poison=True, values=True) -> Wo
                           scale=1.0 / math.sqrt(128), layout=layout, poison=poison, values=values)
 
 
-def mla_decode(seed=1005, poison=True, B=64, values=True) -> Workload:
+def mla_decode(seed=1005, poison=True, B=64, values=True, q_len=1) -> Workload:
     """Absorbed MLA (DeepSeek-V3 shape): 64 seqs, 128 query heads over one
     latent KV row of 512 + 64 rope (QK over 576, V = the 512 latent), lengths
-    U[1024, 8192], page 64, random pages, scale 1/sqrt(192)."""
+    U[1024, 8192], page 64, random pages, scale 1/sqrt(192). q_len > 1: that
+    many new query tokens per sequence (multi-token prediction)."""
     rng = _structure_rng(seed)
     lens = rng.integers(1024, 8192, size=B, endpoint=True).astype(np.int32)
     pages = int(((lens + 63) // 64).sum())
@@ -287,7 +288,8 @@ def mla_decode(seed=1005, poison=True, B=64, values=True) -> Workload:
     table = place_pages(rng, lens, 64, num_pages)
     return build_workload("mla_decode", seed, B=B, Hq=128, Hkv=1, D_qk=576, D_v=512,
                           page_size=64, seq_lens=lens, block_table=table, num_pages=num_pages,
-                          scale=1.0 / math.sqrt(192), mla=True, poison=poison, values=values)
+                          scale=1.0 / math.sqrt(192), mla=True, poison=poison, values=values,
+                          q_len=q_len)
 
 
 WORKLOADS = {

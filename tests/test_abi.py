@@ -101,7 +101,7 @@ def _mla_params(**over):
     (dict(page_size=16), zl.ERR_UNSUPPORTED),
     (dict(page_size=48), zl.ERR_UNSUPPORTED),
     (dict(page_size=32), zl.ERR_UNSUPPORTED),
-    (dict(q_len=2), zl.ERR_UNSUPPORTED),
+    (dict(B=600, q_len=2), zl.ERR_UNSUPPORTED),    # 1200 (sequence, token) pairs
     (dict(B=3000), zl.ERR_UNSUPPORTED),
     (dict(flags=zl.SINGLE_LAUNCH), zl.ERR_UNSUPPORTED),
     (dict(flags=zl.TEST_STALL), zl.ERR_UNSUPPORTED),

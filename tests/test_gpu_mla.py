@@ -70,3 +70,45 @@ def test_mla_empty_and_bad_page():
 
 def test_mla_full_workload():
     _parity(wl.mla_decode())
+
+
+@pytest.mark.parametrize("q_len", [2, 3])
+def test_mla_multi_token(q_len):
+    """q_len query tokens per sequence (multi-token prediction): token i sees the
+    first L - q_len + 1 + i tokens; contexts shorter than q_len included."""
+    lens = [1, 2, 3, 64, 65, 130, 700]
+    w = wl.random_case(620 + q_len, B=len(lens), Hq=128, Hkv=1, D=576, D_v=512, mla=True,
+                       page_size=64, lens=lens, q_len=q_len)
+    _parity(w)
+
+
+def test_mla_multi_token_split_and_last_row():
+    """Split across many clusters; the last query token's rows equal a q_len = 1
+    call with that query, bit for bit."""
+    w = wl.random_case(630, B=5, Hq=128, Hkv=1, D=576, D_v=512, mla=True, page_size=64,
+                       max_len=900, q_len=2)
+    g = _parity(w, num_ctas=60)
+    w1 = wl.random_case(630, B=5, Hq=128, Hkv=1, D=576, D_v=512, mla=True, page_size=64,
+                        max_len=900, q_len=1)
+    w1.q = w.q[:, -1:].contiguous()
+    g1 = run_gpu(w1, num_ctas=60)
+    ref1, _, _ = run_oracle(w1)
+    assert_close(g1.out64(), ref1, "q_len 1")
+    assert_close(g.out64()[:, -1:], g1.out64(), "last row vs q_len 1")
+
+
+def test_mla_deepseek_mtp_shape_sampled():
+    """The DeepSeek-V3 shape with 2 query tokens (one extra MTP token): sampled
+    sequences against the oracle at full context lengths."""
+    w = wl.mla_decode(q_len=2)
+    g = run_gpu(w)
+    rng = np.random.default_rng(11)
+    bs = rng.choice(w.B, size=4, replace=False)
+    ws = wl.build_workload("sampled", 0, B=len(bs), Hq=128, Hkv=1, D_qk=576, D_v=512,
+                           page_size=64, seq_lens=w.seq_lens[bs], block_table=w.block_table[bs],
+                           num_pages=w.num_pages, scale=w.scale, q_len=2, mla=True, values=False)
+    ws.q, ws.k_pool, ws.v_pool = w.q[bs].contiguous(), w.k_pool, None
+    ref, ref_lse, st = run_oracle(ws)
+    assert st == 0
+    assert_close(g.out64()[bs], ref, "sampled out")
+    assert_close(g.lse64()[bs], ref_lse, "sampled lse")
