@@ -158,6 +158,16 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+def max_over_ranks(x, world, device):
+    """The largest value of x over all ranks (the job's time is its slowest rank's)."""
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -369,10 +379,7 @@ def run_ours(args, world, rank, local):
         ms = t_begin.elapsed_time(t_end) / args.steps
     else:
         ms = sum(a.elapsed_time(b) for a, b in step_evs) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     # attention + merge: one launch with ZL_DECODE_SINGLE_LAUNCH, else two (MLA and
     # shared-prefix calls: two)
     launches = args.steps * (1 if (kind == "gqa" and args.single_launch) else 2)

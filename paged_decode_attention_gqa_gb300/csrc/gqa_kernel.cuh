@@ -108,12 +108,6 @@ __device__ __forceinline__ unsigned long long cas_acq_rel(unsigned long long* ad
   return old;
 }
 
-__device__ __forceinline__ unsigned long long ld_relaxed(const unsigned long long* addr) {
-  unsigned long long v;
-  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(addr) : "memory");
-  return v;
-}
-
 __device__ __forceinline__ void st_relaxed(unsigned long long* addr, unsigned long long v) {
   asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(addr), "l"(v) : "memory");
 }
