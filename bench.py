@@ -506,7 +506,7 @@ def run_ours(args, world, rank, local):
     achieved = algo / (attn_ms * 1e-3) / 1e9
     cpu = None
     parity = None
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and world == 1:  # the oracle baseline is an N = 1 figure
         cpu_s, cpu_calls, cores, res = time_oracle(w)
         cpu = {"value": kvb / cpu_s / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"the whole workload per call, {cpu_calls} calls (median)"}
