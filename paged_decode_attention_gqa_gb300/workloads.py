@@ -243,13 +243,15 @@ def llama3_8b_decode(seed=1002, layout="NHD", poison=True, B=64, values=True,
                           values=values, q_len=q_len)
 
 
-def llama70b_prefix_decode(seed=1003, layout="NHD", poison=True, sigma=1.0, values=True) -> Workload:
+def llama70b_prefix_decode(seed=1003, layout="NHD", poison=True, sigma=1.0, values=True,
+                           B=128) -> Workload:
     """70B attention shape with prefix sharing: 128 seqs, 64 query / 8 KV heads,
     D 128, page 16; a 2048-token prefix on the same physical pages in every
-    table plus a private lognormal suffix (median 300, sigma 1, cap 6144)."""
+    table plus a private lognormal suffix (median 300, sigma 1, cap 6144). (A
+    smaller B takes the first B suffixes of the same draw; for profiling.)"""
     rng = _structure_rng(seed)
-    B, prefix = 128, 2048
-    z = rng.standard_normal(B)
+    prefix = 2048
+    z = rng.standard_normal(128)[:B]
     suffix = np.clip(np.rint(np.exp(math.log(300.0) + sigma * z)), 1, 6144).astype(np.int64)
     lens = (prefix + suffix).astype(np.int32)
     pfx_pages = prefix // 16
@@ -263,15 +265,16 @@ def llama70b_prefix_decode(seed=1003, layout="NHD", poison=True, sigma=1.0, valu
                           values=values)
 
 
-def long_context_decode(seed=1004, layout="NHD", poison=True, values=True) -> Workload:
+def long_context_decode(seed=1004, layout="NHD", poison=True, values=True, B=8) -> Workload:
     """Long contexts: 8 seqs, 32 query / 8 KV heads, D 128, lengths
-    U[32768, 131072], page 64, random placement, pool 1.25x."""
+    U[32768, 131072], page 64, random placement, pool 1.25x. (A smaller B takes
+    the first B lengths of the same draw; used for profiling captures.)"""
     rng = _structure_rng(seed)
-    lens = rng.integers(32768, 131072, size=8, endpoint=True).astype(np.int32)
+    lens = rng.integers(32768, 131072, size=8, endpoint=True).astype(np.int32)[:B]
     pages = int(((lens + 63) // 64).sum())
     num_pages = _pool_for(pages)
     table = place_pages(rng, lens, 64, num_pages)
-    return build_workload("long_context_decode", seed, B=8, Hq=32, Hkv=8, D_qk=128,
+    return build_workload("long_context_decode", seed, B=B, Hq=32, Hkv=8, D_qk=128,
                           page_size=64, seq_lens=lens, block_table=table, num_pages=num_pages,
                           scale=1.0 / math.sqrt(128), layout=layout, poison=poison, values=values)
 
