@@ -8,20 +8,29 @@
 // QK over the 576 columns and V = the first 512 columns.
 //
 // Shape of the problem on one SM: fp32 O for 128 heads x 512 columns is the
-// whole of TMEM (512 columns x 128 lanes), and Q (128 x 576 bf16) is 147 KB of
-// shared memory. So a cluster of two CTAs shares each tile of 64 tokens:
-//   rank 0 loads latent columns [0,256) and the rope [512,576),
-//   rank 1 loads latent columns [256,512);
-// each rank computes a partial S = Q K^T over its columns into TMEM (M = 128
-// heads, N = 64 tokens, K = 320 or 256), the two fp32 partials are swapped
-// through distributed shared memory and summed (both ranks then hold the same
-// S and make the same softmax decisions), and each rank accumulates its own
-// 256 columns of O = P V in TMEM (N = 256, V read MN-major straight from the
-// tile it loaded). Every K/V byte leaves HBM once.
+// whole of TMEM (512 columns x 128 lanes). So a cluster of two CTAs shares
+// each range of 64-token tiles, and each CTA owns half of O: rank r
+// accumulates O columns [256r, 256r + 256) in TMEM. Both ranks compute the
+// whole score tile S = Q K^T (M = 128 heads, N = 64 tokens, K = 576) and run
+// the same softmax; computing S twice costs less tensor time than trading
+// fp32 partial scores between the CTAs every tile. Both CTAs load every tile
+// at about the same time, so the second load is served by L2.
 //
-// Warp roles (224 threads): warp 0 TMA producer, warp 1 MMA issuer (and TMEM
-// owner), warps 2-5 softmax / epilogue, one thread per head row (TMEM lane),
-// warp 6 releases the exchange buffer to the peer.
+// Where the operands live (per CTA):
+//   TMEM: O (256 columns) | S (64) | P (64 bf16 = 32) | Q of this rank's
+//         latent half and the rope (320 dims = 160 columns);
+//   smem: Q of the other latent half (128 x 256 bf16, 128-byte swizzle) and
+//         two stages of K/V, each split into an "E" part (the other latent
+//         half and the rope: read by QK only) and an "L" part (this rank's
+//         latent half: read by QK and then, as V, by PV).
+// The E part of a stage is released when the QK that reads it is done, the L
+// part when the PV is done, and every tile's QK starts with its E part, so the
+// loads of tile j + 2 have about a whole tile of slack with two stages.
+//
+// Warp roles (224 threads): warp 0 loads the E parts, warp 6 the L parts
+// (TMA), warp 1 issues the MMAs (and owns TMEM), warps 2-5 softmax /
+// epilogue, one thread per head row (TMEM lane). The MMA issuer interleaves
+// PV of tile j - 1 between the two halves of QK of tile j when P is ready.
 // The running max is only moved when it grows by more than 2^8, so O in TMEM
 // is rarely rescaled (P <= 256 meanwhile).
 #include "kernels.h"
@@ -39,36 +48,39 @@ constexpr uint32_t kErrTimeout = 4u;
 
 constexpr int kTile = kMlaTile;               // tokens per tile
 constexpr int kRows = 128;                    // query heads = TMEM lanes
-constexpr int kBoxKV = kTile * 128;           // 4 KB: 32 tokens x 64 bf16
-constexpr int kMaxBoxes = 5;                  // rank 0: 4 latent + 1 rope
-constexpr int kStages = 3;
-constexpr int kStageBytes = kMaxBoxes * kBoxKV;  // 40 KB
-constexpr int kXRow = kTile * 4;                 // 256 B: one row of fp32 partial scores
-constexpr int kXBytes = kRows * kXRow;           // 32 KB
-constexpr int kOffKV = 0;
-constexpr int kOffX = kOffKV + kStages * kStageBytes;  // received partials (single buffer)
-constexpr int kOffStg = kOffX + kXBytes;               // own partials (double buffer)
-constexpr int kOffBar = kOffStg + 2 * kXBytes;
+constexpr int kBox = kTile * 128;             // 8 KB: kTile tokens x 64 bf16
+constexpr int kEBoxes = 5;                    // other latent half (4 boxes) + rope
+constexpr int kLBoxes = 4;                    // this rank's latent half
+constexpr int kStages = 2;
+constexpr int kEBytes = kEBoxes * kBox;       // 40 KB
+constexpr int kLBytes = kLBoxes * kBox;       // 32 KB
+constexpr int kQBox = kRows * 128;            // 16 KB: 128 heads x 64 dims of Q
+constexpr int kOffE = 0;
+constexpr int kOffL = kOffE + kStages * kEBytes;
+constexpr int kOffQ = kOffL + kStages * kLBytes;  // Q of the other latent half
+constexpr int kOffBar = kOffQ + 4 * kQBox;
 enum : int {
   B_Q_FULL = 0,
-  B_KV_FULL0, B_KV_EMPTY0 = B_KV_FULL0 + kStages, B_S_FULL = B_KV_EMPTY0 + kStages,
-  B_S_EMPTY, B_P_FULL, B_PV_DONE, B_X_FULL, B_X_FREE, B_READ_DONE, B_STAGED0,
-  B_FINAL = B_STAGED0 + 2,
+  B_E_FULL0, B_E_EMPTY0 = B_E_FULL0 + kStages,
+  B_L_FULL0 = B_E_EMPTY0 + kStages, B_L_EMPTY0 = B_L_FULL0 + kStages,
+  B_S_FULL = B_L_EMPTY0 + kStages, B_S_EMPTY, B_P_FULL, B_PV_DONE, B_FINAL,
   B_COUNT
 };
 constexpr int kOffMisc = kOffBar + 8 * B_COUNT;
 constexpr int kOffPrefix = kOffMisc + 64;
 constexpr size_t kSmemBytes = 1024 + kOffPrefix + size_t(kMlaMaxBatch + 1) * 4;
 static_assert(kSmemBytes <= 232448, "MLA kernel exceeds 227 KB of shared memory");
-static_assert(kOffKV % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle atoms need aligned buffers");
+static_assert(kOffL % 1024 == 0 && kOffQ % 1024 == 0 && kEBytes % 1024 == 0 &&
+                  kLBytes % 1024 == 0,
+              "swizzle atoms need 1024-byte aligned buffers");
 // TMEM columns (fp32 or bf16 pairs), 128 lanes = 128 heads:
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;                // O, this rank's 256 columns of D_v
 constexpr uint32_t kTmemS = 256;              // S tile: kTile fp32 columns
 constexpr uint32_t kTmemP = kTmemS + kTile;   // P tile: kTile bf16 = kTile / 2 columns
-constexpr uint32_t kTmemQ = kTmemP + kTile / 2;  // Q, this rank's 320 or 256 dims
+constexpr uint32_t kTmemQ = kTmemP + kTile / 2;  // Q: this rank's latent half, then the rope
 static_assert(kTmemQ + 160 <= kTmemCols, "TMEM holds O, S, P and Q");
-constexpr int kThreads = 224;  // producer, MMA, 4 softmax warps, exchange warp
+constexpr int kThreads = 224;  // E producer, MMA, 4 softmax warps, L producer
 
 __device__ __forceinline__ void raise_error(uint32_t* flags, uint32_t bits) {
   if (flags) atomicOr(flags, bits);
@@ -83,6 +95,23 @@ __device__ __forceinline__ int locate(const int* prefix, int B, int64_t idx) {
   return lo;
 }
 
+// Wait on an mbarrier with the whole warp by polling with test_wait (which
+// never suspends the warp, so the MMA issuer sees a completed phase at once);
+// true on every lane only if the phase completed, false on every lane after a
+// timeout or an abort.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity,
+                                          const volatile int* abort_flag) {
+  if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
+    if ((i & 63u) == 0) {
+      const bool stop = *abort_flag || globaltimer_ns() - t0 > kWaitTimeoutNs;
+      if (__any_sync(0xffffffffu, stop)) return false;
+    }
+  }
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 mla_decode_kernel(const __grid_constant__ MlaParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -95,9 +124,8 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
   int* prefix = reinterpret_cast<int*>(smem + kOffPrefix);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
+  const int rank = int(cluster_ctarank()), other = rank ^ 1;
   const int cid = blockIdx.x >> 1, NC = gridDim.x >> 1;
-  const int nbox = rank == 0 ? 5 : 4;
   // The units of work are (sequence b, query token i) pairs, v = b * q_len + i:
   // q, out and lse rows of v are contiguous, and v attends causally to the
   // first L_b - q_len + 1 + i tokens of sequence b's pages.
@@ -112,20 +140,17 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
   };
 
   if (tid == 0) {
-    mbar_init(bar(B_Q_FULL), kRows);  // softmax threads wrote this piece's Q into TMEM
+    mbar_init(bar(B_Q_FULL), kRows);  // softmax threads wrote this piece's Q
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(B_KV_FULL0 + s), 1);
-      mbar_init(bar(B_KV_EMPTY0 + s), 1);
+      mbar_init(bar(B_E_FULL0 + s), 1);
+      mbar_init(bar(B_E_EMPTY0 + s), 1);
+      mbar_init(bar(B_L_FULL0 + s), 1);
+      mbar_init(bar(B_L_EMPTY0 + s), 1);
     }
     mbar_init(bar(B_S_FULL), 1);
     mbar_init(bar(B_S_EMPTY), kRows);
     mbar_init(bar(B_P_FULL), kRows);
     mbar_init(bar(B_PV_DONE), 1);
-    mbar_init(bar(B_X_FULL), 1);      // local expect_tx + the peer's bulk-copy bytes
-    mbar_init(bar(B_X_FREE), 1);      // the peer has read our previous partial
-    mbar_init(bar(B_READ_DONE), kRows);  // all rows of the received partial read
-    for (int i = 0; i < 2; ++i)
-      mbar_init(bar(B_STAGED0 + i), kRows);  // all rows of the outgoing partial written
     mbar_init(bar(B_FINAL), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -138,10 +163,10 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     tmem_alloc(sbase + kOffMisc, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 0 && lane == 0) {
+  if ((warp == 0 || warp == 6) && lane == 0) {
     tma_prefetch_desc(&p.tmap_kv);
   }
-  // Tiles (of 64 tokens) per sequence, exclusive prefix sum.
+  // Tiles (of 64 tokens) per unit, exclusive prefix sum.
   if (warp == 2) {
     const int per = (B + 31) / 32;
     const int b0 = lane * per;
@@ -174,7 +199,6 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  cluster_sync();  // the peer's barriers exist before any remote arrive
   const uint32_t tmem = *tmem_slot;
 
   if (blockIdx.x == 0)
@@ -187,216 +211,238 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
   const int64_t s_c = int64_t(cid) * W / NC;
   const int64_t e_c = int64_t(cid + 1) * W / NC;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int it = 0;
-      bool ok = true;
-      for (int64_t idx = s_c; idx < e_c && ok;) {
-        const int b = locate(prefix, B, idx);
-        const int j0 = int(idx - prefix[b]);
-        const int64_t pend = min(e_c, int64_t(prefix[b + 1]));
-        for (int j = j0; j < j0 + int(pend - idx); ++j, ++it) {
-          const int s = it % kStages;
-          if (!mbar_wait(bar(B_KV_EMPTY0 + s), ((it / kStages) & 1) ^ 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
-          const int tok0 = j * kTile;
-          const int page =
-              p.block_table[int64_t(b / p.q_len) * p.bt_stride + tok0 / p.page_size];
-          if (page < 0 || page >= p.num_pages) {
-            mbar_arrive(bar(B_KV_FULL0 + s));  // nothing loaded; the piece is discarded
-          } else {
-            const int slot = tok0 % p.page_size;
-            mbar_arrive_expect_tx(bar(B_KV_FULL0 + s), nbox * kBoxKV);
-            for (int i = 0; i < nbox; ++i) {
-              const int col = i < 4 ? int(rank) * 256 + 64 * i : 512;
-              tma_load_3d(sbase + kOffKV + s * kStageBytes + i * kBoxKV, &p.tmap_kv,
-                          bar(B_KV_FULL0 + s), col, slot, page);
-            }
-          }
-        }
-        idx = pend;
-      }
-      if (!ok) {
-        raise_error(p.err_flags, kErrTimeout);
-        *abort_flag = 1;
-      }
-      // Leave no copy in flight: wait for the last stages and the last Q.
-      const volatile int never = 0;
-      for (int j = (it > kStages ? it - kStages : 0); j < it; ++j)
-        mbar_wait(bar(B_KV_FULL0 + j % kStages), (j / kStages) & 1, &never);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // An event loop: issue whichever is ready first, QK of the next tile (its
-    // K/V staged and the S tile read out by the softmax warps) or PV of the
-    // oldest tile whose P is written.
-    if (lane == 0) {
-      const uint32_t idesc_qk = umma_idesc_bf16(kRows, kTile, false);
-      const uint32_t idesc_pv = umma_idesc_bf16(kRows, 256, true);
-      const int total = int(e_c - s_c);
-      int qk = 0, pv = 0, qpiece = 0;
-      bool ok = true;
-      uint64_t last_progress = globaltimer_ns();
-      while (pv < total && ok) {
-        bool progressed = false;
-        if (qk < total) {
-          const int64_t idx = s_c + qk;
-          const int b = locate(prefix, B, idx);
-          const bool first = (qk == 0) || (idx == prefix[b]);
-          const bool last = (qk == total - 1) || (idx + 1 == prefix[b + 1]);
-          const int s = qk % kStages;
-          if (mbar_test(bar(B_KV_FULL0 + s), (qk / kStages) & 1) &&
-              mbar_test(bar(B_S_EMPTY), (qk & 1) ^ 1u) &&
-              (!first || mbar_test(bar(B_Q_FULL), qpiece & 1))) {
-            tc_fence_after();
-            const uint32_t kvbase = sbase + kOffKV + s * kStageBytes;
-            // S = Q K^T: A = Q from TMEM (16 dims = 8 columns per step), B = K
-            // K-major with the 128-byte swizzle.
-            for (int i = 0; i < nbox; ++i) {
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t bdesc = umma_smem_desc(kvbase + i * kBoxKV + kk * 32, 0, 1024, 2);
-                umma_bf16_tmem_a(tmem + kTmemS, tmem + kTmemQ + 32 * i + 8 * kk, bdesc, idesc_qk,
-                                 (i | kk) ? 1u : 0u);
-              }
-            }
-            umma_commit(bar(B_S_FULL));
-            if (last) ++qpiece;
-            ++qk;
-            progressed = true;
-          }
-        }
-        if (pv < qk && mbar_test(bar(B_P_FULL), pv & 1)) {
-          const int64_t idx = s_c + pv;
-          const int b = locate(prefix, B, idx);
-          const bool first = (pv == 0) || (idx == prefix[b]);  // overwrite O
-          tc_fence_after();
-          // O[:, rank half] (+)= P V: A = P from TMEM (16 tokens = 8 columns per
-          // step); B = V, MN-major with the 128-byte swizzle (8-token groups 1 KB
-          // apart, the next 64 columns in the next box).
-          const int s = pv % kStages;
-          const uint32_t vbase = sbase + kOffKV + s * kStageBytes;
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            const uint64_t bdesc = umma_smem_desc(vbase + kk * 16 * 128, kBoxKV, 1024, 2);
-            umma_bf16_tmem_a(tmem + kTmemO, tmem + kTmemP + 8 * kk, bdesc, idesc_pv,
-                             (first && kk == 0) ? 0u : 1u);
-          }
-          umma_commit(bar(B_KV_EMPTY0 + s));
-          umma_commit(bar(B_PV_DONE));
-          ++pv;
-          progressed = true;
-        }
-        if (progressed) {
-          last_progress = globaltimer_ns();
-        } else if (*abort_flag || globaltimer_ns() - last_progress > kWaitTimeoutNs) {
+  if ((warp == 0 || warp == 6) && lane == 0) {
+    // ------------------------------------------------------------ producers
+    // Warp 0 streams the E parts (the other latent half and the rope), warp 6
+    // the L parts (this rank's latent half) of the tiles of this cluster.
+    const bool e_part = warp == 0;
+    const int full0 = e_part ? B_E_FULL0 : B_L_FULL0;
+    const int empty0 = e_part ? B_E_EMPTY0 : B_L_EMPTY0;
+    const uint32_t region = sbase + (e_part ? kOffE : kOffL);
+    const int stage_bytes = e_part ? kEBytes : kLBytes;
+    const int nbox = e_part ? kEBoxes : kLBoxes;
+    const int half = e_part ? other : rank;
+    int it = 0;
+    bool ok = true;
+    for (int64_t idx = s_c; idx < e_c && ok;) {
+      const int b = locate(prefix, B, idx);
+      const int j0 = int(idx - prefix[b]);
+      const int64_t pend = min(e_c, int64_t(prefix[b + 1]));
+      for (int j = j0; j < j0 + int(pend - idx); ++j, ++it) {
+        const int s = it % kStages;
+        const int tok0 = j * kTile;
+        // the block-table read is issued before the wait, so its latency is hidden
+        const int page = p.block_table[int64_t(b / p.q_len) * p.bt_stride + tok0 / p.page_size];
+        if (!mbar_wait(bar(empty0 + s), ((it / kStages) & 1) ^ 1u, abort_flag)) {
           ok = false;
-        }
-      }
-      if (!ok) {
-        raise_error(p.err_flags, kErrTimeout);
-        *abort_flag = 1;
-      }
-      // Every MMA done before TMEM is released.
-      umma_commit(bar(B_FINAL));
-      const volatile int never = 0;
-      mbar_wait(bar(B_FINAL), 0, &never);
-    }
-  } else if (warp == 6) {
-    // ------------------------------------------------------------ exchange warp
-    // Once all rows of received tile j are read, tell the peer its next bulk
-    // copy may land (the remote arrive's latency stays off the softmax path).
-    if (lane == 0) {
-      const uint32_t peer_xfree = mapa_shared(bar(B_X_FREE), peer);
-      const int total = int(e_c - s_c);
-      for (int j = 0; j < total; ++j) {
-        if (!mbar_wait(bar(B_READ_DONE), j & 1, abort_flag)) {
-          raise_error(p.err_flags, kErrTimeout);
-          *abort_flag = 1;
           break;
         }
-        mbar_arrive_remote(peer_xfree);
+        if (page < 0 || page >= p.num_pages) {
+          mbar_arrive(bar(full0 + s));  // nothing loaded; the piece is discarded
+        } else {
+          const int slot = tok0 % p.page_size;
+          mbar_arrive_expect_tx(bar(full0 + s), uint32_t(stage_bytes));
+          for (int i = 0; i < nbox; ++i) {
+            const int col = i < 4 ? half * 256 + 64 * i : 512;
+            tma_load_3d(region + s * stage_bytes + i * kBox, &p.tmap_kv, bar(full0 + s), col, slot,
+                        page);
+          }
+        }
+      }
+      idx = pend;
+    }
+    if (!ok) {
+      raise_error(p.err_flags, kErrTimeout);
+      *abort_flag = 1;
+    }
+    // Leave no copy in flight: wait for the last stages to land.
+    const volatile int never = 0;
+    for (int j = (it > kStages ? it - kStages : 0); j < it; ++j)
+      mbar_wait(bar(full0 + j % kStages), (j / kStages) & 1, &never);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    // The whole warp runs this loop (waits and bookkeeping are warp-uniform);
+    // one elected lane issues. Per tile k: QK over the E part (Q from shared
+    // memory for the other latent half, from TMEM for the rope), then PV of
+    // tile k - 1 if its P is already written, then QK over the L part (Q from
+    // TMEM), then PV of tile k - 1 if it was not issued yet.
+    const uint32_t idesc_qk = umma_idesc_bf16(kRows, kTile, false);
+    const uint32_t idesc_pv = umma_idesc_bf16(kRows, 256, true);
+    const uint32_t qs = sbase + kOffQ;
+    const int total = int(e_c - s_c);
+    int qpiece = 0, pv_next = 0;
+    bool ok = true;
+    // The unit of the current tile and the end of its tiles, kept in
+    // registers: shared memory is only read when a new unit starts.
+    int ub = total > 0 ? locate(prefix, B, s_c) : 0;
+    int64_t ub_end = total > 0 ? prefix[ub + 1] : 0;
+    bool cur_first = true;  // tile k starts a unit (its PV overwrites O)
+    // O[:, rank half] (+)= P V: A = P from TMEM (16 tokens = 8 columns per
+    // step); B = V, MN-major with the 128-byte swizzle (8-token groups 1 KB
+    // apart, the next 64 columns in the next box).
+    auto issue_pv = [&](int j, bool first) {
+      const int s = j % kStages;
+      const uint32_t vbase = sbase + kOffL + s * kLBytes;
+      tc_fence_after();
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint64_t bdesc = umma_smem_desc(vbase + kk * 16 * 128, kBox, 1024, 2);
+          umma_bf16_tmem_a(tmem + kTmemO, tmem + kTmemP + 8 * kk, bdesc, idesc_pv,
+                           (first && kk == 0) ? 0u : 1u);
+        }
+        umma_commit(bar(B_L_EMPTY0 + s));
+        umma_commit(bar(B_PV_DONE));
+      }
+      __syncwarp();
+    };
+    for (int k = 0; k < total && ok; ++k) {
+      const int64_t idx = s_c + k;
+      const bool prev_first = cur_first;  // of tile k - 1
+      cur_first = k == 0;
+      if (idx == ub_end) {  // the next unit with tiles
+        do {
+          ++ub;
+          ub_end = prefix[ub + 1];
+        } while (ub_end <= idx);
+        cur_first = true;
+      }
+      const bool first = cur_first;
+      const bool last = (k == total - 1) || (idx + 1 == ub_end);
+      const int s = k % kStages;
+      const uint32_t ph = (k / kStages) & 1;
+      // a new unit needs its Q; S must have been read out; the E part loaded
+      if ((first && !warp_wait(bar(B_Q_FULL), qpiece & 1, abort_flag)) ||
+          !warp_wait(bar(B_S_EMPTY), (k & 1) ^ 1u, abort_flag) ||
+          !warp_wait(bar(B_E_FULL0 + s), ph, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      {
+        const uint32_t ebase = sbase + kOffE + s * kEBytes;
+        if (elect_one()) {
+          // S = Q K^T over the other latent half: A = Q in shared memory, B =
+          // K, both K-major with the 128-byte swizzle (16 dims = 32 bytes per
+          // step).
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t adesc = umma_smem_desc(qs + i * kQBox + kk * 32, 0, 1024, 2);
+              const uint64_t bdesc = umma_smem_desc(ebase + i * kBox + kk * 32, 0, 1024, 2);
+              umma_bf16(tmem + kTmemS, adesc, bdesc, idesc_qk, (i | kk) ? 1u : 0u);
+            }
+          }
+          // ... and over the rope: A = Q in TMEM (16 dims = 8 columns per step)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bdesc = umma_smem_desc(ebase + 4 * kBox + kk * 32, 0, 1024, 2);
+            umma_bf16_tmem_a(tmem + kTmemS, tmem + kTmemQ + 128 + 8 * kk, bdesc, idesc_qk, 1u);
+          }
+          umma_commit(bar(B_E_EMPTY0 + s));
+        }
+        __syncwarp();
+      }
+      if (pv_next < k && __all_sync(0xffffffffu, mbar_test(bar(B_P_FULL), (k - 1) & 1))) {
+        issue_pv(k - 1, prev_first);
+        ++pv_next;
+      }
+      if (!warp_wait(bar(B_L_FULL0 + s), ph, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      {
+        const uint32_t lbase = sbase + kOffL + s * kLBytes;
+        if (elect_one()) {
+          // S += Q K^T over this rank's latent half, A = Q from TMEM.
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t bdesc = umma_smem_desc(lbase + i * kBox + kk * 32, 0, 1024, 2);
+              umma_bf16_tmem_a(tmem + kTmemS, tmem + kTmemQ + 32 * i + 8 * kk, bdesc, idesc_qk,
+                               1u);
+            }
+          }
+          umma_commit(bar(B_S_FULL));
+        }
+        __syncwarp();
+      }
+      if (last) ++qpiece;
+      if (pv_next < k) {
+        if (!warp_wait(bar(B_P_FULL), (k - 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        issue_pv(k - 1, prev_first);
+        ++pv_next;
       }
     }
-  } else {
+    if (ok && pv_next < total) {
+      if (warp_wait(bar(B_P_FULL), (total - 1) & 1, abort_flag))
+        issue_pv(total - 1, cur_first);
+      else
+        ok = false;
+    }
+    if (!ok && lane == 0) {
+      raise_error(p.err_flags, kErrTimeout);
+      *abort_flag = 1;
+    }
+    // Every MMA done before TMEM is released.
+    if (elect_one()) umma_commit(bar(B_FINAL));
+    __syncwarp();
+    const volatile int never = 0;
+    mbar_wait(bar(B_FINAL), 0, &never);
+  } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------ softmax / epilogue
     const int q4 = warp & 3;
     const int row = 32 * q4 + lane;                 // query head = TMEM lane
     const uint32_t tl = tmem + (uint32_t(32 * q4) << 16);
     const float c = p.scale_log2;
-    const uint32_t peer_x = mapa_shared(sbase + kOffX, peer);
-    const uint32_t peer_xfull = mapa_shared(bar(B_X_FULL), peer);
     const int stid = tid - 64;                       // 0..127 within the softmax group
     const int total = int(e_c - s_c);                // tiles of this cluster
-    // 16-byte chunk k of this row in an exchange buffer (swizzled by row).
-    auto xaddr = [&](uint32_t buf, int k) -> uint32_t {
-      return buf + uint32_t(row * kXRow) + ((uint32_t(k) ^ uint32_t(row & 7)) << 4);
-    };
+    const uint32_t qs = sbase + kOffQ;
 
-    // send(j): this rank's partial scores of tile j. The rows go to the local
-    // staging buffer j & 1 (they are re-read from there when tile j is summed);
-    // once all 128 are there, one thread bulk-copies the buffer into the peer's
-    // receive buffer j & 1, crediting the bytes to the peer's X_FULL barrier.
-    // No flow-control barrier is needed: the peer sends tile j + 2 into our
-    // buffer only after receiving our tile j + 1, which we send after summing
-    // tile j; and staging buffer j & 1 is rewritten only after the peer's tile
-    // j + 1 reached us, which the peer sent after receiving our tile j.
-    auto send = [&](int j) -> bool {
-      const int xb = j & 1;
-      if (!mbar_wait(bar(B_S_FULL), j & 1, abort_flag)) return false;
-      tc_fence_after();
-      const uint32_t stg = sbase + kOffStg + xb * kXBytes;
-#pragma unroll 1
-      for (int h = 0; h < kTile / 32; ++h) {
-        uint32_t v[32];
-        tmem_ld32(tl + kTmemS + 32 * h, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(xaddr(stg, 8 * h + k)),
-                       "r"(v[4 * k]), "r"(v[4 * k + 1]), "r"(v[4 * k + 2]), "r"(v[4 * k + 3])
-                       : "memory");
-      }
-      tc_fence_before();
-      mbar_arrive(bar(B_S_EMPTY));                   // QK of the next tile may start
-      fence_proxy_async_smem();
-      mbar_arrive(bar(B_STAGED0 + xb));
-      if (stid == 0) {
-        if (!mbar_wait(bar(B_STAGED0 + xb), (j >> 1) & 1, abort_flag)) return false;
-        // the peer's single receive buffer must have been read (tile j - 1)
-        if (j >= 1 && !mbar_wait_cluster(bar(B_X_FREE), (j - 1) & 1, abort_flag)) return false;
-        bulk_copy_to_peer(peer_x, stg, kXBytes, peer_xfull);
-      }
-      return true;
-    };
-
-    // Q of sequence b (this rank's columns, 2 bf16 per 32-bit column) into
-    // TMEM, one head row per thread; the MMA issuer waits on Q_FULL.
-    auto load_q = [&](int b) {
-      const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (int64_t(b) * kRows + row) * kMlaDqk);
-      for (int i = 0; i < nbox; ++i) {
-        const int col = i < 4 ? int(rank) * 256 + 64 * i : 512;
-        uint32_t v[32];
+    // Q of unit v, one head row per thread: this rank's latent half and the
+    // rope into TMEM (2 bf16 per 32-bit column), the other latent half into
+    // shared memory in the 128-byte swizzled K-major layout. The MMA issuer
+    // waits on Q_FULL.
+    auto load_q = [&](int v) {
+      const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (int64_t(v) * kRows + row) * kMlaDqk);
+      for (int i = 0; i < 5; ++i) {
+        const int col = i < 4 ? rank * 256 + 64 * i : 512;
+        uint32_t r[32];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint4 u = __ldg(qrow + col / 8 + k);
-          v[4 * k] = u.x;
-          v[4 * k + 1] = u.y;
-          v[4 * k + 2] = u.z;
-          v[4 * k + 3] = u.w;
+          r[4 * k] = u.x;
+          r[4 * k + 1] = u.y;
+          r[4 * k + 2] = u.z;
+          r[4 * k + 3] = u.w;
         }
-        tmem_st32(tl + kTmemQ + 32 * i, v);
+        tmem_st32(tl + kTmemQ + 32 * i, r);
       }
+      for (int i = 0; i < 4; ++i) {
+        const int col = other * 256 + 64 * i;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint4 u = __ldg(qrow + col / 8 + k);
+          const uint32_t dst = qs + uint32_t(i * kQBox + row * 128) + ((uint32_t(k) ^ uint32_t(row & 7)) << 4);
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(u.x), "r"(u.y),
+                       "r"(u.z), "r"(u.w)
+                       : "memory");
+        }
+      }
+      fence_proxy_async_smem();
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(B_Q_FULL));
     };
 
     if (total > 0) load_q(locate(prefix, B, s_c));
-    bool ok = total == 0 || send(0);
+    bool ok = true;
     int it = 0;
     for (int64_t idx = s_c; idx < e_c && ok;) {
       const int b = locate(prefix, B, idx);
@@ -411,41 +457,41 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       int bad = 0;
       int page_cur = bt_row[(j0 * kTile) / p.page_size];
       for (int t = 0; t < ntiles; ++t, ++it) {
-        const int xb = it & 1;
         const int tok0 = (j0 + t) * kTile;
         const int valid = min(kTile, L - tok0);
         // block-table entry of the next tile, loaded one tile ahead
         const int page_nxt = (t + 1 < ntiles) ? bt_row[(tok0 + kTile) / p.page_size] : 0;
         bad |= (page_cur < 0 || page_cur >= p.num_pages) ? 1 : 0;
 
-        // receive the peer's partial of this tile; S = own + peer
-        if (stid == 0) mbar_arrive_expect_tx(bar(B_X_FULL), kXBytes);
-        if (!mbar_wait_cluster(bar(B_X_FULL), it & 1, abort_flag)) { ok = false; break; }
+        // S of this tile: TMEM -> registers, then hand the columns back
+        if (!mbar_wait(bar(B_S_FULL), it & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
         float x[kTile];
         {
-          const uint32_t own = sbase + kOffStg + xb * kXBytes;
-          const uint32_t got = sbase + kOffX;
+          uint32_t s0[32], s1[32];
+          tmem_ld32(tl + kTmemS, s0);
+          tmem_ld32(tl + kTmemS + 32, s1);
+          tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < kTile / 4; ++k) {
-            float a0, a1, a2, a3, b0, b1, b2, b3;
-            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3) : "r"(xaddr(own, k)) : "memory");
-            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(b0), "=f"(b1), "=f"(b2), "=f"(b3) : "r"(xaddr(got, k)) : "memory");
-            x[4 * k] = a0 + b0;
-            x[4 * k + 1] = a1 + b1;
-            x[4 * k + 2] = a2 + b2;
-            x[4 * k + 3] = a3 + b3;
+          for (int k = 0; k < 32; ++k) {
+            x[k] = __uint_as_float(s0[k]);
+            x[32 + k] = __uint_as_float(s1[k]);
           }
         }
-        mbar_arrive(bar(B_READ_DONE));  // the exchange warp releases the buffer to the peer
+        tc_fence_before();
+        mbar_arrive(bar(B_S_EMPTY));  // QK of the next tile may start
+        // Every QK of this unit's piece is done: the next piece's Q may go in.
+        if (it + 1 < total && t + 1 == ntiles) load_q(locate(prefix, B, s_c + it + 1));
+
         // online softmax (base 2); the max moves only when it grows by > 8
-        float mx = -CUDART_INF_F;
+        // (four partial maxima and sums keep the dependency chains short)
+        float mq[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
         for (int k = 0; k < kTile; ++k) {
           x[k] = (k < valid) ? x[k] * c : -CUDART_INF_F;
-          mx = fmaxf(mx, x[k]);
+          mq[k & 3] = fmaxf(mq[k & 3], x[k]);
         }
+        const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
         float alpha = 1.f;
         bool rescale = false;
         if (t == 0) {
@@ -456,26 +502,27 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
           rescale = true;
         }
         uint32_t pk[kTile / 2];
-        float lsum = 0.f;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int k = 0; k < kTile / 2; ++k) {
           pk[k] = pack_bf16x2(ex2_approx(x[2 * k] - m_used), ex2_approx(x[2 * k + 1] - m_used));
           const float2 f = unpack_bf16x2(pk[k]);
-          lsum += f.x + f.y;
+          ls[k & 3] += f.x + f.y;
         }
-        l = l * alpha + lsum;
+        l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
 
         // tail tile: zero the V rows past the end (NaN there would poison 0 * V)
         if (valid < kTile) {
-          const uint32_t vb = sbase + kOffKV + (it % kStages) * kStageBytes;
-          const int nz = (kTile - valid) * 4 * 8;  // 16-byte chunks in 4 latent boxes
+          const uint32_t vb = sbase + kOffL + (it % kStages) * kLBytes;
+          const int nz = (kTile - valid) * kLBoxes * 8;  // 16-byte chunks in the V boxes
           for (int z = stid; z < nz; z += kRows) {
             const int chunk = z & 7, box = (z >> 3) & 3, r = valid + (z >> 5);
             asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(
-                             vb + box * kBoxKV + r * 128 + chunk * 16),
+                             vb + box * kBox + r * 128 + chunk * 16),
                          "r"(0u)
                          : "memory");
           }
+          fence_proxy_async_smem();  // the PV MMA reads these rows
         }
 
         // The P tile in TMEM is free (and O stable for a rescale) once PV(it - 1)
@@ -499,11 +546,6 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(B_P_FULL));
-
-        // send the next tile's partial; a new sequence first needs its Q in TMEM
-        // (every QK of this one is done: this tile's S was read out)
-        if (it + 1 < total && t + 1 == ntiles) load_q(locate(prefix, B, s_c + it + 1));
-        if (it + 1 < total && !send(it + 1)) { ok = false; break; }
         page_cur = page_nxt;
       }
       if (!ok) break;
@@ -568,7 +610,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     }
   }
 
-  // ---- teardown: all roles done; release TMEM, then leave the cluster together
+  // ---- teardown: all roles done; release TMEM
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -576,7 +618,6 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     __syncwarp();
     tmem_dealloc(tmem, kTmemCols);
   }
-  cluster_sync();
 }
 
 __device__ __forceinline__ int cluster_of_tile(int64_t x, int64_t W, int NC) {

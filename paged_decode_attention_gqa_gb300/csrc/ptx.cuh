@@ -374,3 +374,18 @@ __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tme
 }
 
 }  // namespace zl
+
+namespace zl {
+
+// One lane of the (converged) warp returns true. MMA issue loops run on the
+// whole warp and let the elected lane issue, which keeps their descriptors in
+// warp-uniform registers.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+}  // namespace zl
