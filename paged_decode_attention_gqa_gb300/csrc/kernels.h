@@ -50,6 +50,7 @@ constexpr int kMlaDqk = 576;       // latent 512 + rope 64
 constexpr int kMlaDv = 512;        // V = first 512 latent columns
 constexpr int kMlaHeads = 128;     // query heads (= TMEM lanes)
 constexpr int kMlaMaxBatch = 1024; // (sequence, query token) pairs per MLA call
+constexpr int kMlaUnitCost = 4;     // extra cost of a unit (Q load, epilogue) in tiles, for the split
 
 // Everything the MLA kernel and its merge kernel read.
 struct MlaParams {
@@ -61,11 +62,13 @@ struct MlaParams {
   const int32_t* seq_lens;
   int64_t bt_stride;
   int32_t* ws_prefix;   // [B + 1] tile prefix sums
+  int32_t* ws_split;    // [clusters + 1] first tile of each cluster's range
   float* ws_o;          // [clusters][2][128][512] normalised partial outputs
   float* ws_lse;        // [clusters][2][128] base-2 lse of partials (NaN = bad piece)
   uint32_t* err_flags;
   int B, q_len, page_size, num_pages;
   float scale_log2;
+  int out_align32;      // out is 32-byte aligned: 32-byte stores
 };
 
 size_t mla_smem_bytes();

@@ -64,11 +64,13 @@ enum : int {
   B_E_FULL0, B_E_EMPTY0 = B_E_FULL0 + kStages,
   B_L_FULL0 = B_E_EMPTY0 + kStages, B_L_EMPTY0 = B_L_FULL0 + kStages,
   B_S_FULL = B_L_EMPTY0 + kStages, B_S_EMPTY, B_P_FULL, B_PV_DONE, B_FINAL,
+  B_Q_STAGED, B_Q_USED,  // the softmax threads' own syncs around the Q staging buffer
   B_COUNT
 };
 constexpr int kOffMisc = kOffBar + 8 * B_COUNT;
-constexpr int kOffPrefix = kOffMisc + 64;
-constexpr size_t kSmemBytes = 1024 + kOffPrefix + size_t(kMlaMaxBatch + 1) * 4;
+constexpr int kOffPrefix = kOffMisc + 64;                            // tile prefix sums
+constexpr int kOffCost = kOffPrefix + (kMlaMaxBatch + 1) * 4 + 12;  // cost prefix sums
+constexpr size_t kSmemBytes = 1024 + kOffCost + size_t(kMlaMaxBatch + 1) * 4;
 static_assert(kSmemBytes <= 232448, "MLA kernel exceeds 227 KB of shared memory");
 static_assert(kOffL % 1024 == 0 && kOffQ % 1024 == 0 && kEBytes % 1024 == 0 &&
                   kLBytes % 1024 == 0,
@@ -122,6 +124,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 8);
   int* prefix = reinterpret_cast<int*>(smem + kOffPrefix);
+  int* cost = reinterpret_cast<int*>(smem + kOffCost);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rank = int(cluster_ctarank()), other = rank ^ 1;
@@ -152,6 +155,8 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     mbar_init(bar(B_P_FULL), kRows);
     mbar_init(bar(B_PV_DONE), 1);
     mbar_init(bar(B_FINAL), 1);
+    mbar_init(bar(B_Q_STAGED), kRows);
+    mbar_init(bar(B_Q_USED), kRows);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -166,50 +171,77 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
   if ((warp == 0 || warp == 6) && lane == 0) {
     tma_prefetch_desc(&p.tmap_kv);
   }
-  // Tiles (of 64 tokens) per unit, exclusive prefix sum.
+  // Tiles (of 64 tokens) per unit, exclusive prefix sum; and the same for the
+  // cost of a unit: its tiles plus kMlaUnitCost when it has any (its Q load
+  // and epilogue), which the clusters share equally.
   if (warp == 2) {
     const int per = (B + 31) / 32;
     const int b0 = lane * per;
-    int local = 0;
+    int local = 0, local_cost = 0;
     for (int i = 0; i < per; ++i) {
       const int b = b0 + i;
       if (b < B) {
         const int L = p.seq_lens[b / p.q_len];
         const bool ok = L >= 0 && int64_t(L) <= cap;
         if (!ok && blockIdx.x == 0) raise_error(p.err_flags, kErrBadLen);
-        local += (vis_len(b) + kTile - 1) / kTile;
+        const int n = (vis_len(b) + kTile - 1) / kTile;
+        local += n;
+        local_cost += n > 0 ? n + kMlaUnitCost : 0;
       }
     }
-    int incl = local;
+    int incl = local, incl_cost = local_cost;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const int v = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += v;
+      const int vc = __shfl_up_sync(0xffffffffu, incl_cost, off);
+      if (lane >= off) {
+        incl += v;
+        incl_cost += vc;
+      }
     }
-    int run = incl - local;
+    int run = incl - local, run_cost = incl_cost - local_cost;
     for (int i = 0; i < per; ++i) {
       const int b = b0 + i;
       if (b < B) {
         prefix[b] = run;
-        run += (vis_len(b) + kTile - 1) / kTile;
+        cost[b] = run_cost;
+        const int n = (vis_len(b) + kTile - 1) / kTile;
+        run += n;
+        run_cost += n > 0 ? n + kMlaUnitCost : 0;
       }
     }
-    if (lane == 31) prefix[B] = incl;
+    if (lane == 31) {
+      prefix[B] = incl;
+      cost[B] = incl_cost;
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // This cluster's tiles [s_c, e_c): equal shares of the cost line, mapped
+  // back to tiles (a share that starts inside a unit's fixed cost starts at
+  // the unit's first tile).
+  const int64_t W = prefix[B];
+  auto tile_at = [&](int64_t a) -> int64_t {
+    if (a >= cost[B]) return W;
+    const int u = locate(cost, B, a);
+    const int64_t o = a - cost[u] - kMlaUnitCost;
+    return prefix[u] + (o > 0 ? o : 0);
+  };
+  const int64_t s_c = tile_at(int64_t(cid) * cost[B] / NC);
+  const int64_t e_c = tile_at(int64_t(cid + 1) * cost[B] / NC);
+
   if (blockIdx.x == 0)
     for (int b = tid; b <= B; b += kThreads) p.ws_prefix[b] = prefix[b];
+  if (rank == 0 && tid == 0) {
+    p.ws_split[cid] = int32_t(s_c);
+    if (cid == NC - 1) p.ws_split[NC] = int32_t(e_c);
+  }
   // The merge kernel may be scheduled from here on; it waits for this whole
   // grid to finish before it reads anything.
   griddep_launch_dependents();
-
-  const int64_t W = prefix[B];
-  const int64_t s_c = int64_t(cid) * W / NC;
-  const int64_t e_c = int64_t(cid + 1) * W / NC;
 
   if ((warp == 0 || warp == 6) && lane == 0) {
     // ------------------------------------------------------------ producers
@@ -222,34 +254,50 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     const int stage_bytes = e_part ? kEBytes : kLBytes;
     const int nbox = e_part ? kEBoxes : kLBoxes;
     const int half = e_part ? other : rank;
+    const int total = int(e_c - s_c);
+    // Tile `it` is tile j of unit b; the block-table entry of the next tile
+    // is read one tile ahead, so its latency is hidden behind the stage wait.
+    int b = total > 0 ? locate(prefix, B, s_c) : 0;
+    int j = total > 0 ? int(s_c - prefix[b]) : 0;
+    int64_t ub_end = total > 0 ? prefix[b + 1] : 0;
+    auto page_of = [&](int u, int jt) -> int {
+      return p.block_table[int64_t(u / p.q_len) * p.bt_stride + (jt * kTile) / p.page_size];
+    };
+    int page = total > 0 ? page_of(b, j) : 0;
     int it = 0;
     bool ok = true;
-    for (int64_t idx = s_c; idx < e_c && ok;) {
-      const int b = locate(prefix, B, idx);
-      const int j0 = int(idx - prefix[b]);
-      const int64_t pend = min(e_c, int64_t(prefix[b + 1]));
-      for (int j = j0; j < j0 + int(pend - idx); ++j, ++it) {
-        const int s = it % kStages;
-        const int tok0 = j * kTile;
-        // the block-table read is issued before the wait, so its latency is hidden
-        const int page = p.block_table[int64_t(b / p.q_len) * p.bt_stride + tok0 / p.page_size];
-        if (!mbar_wait(bar(empty0 + s), ((it / kStages) & 1) ^ 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
-        if (page < 0 || page >= p.num_pages) {
-          mbar_arrive(bar(full0 + s));  // nothing loaded; the piece is discarded
-        } else {
-          const int slot = tok0 % p.page_size;
-          mbar_arrive_expect_tx(bar(full0 + s), uint32_t(stage_bytes));
-          for (int i = 0; i < nbox; ++i) {
-            const int col = i < 4 ? half * 256 + 64 * i : 512;
-            tma_load_3d(region + s * stage_bytes + i * kBox, &p.tmap_kv, bar(full0 + s), col, slot,
-                        page);
-          }
+    for (; it < total; ++it) {
+      const int s = it % kStages;
+      const int tok0 = j * kTile;
+      // advance to the next tile (skipping units without tiles) and read its page
+      const int64_t nidx = s_c + it + 1;
+      int nb = b, nj = j + 1;
+      if (nidx == ub_end && it + 1 < total) {
+        do {
+          ++nb;
+        } while (prefix[nb + 1] <= nidx);
+        nj = 0;
+      }
+      const int page_next = it + 1 < total ? page_of(nb, nj) : 0;
+      if (!mbar_wait(bar(empty0 + s), ((it / kStages) & 1) ^ 1u, abort_flag)) {
+        ok = false;
+        break;
+      }
+      if (page < 0 || page >= p.num_pages) {
+        mbar_arrive(bar(full0 + s));  // nothing loaded; the piece is discarded
+      } else {
+        const int slot = tok0 % p.page_size;
+        mbar_arrive_expect_tx(bar(full0 + s), uint32_t(stage_bytes));
+        for (int i = 0; i < nbox; ++i) {
+          const int col = i < 4 ? half * 256 + 64 * i : 512;
+          tma_load_3d(region + s * stage_bytes + i * kBox, &p.tmap_kv, bar(full0 + s), col, slot,
+                      page);
         }
       }
-      idx = pend;
+      if (nb != b) ub_end = prefix[nb + 1];
+      b = nb;
+      j = nj;
+      page = page_next;
     }
     if (!ok) {
       raise_error(p.err_flags, kErrTimeout);
@@ -310,6 +358,16 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       const bool first = cur_first;
       const bool last = (k == total - 1) || (idx + 1 == ub_end);
       const int s = k % kStages;
+      // A new unit: finish the previous one first (its last PV is what the
+      // epilogue waits for; the new unit's Q may still be loading).
+      if (first && pv_next < k) {
+        if (!warp_wait(bar(B_P_FULL), (k - 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        issue_pv(k - 1, prev_first);
+        ++pv_next;
+      }
       const uint32_t ph = (k / kStages) & 1;
       // a new unit needs its Q; S must have been read out; the E part loaded
       if ((first && !warp_wait(bar(B_Q_FULL), qpiece & 1, abort_flag)) ||
@@ -405,44 +463,93 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     const int total = int(e_c - s_c);                // tiles of this cluster
     const uint32_t qs = sbase + kOffQ;
 
-    // Q of unit v, one head row per thread: this rank's latent half and the
-    // rope into TMEM (2 bf16 per 32-bit column), the other latent half into
-    // shared memory in the 128-byte swizzled K-major layout. The MMA issuer
-    // waits on Q_FULL.
-    auto load_q = [&](int v) {
-      const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (int64_t(v) * kRows + row) * kMlaDqk);
-      for (int i = 0; i < 5; ++i) {
-        const int col = i < 4 ? rank * 256 + 64 * i : 512;
-        uint32_t r[32];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint4 u = __ldg(qrow + col / 8 + k);
-          r[4 * k] = u.x;
-          r[4 * k + 1] = u.y;
-          r[4 * k + 2] = u.z;
-          r[4 * k + 3] = u.w;
-        }
-        tmem_st32(tl + kTmemQ + 32 * i, r);
+    // Q of unit v: this rank's latent half and the rope into TMEM (one head
+    // row per TMEM lane, 2 bf16 per 32-bit column), the other latent half
+    // into shared memory in the 128-byte swizzled K-major layout. Global reads
+    // are coalesced (one warp copies one 512-byte row segment per
+    // instruction): the latent half bound for TMEM is first staged in the Q
+    // buffer (row-contiguous, 16-byte chunk c of row r at c ^ (r % 32)), read
+    // back one row per thread and written to TMEM; then the other half is
+    // copied into its final place. Phase 1 (q_stage) may start as soon as
+    // every QK of the previous piece is done; phase 2 (q_finish) publishes Q
+    // to the MMA issuer (Q_FULL).
+    auto q_base = [&](int v) -> const uint4* {
+      return reinterpret_cast<const uint4*>(p.q + int64_t(v) * kRows * kMlaDqk);
+    };
+    // chunk i * 128 + stid of the 128 x 32 grid of 16-byte chunks of a half
+    auto q_stage = [&](int v) {
+      const uint4* qb = q_base(v);
+#pragma unroll 8
+      for (int i = 0; i < 32; ++i) {
+        const int c = i * 128 + stid, r = c >> 5, k = c & 31;
+        cp_async_16(qs + uint32_t(r * 512 + ((k ^ (r & 31)) << 4)), qb + r * (kMlaDqk / 8) + rank * 32 + k);
       }
+    };
+    int qn = 0;  // Q loads so far (phase parity of Q_STAGED and Q_USED)
+    auto q_finish = [&](int v) -> bool {
+      const uint4* qb = q_base(v);
+      cp_async_wait_all();
+      mbar_arrive(bar(B_Q_STAGED));  // every staged row has landed
+      if (!mbar_wait(bar(B_Q_STAGED), qn & 1, abort_flag)) return false;
+#pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int col = other * 256 + 64 * i;
+        uint32_t r32[32];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint4 u = __ldg(qrow + col / 8 + k);
-          const uint32_t dst = qs + uint32_t(i * kQBox + row * 128) + ((uint32_t(k) ^ uint32_t(row & 7)) << 4);
-          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(u.x), "r"(u.y),
-                       "r"(u.z), "r"(u.w)
+          const uint32_t src = qs + uint32_t(row * 512 + (((8 * i + k) ^ (row & 31)) << 4));
+          asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(r32[4 * k]), "=r"(r32[4 * k + 1]), "=r"(r32[4 * k + 2]),
+                         "=r"(r32[4 * k + 3])
+                       : "r"(src)
                        : "memory");
         }
+        tmem_st32(tl + kTmemQ + 32 * i, r32);
       }
+      mbar_arrive(bar(B_Q_USED));  // the staging rows are consumed
+      if (!mbar_wait(bar(B_Q_USED), qn & 1, abort_flag)) return false;
+      ++qn;
+      // the other latent half, straight into the swizzled operand layout
+#pragma unroll 8
+      for (int i = 0; i < 32; ++i) {
+        const int c = i * 128 + stid, r = c >> 5, k = c & 31;  // k: 16-byte chunk of 32
+        cp_async_16(qs + uint32_t((k >> 3) * kQBox + r * 128) + ((uint32_t(k & 7) ^ uint32_t(r & 7)) << 4),
+                    qb + r * (kMlaDqk / 8) + other * 32 + k);
+      }
+      // the rope (128 bytes of this thread's row)
+      {
+        const uint4* qrow = qb + row * (kMlaDqk / 8) + 64;
+        uint32_t r32[32];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint4 u = __ldg(qrow + k);
+          r32[4 * k] = u.x;
+          r32[4 * k + 1] = u.y;
+          r32[4 * k + 2] = u.z;
+          r32[4 * k + 3] = u.w;
+        }
+        tmem_st32(tl + kTmemQ + 128, r32);
+      }
+      cp_async_wait_all();
       fence_proxy_async_smem();
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(B_Q_FULL));
+      return true;
+    };
+    // L2 prefetch of the Q rows of unit v (128 heads x 576 bf16, contiguous).
+    auto q_prefetch = [&](int v) {
+      const char* base = reinterpret_cast<const char*>(p.q + int64_t(v) * kRows * kMlaDqk);
+      constexpr uint32_t kQBytes = uint32_t(kRows) * kMlaDqk * 2;  // 147456
+      for (uint32_t off = 0; off < kQBytes; off += 16384u)
+        prefetch_l2_bulk(base + off, min(16384u, kQBytes - off));
     };
 
-    if (total > 0) load_q(locate(prefix, B, s_c));
     bool ok = true;
+    if (total > 0) {
+      const int v0 = locate(prefix, B, s_c);
+      q_stage(v0);
+      ok = q_finish(v0);
+    }
     int it = 0;
     for (int64_t idx = s_c; idx < e_c && ok;) {
       const int b = locate(prefix, B, idx);
@@ -455,6 +562,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       const int32_t* bt_row = p.block_table + int64_t(b / p.q_len) * p.bt_stride;
       float m_used = -CUDART_INF_F, l = 0.f;
       int bad = 0;
+      if (stid == 0 && pend < e_c) q_prefetch(locate(prefix, B, pend));
       int page_cur = bt_row[(j0 * kTile) / p.page_size];
       for (int t = 0; t < ntiles; ++t, ++it) {
         const int tok0 = (j0 + t) * kTile;
@@ -480,18 +588,24 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         }
         tc_fence_before();
         mbar_arrive(bar(B_S_EMPTY));  // QK of the next tile may start
-        // Every QK of this unit's piece is done: the next piece's Q may go in.
-        if (it + 1 < total && t + 1 == ntiles) load_q(locate(prefix, B, s_c + it + 1));
+        // Every QK of this unit's piece is done: the next piece's Q may go in
+        // (the shared-memory part now, the TMEM part once P is written).
+        const int v_next = (it + 1 < total && t + 1 == ntiles) ? locate(prefix, B, s_c + it + 1) : -1;
+        if (v_next >= 0) q_stage(v_next);
 
-        // online softmax (base 2); the max moves only when it grows by > 8
-        // (four partial maxima and sums keep the dependency chains short)
-        float mq[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+        // online softmax (base 2); the max moves only when it grows by > 8.
+        // The max is taken on the raw scores (c > 0, so max(c x) = c max(x)
+        // exactly) and the scale goes into the exponent's FFMA; four partial
+        // maxima and sums keep the dependency chains short.
+        if (valid < kTile) {  // the same for every row: no divergence
 #pragma unroll
-        for (int k = 0; k < kTile; ++k) {
-          x[k] = (k < valid) ? x[k] * c : -CUDART_INF_F;
-          mq[k & 3] = fmaxf(mq[k & 3], x[k]);
+          for (int k = 0; k < kTile; ++k)
+            if (k >= valid) x[k] = -CUDART_INF_F;
         }
-        const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+        float mq[4] = {x[0], x[1], x[2], x[3]};
+#pragma unroll
+        for (int k = 4; k < kTile; ++k) mq[k & 3] = fmaxf(mq[k & 3], x[k]);
+        const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * c;
         float alpha = 1.f;
         bool rescale = false;
         if (t == 0) {
@@ -505,7 +619,8 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int k = 0; k < kTile / 2; ++k) {
-          pk[k] = pack_bf16x2(ex2_approx(x[2 * k] - m_used), ex2_approx(x[2 * k + 1] - m_used));
+          pk[k] = pack_bf16x2(ex2_approx(fmaf(x[2 * k], c, -m_used)),
+                              ex2_approx(fmaf(x[2 * k + 1], c, -m_used)));
           const float2 f = unpack_bf16x2(pk[k]);
           ls[k & 3] += f.x + f.y;
         }
@@ -546,6 +661,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(B_P_FULL));
+        if (v_next >= 0 && !q_finish(v_next)) { ok = false; break; }
         page_cur = page_nxt;
       }
       if (!ok) break;
@@ -559,31 +675,43 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       if (bad && stid == 0) raise_error(p.err_flags, kErrBadPage);
       const float inv = bad ? 0.f : 1.f / l;
       const float lse2 = bad ? -CUDART_INF_F : m_used + log2f(l);
+      // O / l, two 32-column chunks per TMEM wait, 32-byte stores
 #pragma unroll 1
-      for (int cc = 0; cc < 8; ++cc) {
-        uint32_t o[32];
-        tmem_ld32(tl + kTmemO + 32 * cc, o);
+      for (int cc = 0; cc < 8; cc += 2) {
+        uint32_t o[2][32];
+        tmem_ld32(tl + kTmemO + 32 * cc, o[0]);
+        tmem_ld32(tl + kTmemO + 32 * (cc + 1), o[1]);
         tmem_wait_ld();
-        const int col = int(rank) * 256 + 32 * cc;
-        if (!partial) {
-          uint4* dst = reinterpret_cast<uint4*>(p.out + (int64_t(b) * kRows + row) * kMlaDv + col);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            uint4 v;
-            v.x = bad ? 0u : pack_bf16x2(__uint_as_float(o[8 * k]) * inv, __uint_as_float(o[8 * k + 1]) * inv);
-            v.y = bad ? 0u : pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv);
-            v.z = bad ? 0u : pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv);
-            v.w = bad ? 0u : pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv);
-            dst[k] = v;
+        for (int h = 0; h < 2; ++h) {
+          const int col = rank * 256 + 32 * (cc + h);
+          float f[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) f[k] = bad ? 0.f : __uint_as_float(o[h][k]) * inv;
+          if (!partial) {
+            __nv_bfloat16* dst = p.out + (int64_t(b) * kRows + row) * kMlaDv + col;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              uint32_t w[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(f[16 * k + 2 * e], f[16 * k + 2 * e + 1]);
+              if (p.out_align32) {
+                st_global_v8(dst + 16 * k, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+              } else {
+                uint4* d4 = reinterpret_cast<uint4*>(dst + 16 * k);
+                d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+              }
+            }
+          } else {
+            float* dst = p.ws_o + ((int64_t(cid) * 2 + slot) * kRows + row) * kMlaDv + col;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              st_global_v8(dst + 8 * k, __float_as_uint(f[8 * k]), __float_as_uint(f[8 * k + 1]),
+                           __float_as_uint(f[8 * k + 2]), __float_as_uint(f[8 * k + 3]),
+                           __float_as_uint(f[8 * k + 4]), __float_as_uint(f[8 * k + 5]),
+                           __float_as_uint(f[8 * k + 6]), __float_as_uint(f[8 * k + 7]));
           }
-        } else {
-          float4* dst = reinterpret_cast<float4*>(
-              p.ws_o + ((int64_t(cid) * 2 + slot) * kRows + row) * kMlaDv + col);
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            dst[k] = bad ? make_float4(0.f, 0.f, 0.f, 0.f)
-                         : make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
-                                       __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
         }
       }
       if (rank == 0) {
@@ -620,10 +748,6 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
   }
 }
 
-__device__ __forceinline__ int cluster_of_tile(int64_t x, int64_t W, int NC) {
-  return int(((x + 1) * NC + W - 1) / W) - 1;
-}
-
 // One warp per (sequence, head): log-sum-exp merge of the partials of a
 // sequence cut between clusters, in cluster order. A programmatic dependent
 // launch of the attention kernel: it waits here until that grid is done.
@@ -638,14 +762,14 @@ __global__ void __launch_bounds__(128) mla_merge_kernel(const __grid_constant__ 
   const int* prefix = p.ws_prefix;
   const int n = prefix[b + 1] - prefix[b];
   if (n == 0) return;
-  const int64_t W = prefix[p.B * p.q_len];
+  const int* split = p.ws_split;  // first tile of each cluster's range, [NC + 1]
   const int64_t U0 = prefix[b];
-  const int c_lo = cluster_of_tile(U0, W, NC), c_hi = cluster_of_tile(U0 + n - 1, W, NC);
+  const int c_lo = locate(split, NC, U0), c_hi = locate(split, NC, U0 + n - 1);
   if (c_lo == c_hi) return;
   float M = -CUDART_INF_F;
   bool bad = false;
   for (int c = c_lo; c <= c_hi; ++c) {
-    const int64_t s_c = int64_t(c) * W / NC, e_c = int64_t(c + 1) * W / NC;
+    const int64_t s_c = split[c], e_c = split[c + 1];
     if (s_c == e_c) continue;
     const int slot = (c == c_lo && U0 > s_c) ? 1 : 0;
     const float l = p.ws_lse[(int64_t(c) * 2 + slot) * kRows + h];
@@ -656,7 +780,7 @@ __global__ void __launch_bounds__(128) mla_merge_kernel(const __grid_constant__ 
   float den = 0.f;
   if (!bad) {
     for (int c = c_lo; c <= c_hi; ++c) {
-      const int64_t s_c = int64_t(c) * W / NC, e_c = int64_t(c + 1) * W / NC;
+      const int64_t s_c = split[c], e_c = split[c + 1];
       if (s_c == e_c) continue;
       const int slot = (c == c_lo && U0 > s_c) ? 1 : 0;
       const int64_t wrow = (int64_t(c) * 2 + slot) * kRows + h;

@@ -72,6 +72,23 @@ def test_mla_full_workload():
     _parity(wl.mla_decode())
 
 
+def test_mla_output_16_byte_aligned():
+    """An output that is 16- but not 32-byte aligned takes 16-byte stores."""
+    w = _mla_case(612, [300, 64, 1000])
+    d = device_inputs(w)
+    n = w.B * w.q_len * w.Hq * w.D_v
+    buf = torch.empty(n + 8, dtype=torch.bfloat16, device="cuda")
+    out = buf[8:].view(w.B, w.q_len, w.Hq, w.D_v)
+    assert out.data_ptr() % 32 == 16
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    zl.decode_attn_mla(d["q"], d["k"], d["bt"], d["sl"], page_size=w.page_size, scale=w.scale,
+                       D_v=w.D_v, out=out, err_flags=err, max_seq_len=w.max_seq_len)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref, _, _ = run_oracle(w)
+    assert_close(out.float().cpu().numpy(), ref, "mla out at 16-byte alignment")
+
+
 @pytest.mark.parametrize("q_len", [2, 3])
 def test_mla_multi_token(q_len):
     """q_len query tokens per sequence (multi-token prediction): token i sees the
