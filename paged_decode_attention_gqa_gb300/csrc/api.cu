@@ -166,7 +166,7 @@ zl_status gqa_plan(const zl_decode_attn_params* a, GqaPlan* plan) {
 // ------------------------------------------------------------------ MLA plan
 struct MlaPlan {
   int clusters = 0;
-  size_t off_split = 0, off_lse = 0, off_o = 0, bytes = 0;
+  size_t off_split = 0, off_span = 0, off_lse = 0, off_o = 0, bytes = 0;
 };
 
 zl_status mla_validate_shape(const zl_decode_attn_params* a) {
@@ -204,9 +204,11 @@ zl_status mla_plan(const zl_decode_attn_params* a, MlaPlan* plan) {
   plan->clusters = clusters;
   const size_t rows = size_t(clusters) * 2 * zl::kMlaHeads;
   // tile prefix sums per (sequence, query token) | first tile of each cluster |
-  // partial lse | partial outputs
-  plan->off_split = round_up((size_t(a->B) * a->q_len + 1) * sizeof(int32_t), 256);
-  plan->off_lse = plan->off_split + round_up((size_t(clusters) + 1) * sizeof(int32_t), 256);
+  // first and last cluster of each unit | partial lse | partial outputs
+  const size_t units = size_t(a->B) * a->q_len;
+  plan->off_split = round_up((units + 1) * sizeof(int32_t), 256);
+  plan->off_span = plan->off_split + round_up((size_t(clusters) + 1) * sizeof(int32_t), 256);
+  plan->off_lse = plan->off_span + round_up(units * 2 * sizeof(int32_t), 256);
   plan->off_o = plan->off_lse + round_up(rows * sizeof(float), 256);
   plan->bytes = plan->off_o + rows * zl::kMlaDv * sizeof(float);
   return ZL_OK;
@@ -396,6 +398,7 @@ zl_status zl_decode_attn_mla(const zl_decode_attn_params* a, zl_stream_t stream)
   char* ws = static_cast<char*>(a->workspace);
   p.ws_prefix = reinterpret_cast<int32_t*>(ws);
   p.ws_split = reinterpret_cast<int32_t*>(ws + plan.off_split);
+  p.ws_span = reinterpret_cast<int32_t*>(ws + plan.off_span);
   p.ws_lse = reinterpret_cast<float*>(ws + plan.off_lse);
   p.ws_o = reinterpret_cast<float*>(ws + plan.off_o);
   p.err_flags = a->err_flags;

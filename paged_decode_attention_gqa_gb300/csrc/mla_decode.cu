@@ -562,6 +562,11 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       const int32_t* bt_row = p.block_table + int64_t(b / p.q_len) * p.bt_stride;
       float m_used = -CUDART_INF_F, l = 0.f;
       int bad = 0;
+      // the first and the last cluster holding tiles of unit b, for the merge
+      if (rank == 0 && stid == 0) {
+        if (j0 == 0) p.ws_span[2 * b] = cid;
+        if (pend == prefix[b + 1]) p.ws_span[2 * b + 1] = cid;
+      }
       if (stid == 0 && pend < e_c) q_prefetch(locate(prefix, B, pend));
       int page_cur = bt_row[(j0 * kTile) / p.page_size];
       for (int t = 0; t < ntiles; ++t, ++it) {
@@ -764,8 +769,10 @@ __global__ void __launch_bounds__(128) mla_merge_kernel(const __grid_constant__ 
   if (n == 0) return;
   const int* split = p.ws_split;  // first tile of each cluster's range, [NC + 1]
   const int64_t U0 = prefix[b];
-  const int c_lo = locate(split, NC, U0), c_hi = locate(split, NC, U0 + n - 1);
-  if (c_lo == c_hi) return;
+  const int c_lo = p.ws_span[2 * b], c_hi = p.ws_span[2 * b + 1];
+  // (always in range unless the attention kernel gave up early, which it
+  // reports through err_flags; the check keeps every read in bounds)
+  if (c_lo == c_hi || c_lo < 0 || c_hi >= NC || c_lo > c_hi) return;
   float M = -CUDART_INF_F;
   bool bad = false;
   for (int c = c_lo; c <= c_hi; ++c) {
