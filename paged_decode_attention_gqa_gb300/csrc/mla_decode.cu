@@ -564,7 +564,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       int bad = 0;
       // the first and the last cluster holding tiles of unit b, for the merge
       if (rank == 0 && stid == 0) {
-        if (j0 == 0) p.ws_span[2 * b] = cid;
+        if (j0 == 0) p.ws_span[2 * b] = 2 * cid + slot;  // and its partial's slot
         if (pend == prefix[b + 1]) p.ws_span[2 * b + 1] = cid;
       }
       if (stid == 0 && pend < e_c) q_prefetch(locate(prefix, B, pend));
@@ -693,29 +693,23 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
           float f[32];
 #pragma unroll
           for (int k = 0; k < 32; ++k) f[k] = bad ? 0.f : __uint_as_float(o[h][k]) * inv;
-          if (!partial) {
-            __nv_bfloat16* dst = p.out + (int64_t(b) * kRows + row) * kMlaDv + col;
+          // a whole unit goes to out; a piece of one to this cluster's partial slot
+          __nv_bfloat16* dst =
+              partial ? p.ws_o + ((int64_t(cid) * 2 + slot) * kRows + row) * kMlaDv + col
+                      : p.out + (int64_t(b) * kRows + row) * kMlaDv + col;
+          const bool v8 = partial || p.out_align32;
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              uint32_t w[8];
+          for (int k = 0; k < 2; ++k) {
+            uint32_t w[8];
 #pragma unroll
-              for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(f[16 * k + 2 * e], f[16 * k + 2 * e + 1]);
-              if (p.out_align32) {
-                st_global_v8(dst + 16 * k, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
-              } else {
-                uint4* d4 = reinterpret_cast<uint4*>(dst + 16 * k);
-                d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
-              }
+            for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(f[16 * k + 2 * e], f[16 * k + 2 * e + 1]);
+            if (v8) {
+              st_global_v8(dst + 16 * k, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+            } else {
+              uint4* d4 = reinterpret_cast<uint4*>(dst + 16 * k);
+              d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+              d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
             }
-          } else {
-            float* dst = p.ws_o + ((int64_t(cid) * 2 + slot) * kRows + row) * kMlaDv + col;
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              st_global_v8(dst + 8 * k, __float_as_uint(f[8 * k]), __float_as_uint(f[8 * k + 1]),
-                           __float_as_uint(f[8 * k + 2]), __float_as_uint(f[8 * k + 3]),
-                           __float_as_uint(f[8 * k + 4]), __float_as_uint(f[8 * k + 5]),
-                           __float_as_uint(f[8 * k + 6]), __float_as_uint(f[8 * k + 7]));
           }
         }
       }
@@ -753,9 +747,11 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
   }
 }
 
-// One warp per (sequence, head): log-sum-exp merge of the partials of a
-// sequence cut between clusters, in cluster order. A programmatic dependent
-// launch of the attention kernel: it waits here until that grid is done.
+// One warp per (unit, head) row of a unit cut between clusters: log-sum-exp
+// merge of its normalised partials, in cluster order. The loads of a batch of
+// up to four partials (split bounds, lse, rows) are independent, so a warp
+// waits on memory about twice per batch. A programmatic dependent launch of the
+// attention kernel: it waits here until that grid is done.
 __global__ void __launch_bounds__(128) mla_merge_kernel(const __grid_constant__ MlaParams p,
                                                         int NC) {
   griddep_wait();
@@ -764,54 +760,68 @@ __global__ void __launch_bounds__(128) mla_merge_kernel(const __grid_constant__ 
   const int64_t row = int64_t(blockIdx.x) * 4 + warp;
   if (row >= int64_t(p.B) * p.q_len * kRows) return;
   const int b = int(row / kRows), h = int(row % kRows);
-  const int* prefix = p.ws_prefix;
-  const int n = prefix[b + 1] - prefix[b];
-  if (n == 0) return;
-  const int* split = p.ws_split;  // first tile of each cluster's range, [NC + 1]
-  const int64_t U0 = prefix[b];
-  const int c_lo = p.ws_span[2 * b], c_hi = p.ws_span[2 * b + 1];
+  const int u0 = p.ws_prefix[b], u1 = p.ws_prefix[b + 1];
+  const int2 span = reinterpret_cast<const int2*>(p.ws_span)[b];
+  if (u1 == u0) return;  // no tiles: the attention kernel wrote zeros
+  const int c_lo = span.x >> 1, slot_lo = span.x & 1, c_hi = span.y;
   // (always in range unless the attention kernel gave up early, which it
   // reports through err_flags; the check keeps every read in bounds)
-  if (c_lo == c_hi || c_lo < 0 || c_hi >= NC || c_lo > c_hi) return;
-  float M = -CUDART_INF_F;
+  if (span.x < 0 || c_lo == c_hi || c_hi >= NC || c_lo > c_hi) return;
+  constexpr int kBatch = 4;
+  float M = -CUDART_INF_F, den = 0.f, acc[16] = {};
   bool bad = false;
-  for (int c = c_lo; c <= c_hi; ++c) {
-    const int64_t s_c = split[c], e_c = split[c + 1];
-    if (s_c == e_c) continue;
-    const int slot = (c == c_lo && U0 > s_c) ? 1 : 0;
-    const float l = p.ws_lse[(int64_t(c) * 2 + slot) * kRows + h];
-    bad |= isnan(l);
-    M = fmaxf(M, l);
-  }
-  float acc[16] = {};
-  float den = 0.f;
-  if (!bad) {
-    for (int c = c_lo; c <= c_hi; ++c) {
-      const int64_t s_c = split[c], e_c = split[c + 1];
-      if (s_c == e_c) continue;
-      const int slot = (c == c_lo && U0 > s_c) ? 1 : 0;
-      const int64_t wrow = (int64_t(c) * 2 + slot) * kRows + h;
-      const float wgt = exp2f(p.ws_lse[wrow] - M);
-      const float4* src = reinterpret_cast<const float4*>(p.ws_o + wrow * kMlaDv);
+  for (int c0 = c_lo; c0 <= c_hi; c0 += kBatch) {
+    float lse[kBatch];
+    bool live[kBatch];
+    float4 v[kBatch][4];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int c = min(c0 + i, c_hi);
+      const int64_t wrow = (int64_t(c) * 2 + (c == c_lo ? slot_lo : 0)) * kRows + h;
+      // clusters without tiles hold no partial of this unit
+      live[i] = c0 + i <= c_hi && p.ws_split[c] != p.ws_split[c + 1];
+      lse[i] = p.ws_lse[wrow];
+      const uint2* src = reinterpret_cast<const uint2*>(p.ws_o + wrow * kMlaDv);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const float4 v = src[lane + 32 * k];
-        acc[4 * k] += wgt * v.x;
-        acc[4 * k + 1] += wgt * v.y;
-        acc[4 * k + 2] += wgt * v.z;
-        acc[4 * k + 3] += wgt * v.w;
+        const uint2 u = src[lane + 32 * k];
+        const float2 lo = unpack_bf16x2(u.x), hi = unpack_bf16x2(u.y);
+        v[i][k] = make_float4(lo.x, lo.y, hi.x, hi.y);
       }
+    }
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      if (!live[i]) continue;
+      if (isnan(lse[i])) {  // a piece over a bad page: the row is zeroed
+        bad = true;
+        continue;
+      }
+      if (lse[i] > M) {  // online merge: rescale what is accumulated
+        const float r = exp2f(M - lse[i]);
+        den *= r;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) acc[k] *= r;
+        M = lse[i];
+      }
+      const float wgt = exp2f(lse[i] - M);
       den += wgt;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        acc[4 * k] += wgt * v[i][k].x;
+        acc[4 * k + 1] += wgt * v[i][k].y;
+        acc[4 * k + 2] += wgt * v[i][k].z;
+        acc[4 * k + 3] += wgt * v[i][k].w;
+      }
     }
   }
   const float inv = bad ? 0.f : 1.f / den;
   uint2* dst = reinterpret_cast<uint2*>(p.out + row * kMlaDv);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    uint2 v;
-    v.x = pack_bf16x2(acc[4 * k] * inv, acc[4 * k + 1] * inv);
-    v.y = pack_bf16x2(acc[4 * k + 2] * inv, acc[4 * k + 3] * inv);
-    dst[lane + 32 * k] = v;
+    uint2 o;
+    o.x = pack_bf16x2(acc[4 * k] * inv, acc[4 * k + 1] * inv);
+    o.y = pack_bf16x2(acc[4 * k + 2] * inv, acc[4 * k + 3] * inv);
+    dst[lane + 32 * k] = o;
   }
   if (p.lse && lane == 0)
     p.lse[row] = bad ? -CUDART_INF_F : (M + log2f(den)) * 0.69314718055994531f;
