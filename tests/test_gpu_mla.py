@@ -72,6 +72,13 @@ def test_mla_full_workload():
     _parity(wl.mla_decode())
 
 
+def test_mla_max_units():
+    """1024 (sequence, query token) units, the most one call takes: the tile
+    prefix and cost arrays in shared memory are full."""
+    rng = np.random.default_rng(614)
+    _parity(_mla_case(614, rng.integers(1, 100, size=1024, endpoint=True).tolist()))
+
+
 def test_mla_output_16_byte_aligned():
     """An output that is 16- but not 32-byte aligned takes 16-byte stores."""
     w = _mla_case(612, [300, 64, 1000])
