@@ -160,9 +160,13 @@ typedef struct {
 
 /*
  * GQA / MHA / MQA decode over separate K and V pools.
- *   Supported: D_qk = D_v = 128; Hq % Hkv == 0; 1 <= (Hq/Hkv) * q_len <= 16
- *   (the query rows one kv head serves share one 16-row tensor-core tile);
- *   page_size a multiple of 16 (<= 1024); 1 <= B <= 4096. A query row that
+ *   Supported: D_qk = D_v = 128; Hq % Hkv == 0; g = Hq/Hkv <= 16;
+ *   1 <= q_len <= 128; page_size a multiple of 16 (<= 1024); 1 <= B <= 4096.
+ *   The query rows one kv head serves share a 16-row tensor-core tile: when
+ *   g * q_len > 16 the call runs one attention launch (and merge) per group of
+ *   16 / g query tokens, each reading the KV again; attn_begin is recorded
+ *   before the first and attn_end after the last attention launch. With
+ *   shared_prefix_pages > 0, g * q_len <= 16. A query row that
  *   sees no token (seq_lens[b] < q_len) gives out = 0 and lse = -inf. A bad
  *   page id zeroes every query row of its sequence and kv head.
  *   Anything else returns ZL_ERR_UNSUPPORTED (or ZL_ERR_INVALID_ARG when the

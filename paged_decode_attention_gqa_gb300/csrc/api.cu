@@ -5,6 +5,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstring>
@@ -83,9 +84,14 @@ struct GqaPlan {
   bool fused = false;
   // shared-prefix calls: prefix tiles, sequences per group, groups
   int prefix_tiles = 0, sgs = 0, ng = 0;
+  int q_group = 1;  // query tokens per launch (the call runs ceil(q_len / q_group))
   size_t off_prefix = 0, off_lse = 0, off_o = 0, off_pre_lse = 0, off_pre_o = 0;
   size_t off_suf_lse = 0, off_suf_o = 0, bytes = 0;
 };
+
+// Query tokens per sequence one call takes (the GQA path runs ceil(q_len /
+// (16 / g)) launches for them).
+constexpr int kMaxQueryTokens = 128;
 
 zl_status gqa_validate_shape(const zl_decode_attn_params* a) {
   if (!a || a->struct_size != sizeof(zl_decode_attn_params)) return ZL_ERR_INVALID_ARG;
@@ -99,7 +105,12 @@ zl_status gqa_validate_shape(const zl_decode_attn_params* a) {
   if (a->num_ctas > 65535) return ZL_ERR_UNSUPPORTED;  // the tile cut needs G^2 < 2^32
   if (!(a->scale > 0.f) || !std::isfinite(a->scale)) return ZL_ERR_INVALID_ARG;
   if (a->D_qk != zl::kGqaHeadDim || a->D_v != zl::kGqaHeadDim) return ZL_ERR_UNSUPPORTED;
-  if (a->Hq / a->Hkv * a->q_len > 16) return ZL_ERR_UNSUPPORTED;  // (query, head) rows per tile
+  // (query token, head) rows of one kv head share an m16 tile: at most 16 per
+  // launch, so g <= 16; a call with g * q_len > 16 runs one launch per group
+  // of 16 / g query tokens (each group reads the KV again). A shared-prefix
+  // call keeps all its tokens in one launch.
+  if (a->Hq / a->Hkv > 16 || a->q_len > kMaxQueryTokens) return ZL_ERR_UNSUPPORTED;
+  if (a->shared_prefix_pages > 0 && a->Hq / a->Hkv * a->q_len > 16) return ZL_ERR_UNSUPPORTED;
   if (a->page_size % zl::kGqaTile != 0 || a->page_size > 1024) return ZL_ERR_UNSUPPORTED;
   if (a->B > zl::kMaxBatch) return ZL_ERR_UNSUPPORTED;
   if (a->shared_prefix_pages < 0 || a->shared_prefix_pages > a->block_table_stride)
@@ -118,7 +129,8 @@ zl_status gqa_plan(const zl_decode_attn_params* a, GqaPlan* plan) {
   plan->fused = (a->flags & ZL_DECODE_SINGLE_LAUNCH) != 0;
   plan->hpc = zl::gqa_heads_per_cta(a->Hkv);
   plan->nhg = a->Hkv / plan->hpc;
-  const int rps = plan->g * a->q_len;
+  plan->q_group = std::min(a->q_len, 16 / plan->g);  // query tokens per launch
+  const int rps = plan->g * plan->q_group;
   if (a->shared_prefix_pages > 0) {
     plan->prefix_tiles = a->shared_prefix_pages * a->page_size / zl::kGqaTile;
     plan->sgs = 16 / rps > 0 ? 16 / rps : 1;
@@ -328,7 +340,7 @@ zl_status zl_decode_attn(const zl_decode_attn_params* a, zl_stream_t stream) {
   p.epoch = next_epoch();
   p.test_stall = (a->flags & ZL_DECODE_TEST_STALL) ? 1 : 0;
   p.B = a->B;
-  p.q_len = a->q_len;
+  p.q_total = a->q_len;
   p.Hq = a->Hq;
   p.Hkv = a->Hkv;
   p.g = plan.g;
@@ -345,15 +357,26 @@ zl_status zl_decode_attn(const zl_decode_attn_params* a, zl_stream_t stream) {
   p.suf_lse = reinterpret_cast<float*>(ws + plan.off_suf_lse);
   p.suf_o = reinterpret_cast<float*>(ws + plan.off_suf_o);
 
-  const cudaError_t e =
-      plan.prefix_tiles > 0
-          ? zl::gqa_shared_launch(p, plan.grid, reinterpret_cast<cudaStream_t>(stream),
-                                  reinterpret_cast<cudaEvent_t>(a->attn_begin),
-                                  reinterpret_cast<cudaEvent_t>(a->attn_end))
-          : zl::gqa_decode_launch(p, plan.grid, plan.fused, reinterpret_cast<cudaStream_t>(stream),
-                                  reinterpret_cast<cudaEvent_t>(a->attn_begin),
-                                  reinterpret_cast<cudaEvent_t>(a->attn_end));
-  return e == cudaSuccess ? ZL_OK : ZL_ERR_CUDA;
+  // One launch (attention, then its merge) per group of q_group query tokens;
+  // attn_begin is recorded before the first, attn_end after the last
+  // attention launch. The launches share the workspace: each reads it only
+  // after the one before has finished (programmatic dependent launches).
+  for (int tok0 = 0; tok0 < a->q_len; tok0 += plan.q_group) {
+    p.q_tok0 = tok0;
+    p.q_len = std::min(plan.q_group, a->q_len - tok0);
+    if (tok0 > 0) p.epoch = next_epoch();
+    const bool first = tok0 == 0, last = tok0 + p.q_len == a->q_len;
+    cudaEvent_t begin = first ? reinterpret_cast<cudaEvent_t>(a->attn_begin) : nullptr;
+    cudaEvent_t end = last ? reinterpret_cast<cudaEvent_t>(a->attn_end) : nullptr;
+    const cudaError_t e =
+        plan.prefix_tiles > 0
+            ? zl::gqa_shared_launch(p, plan.grid, reinterpret_cast<cudaStream_t>(stream), begin,
+                                    end)
+            : zl::gqa_decode_launch(p, plan.grid, plan.fused,
+                                    reinterpret_cast<cudaStream_t>(stream), begin, end);
+    if (e != cudaSuccess) return ZL_ERR_CUDA;
+  }
+  return ZL_OK;
 }
 
 zl_status zl_decode_attn_mla_workspace_size(const zl_decode_attn_params* a, size_t* bytes) {

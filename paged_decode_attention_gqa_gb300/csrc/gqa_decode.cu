@@ -57,7 +57,7 @@ cudaError_t gqa_decode_launch(const GqaParams& p, int grid, bool fused, cudaStre
   const bool r16 = p.g * p.q_len > 8;
   const bool known = p.hpc == 1 || p.hpc == 2 || p.hpc == 4 || p.hpc == 8;
   if (!known) return cudaErrorInvalidValue;
-  e = dispatch<Launch>(p.hpc, r16, p.q_len > 1, fused, &p, grid, stream);
+  e = dispatch<Launch>(p.hpc, r16, p.q_total > 1, fused, &p, grid, stream);
   if (e != cudaSuccess) return e;
   if (attn_end && (e = cudaEventRecord(attn_end, stream)) != cudaSuccess) return e;
   if (fused) return cudaSuccess;

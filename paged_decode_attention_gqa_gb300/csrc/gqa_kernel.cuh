@@ -241,7 +241,7 @@ __device__ __forceinline__ void merge_add_store(MergeAcc& m, const GqaParams& p,
   for (int k = 0; k < kMergeRows; ++k) {
     if (k < nrows) {
       const int r = r0 + k;
-      const int64_t orow = (int64_t(b) * p.q_len + r / p.g) * p.Hq + head0 + r % p.g;
+      const int64_t orow = (int64_t(b) * p.q_total + p.q_tok0 + r / p.g) * p.Hq + head0 + r % p.g;
       lv[k] = __ldcg(st_lse + orow);
       ov[k] = __ldcg(reinterpret_cast<const float4*>(st_o + orow * kGqaHeadDim) + lane);
     }
@@ -259,7 +259,7 @@ __device__ __forceinline__ void merge_write_out(const MergeAcc& m, const GqaPara
   for (int k = 0; k < kMergeRows; ++k) {
     if (k < nrows) {
       const int r = r0 + k;
-      const int64_t orow = (int64_t(b) * p.q_len + r / p.g) * p.Hq + head0 + r % p.g;
+      const int64_t orow = (int64_t(b) * p.q_total + p.q_tok0 + r / p.g) * p.Hq + head0 + r % p.g;
       const bool none = m.bad || !(m.den[k] > 0.f);
       const float inv = none ? 0.f : 1.f / m.den[k];
       uint2 packed = make_uint2(0u, 0u);
@@ -335,11 +335,14 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
   const int PT = p.prefix_tiles;
   const int NG = MODE == kModeShared ? p.ng : 0;
   const int V = NG + B;
+  // A sequence's tiles end where its last query token of this launch stops
+  // seeing: L - (q_total - q_tok0 - q_len) tokens (L for the last token).
+  const int unseen = p.q_total - p.q_tok0 - p.q_len;
   auto unit_tiles = [&](int v) -> int {
     if (v < NG) return PT;
     const int L = p.seq_lens[v - NG];
     if (!(L >= 0 && int64_t(L) <= cap)) return 0;
-    const int t = (L + kGqaTile - 1) / kGqaTile - (MODE == kModeShared ? PT : 0);
+    const int t = (L - unseen + kGqaTile - 1) / kGqaTile - (MODE == kModeShared ? PT : 0);
     return t > 0 ? t : 0;
   };
   if (warp == 0) {
@@ -381,7 +384,7 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
       for (int j = lane; j < ppages; j += 32)
         bad |= p.block_table[int64_t(b) * p.bt_stride + j] != p.block_table[j] ? 1 : 0;
       const int L = p.seq_lens[b];
-      if (lane == 0 && (int64_t(L) > cap || L - p.q_len + 1 < PT * kGqaTile)) bad = 1;
+      if (lane == 0 && (int64_t(L) > cap || L - p.q_total + 1 < PT * kGqaTile)) bad = 1;
       if (__any_sync(0xffffffffu, bad) && lane == 0) raise_error(p.err_flags, kErrBadPrefix);
     }
   }
@@ -511,18 +514,20 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
     const int head0 = (hg * HPC + w) * g;  // first query head of this kv head
     // m16 tile rows are (sequence b + r / rps, query token i, head head0 + j)
     // with rps = g * q_len rows per sequence, r % rps = i * g + j; R rows per
-    // partial slot, R_act of them exist, the rest are zero. Query i sees tokens
-    // t < L - q_len + 1 + i (the new tokens are in the cache; each sees itself
-    // and what precedes it); every row sees all of a shared prefix.
+    // partial slot, R_act of them exist, the rest are zero. Query i (token
+    // q_tok0 + i of the q_total) sees tokens t < L - q_total + 1 + q_tok0 + i
+    // (the new tokens are in the cache; each sees itself and what precedes
+    // it); every row sees all of a shared prefix.
     const int rps = g * p.q_len;
     const int R = MODE == kModeShared ? p.sgs * rps : rps;
     const int R_act = pre ? min(p.sgs, B - b) * rps : rps;
     const int ra = gid, rb = gid + 8;
-    const int lim_a = pre ? (1 << 30) : L - p.q_len + 1 + ra / g;
-    const int lim_b = pre ? (1 << 30) : L - p.q_len + 1 + rb / g;
+    const int lim0 = L - p.q_total + 1 + p.q_tok0;
+    const int lim_a = pre ? (1 << 30) : lim0 + ra / g;
+    const int lim_b = pre ? (1 << 30) : lim0 + rb / g;
     auto qrow_index = [&](int r) -> int64_t {
       const int rr = r % rps;
-      return (int64_t(b + r / rps) * p.q_len + rr / g) * p.Hq + head0 + rr % g;
+      return (int64_t(b + r / rps) * p.q_total + p.q_tok0 + rr / g) * p.Hq + head0 + rr % g;
     };
 
     uint32_t qa[8][4];
@@ -746,13 +751,14 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
     // Sequences with no tiles (empty or invalid length): zeros, lse = -inf.
     for (int b = c; b < B; b += G) {
       if (prefix[b + 1] != prefix[b]) continue;
+      // this launch's rows of sequence b: tokens [q_tok0, q_tok0 + q_len)
       const int64_t rows = int64_t(p.q_len) * p.Hq;
-      uint4* dst = reinterpret_cast<uint4*>(p.out + int64_t(b) * rows * kGqaHeadDim);
+      const int64_t row0 = (int64_t(b) * p.q_total + p.q_tok0) * p.Hq;
+      uint4* dst = reinterpret_cast<uint4*>(p.out + row0 * kGqaHeadDim);
       const int64_t n16 = rows * kGqaHeadDim * 2 / 16;
       for (int64_t i = tid; i < n16; i += HPC * 32) dst[i] = make_uint4(0u, 0u, 0u, 0u);
       if (p.lse)
-        for (int64_t i = tid; i < rows; i += HPC * 32)
-          p.lse[int64_t(b) * rows + i] = -CUDART_INF_F;
+        for (int64_t i = tid; i < rows; i += HPC * 32) p.lse[row0 + i] = -CUDART_INF_F;
     }
   }
 }

@@ -57,7 +57,7 @@ cudaError_t gqa_shared_launch(const GqaParams& p, int grid, cudaStream_t stream,
   cudaError_t e = cudaSuccess;
   if (attn_begin && (e = cudaEventRecord(attn_begin, stream)) != cudaSuccess) return e;
   const bool r16 = p.sgs * p.g * p.q_len > 8;
-  if ((e = dispatch_mode<Launch, kModeShared>(p.hpc, r16, p.q_len > 1, &p, grid, stream)) !=
+  if ((e = dispatch_mode<Launch, kModeShared>(p.hpc, r16, p.q_total > 1, &p, grid, stream)) !=
       cudaSuccess)
     return e;
   if (attn_end && (e = cudaEventRecord(attn_end, stream)) != cudaSuccess) return e;

@@ -40,6 +40,10 @@ struct GqaParams {
   float* suf_lse;
   int test_stall;      // failure-detection test hook: stall the producer until its wait runs out
   int B, q_len, Hq, Hkv, g, page_size, num_pages;
+  // Query tokens: q_len of them in this launch, tokens [q_tok0, q_tok0 + q_len)
+  // of the q_total each sequence has (q, out and lse rows are [B, q_total, Hq]).
+  // A call with g * q_total > 16 runs one launch per group of 16 / g tokens.
+  int q_total, q_tok0;
   int hpc;             // kv heads per CTA
   int nhg;             // Hkv / hpc head groups
   float scale_log2;    // scale * log2(e)

@@ -112,3 +112,65 @@ def test_full_size_llama3_8b_mtp_sampled():
     assert st == 0
     assert_close(g.out64()[bs], ref, "sampled out")
     assert_close(g.lse64()[bs], ref_lse, "sampled lse")
+
+
+# More query rows than one tensor-core tile holds (g * q_len > 16): the call
+# runs one launch per group of 16 / g tokens, each with its own causal limits.
+@pytest.mark.parametrize("Hq,Hkv,q_len", [
+    (32, 8, 8), (32, 8, 5), (32, 8, 13),     # group of 4: 4 + 4, 4 + 1, 4 + 4 + 4 + 1
+    (64, 8, 3),                              # group of 8: 2 + 1
+    (128, 8, 2),                             # group of 16: one token per launch
+    (16, 8, 17),                             # group of 2: 8 + 8 + 1
+])
+def test_token_groups(Hq, Hkv, q_len):
+    w = wl.random_case(900 + 31 * Hq + 7 * Hkv + q_len, B=5, Hq=Hq, Hkv=Hkv, max_len=300,
+                       q_len=q_len)
+    _parity(w)
+
+
+def test_token_groups_short_contexts():
+    """Groups whose rows see nothing (L < q_len), and lengths at the tile edges."""
+    q_len = 6
+    lens = [0, 1, 3, 5, 6, 7, 15, 16, 17, 21, 22, 40]
+    w = wl.random_case(910, B=len(lens), Hq=32, Hkv=8, lens=lens, q_len=q_len)
+    g = _parity(w)
+    out = g.out.float().cpu()
+    for b, L in enumerate(lens):
+        for i in range(q_len):
+            if L - q_len + 1 + i <= 0:
+                assert torch.all(out[b, i] == 0)
+                assert torch.all(torch.isneginf(g.lse[b, i].cpu()))
+
+
+@pytest.mark.parametrize("num_ctas", [1, 7, 151, 1000])
+def test_token_groups_any_split(num_ctas):
+    w = wl.random_case(920, B=6, Hq=32, Hkv=8, max_len=700, q_len=8)
+    _parity(w, num_ctas=num_ctas)
+
+
+def test_token_groups_single_launch():
+    w = wl.random_case(930, B=6, Hq=32, Hkv=8, max_len=700, q_len=7)
+    d = device_inputs(w)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lse = torch.empty((w.B, w.q_len, w.Hq), dtype=torch.float32, device="cuda")
+    out = zl.decode_attn(d["q"], d["k"], d["v"], d["bt"], d["sl"], page_size=w.page_size,
+                         scale=w.scale, lse=lse, err_flags=err, max_seq_len=w.max_seq_len,
+                         single_launch=True)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref, ref_lse, _ = run_oracle(w)
+    assert_close(out.float().cpu().numpy(), ref, "single launch, token groups")
+    assert_close(lse.double().cpu().numpy(), ref_lse, "single launch, token groups lse")
+
+
+def test_token_groups_last_row_equals_single_token_call():
+    """The last of 8 query tokens (in the second launch) sees the whole cache:
+    the same row as a q_len = 1 call with that query, bit for bit."""
+    w = wl.random_case(940, B=5, Hq=32, Hkv=8, max_len=400, q_len=8)
+    d = device_inputs(w)
+    g = run_gpu(w, d)
+    q1 = d["q"][:, -1:].contiguous()
+    out1 = zl.decode_attn(q1, d["k"], d["v"], d["bt"], d["sl"], page_size=w.page_size,
+                          scale=w.scale, max_seq_len=w.max_seq_len)
+    torch.cuda.synchronize()
+    assert torch.equal(g.out[:, -1].view(torch.int16), out1[:, 0].view(torch.int16))
