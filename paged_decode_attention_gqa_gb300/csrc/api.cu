@@ -85,7 +85,7 @@ struct GqaPlan {
   // shared-prefix calls: prefix tiles, sequences per group, groups
   int prefix_tiles = 0, sgs = 0, ng = 0;
   int q_group = 1;  // query tokens per launch (the call runs ceil(q_len / q_group))
-  size_t off_prefix = 0, off_lse = 0, off_o = 0, off_pre_lse = 0, off_pre_o = 0;
+  size_t off_lse = 0, off_o = 0, off_pre_lse = 0, off_pre_o = 0;
   size_t off_suf_lse = 0, off_suf_o = 0, bytes = 0;
 };
 
@@ -156,15 +156,11 @@ zl_status gqa_plan(const zl_decode_attn_params* a, GqaPlan* plan) {
   plan->grid = grid;
   const size_t rows = size_t(grid) * 2 * plan->hpc * rows_per_warp;  // partial slots
   const size_t store_rows = plan->prefix_tiles > 0 ? size_t(a->B) * a->q_len * a->Hq : 0;
-  // [0, off_prefix): one arrival counter (8 bytes) per (sequence, kv head);
-  // [off_prefix, off_lse): the tile prefix sums the merge kernel reads (one per
-  // unit: groups, then sequences); then the partials' lse and outputs; then
-  // (shared prefix) each query row's result over its prefix part and over its
-  // suffix part when one CTA had the whole unit: base-2 lse and normalised
-  // fp32 output.
-  plan->off_prefix = round_up(size_t(a->B) * a->Hkv * sizeof(unsigned long long), 256);
-  plan->off_lse =
-      plan->off_prefix + round_up(size_t(plan->ng + a->B + 1) * sizeof(int32_t), 256);
+  // [0, off_lse): one arrival counter (8 bytes) per (sequence, kv head); then
+  // the partials' lse and outputs; then (shared prefix) each query row's
+  // result over its prefix part and over its suffix part when one CTA had the
+  // whole unit: base-2 lse and normalised fp32 output.
+  plan->off_lse = round_up(size_t(a->B) * a->Hkv * sizeof(unsigned long long), 256);
   plan->off_o = plan->off_lse + round_up(rows * sizeof(float), 256);
   plan->off_pre_lse = plan->off_o + round_up(rows * zl::kGqaHeadDim * sizeof(float), 256);
   plan->off_pre_o = plan->off_pre_lse + round_up(store_rows * sizeof(float), 256);
@@ -333,7 +329,6 @@ zl_status zl_decode_attn(const zl_decode_attn_params* a, zl_stream_t stream) {
   p.bt_stride = a->block_table_stride;
   char* ws = static_cast<char*>(a->workspace);
   p.ws_count = reinterpret_cast<unsigned long long*>(ws);
-  p.ws_prefix = reinterpret_cast<int32_t*>(ws + plan.off_prefix);
   p.ws_lse = reinterpret_cast<float*>(ws + plan.off_lse);
   p.ws_o = reinterpret_cast<float*>(ws + plan.off_o);
   p.err_flags = a->err_flags;

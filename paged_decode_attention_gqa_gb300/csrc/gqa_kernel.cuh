@@ -290,6 +290,19 @@ __device__ __forceinline__ void merge_split_rows(const GqaParams& p, const TileC
   }
 }
 
+// Tiles of sequence b's own unit for this launch (seq_lens[b] = L): they end
+// where the launch's last query token stops seeing, L - (q_total - q_tok0 -
+// q_len) tokens; a shared-prefix launch leaves out the prefix tiles. An
+// invalid length (negative, or more tokens than the block table maps) has none.
+template <int MODE>
+__device__ __forceinline__ int seq_unit_tiles(const GqaParams& p, int L) {
+  const int64_t cap = p.bt_stride * int64_t(p.page_size);
+  if (!(L >= 0 && int64_t(L) <= cap)) return 0;
+  const int unseen = p.q_total - p.q_tok0 - p.q_len;
+  const int t = (L - unseen + kGqaTile - 1) / kGqaTile - (MODE == kModeShared ? p.prefix_tiles : 0);
+  return t > 0 ? t : 0;
+}
+
 template <int HPC, bool ROWS16, bool CAUSAL, bool FUSED, int MODE = kModePlain>
 __global__ void __launch_bounds__(GqaCfg<HPC>::kThreads, 1)
 gqa_decode_kernel(const __grid_constant__ GqaParams p) {
@@ -335,15 +348,8 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
   const int PT = p.prefix_tiles;
   const int NG = MODE == kModeShared ? p.ng : 0;
   const int V = NG + B;
-  // A sequence's tiles end where its last query token of this launch stops
-  // seeing: L - (q_total - q_tok0 - q_len) tokens (L for the last token).
-  const int unseen = p.q_total - p.q_tok0 - p.q_len;
   auto unit_tiles = [&](int v) -> int {
-    if (v < NG) return PT;
-    const int L = p.seq_lens[v - NG];
-    if (!(L >= 0 && int64_t(L) <= cap)) return 0;
-    const int t = (L - unseen + kGqaTile - 1) / kGqaTile - (MODE == kModeShared ? PT : 0);
-    return t > 0 ? t : 0;
+    return v < NG ? PT : seq_unit_tiles<MODE>(p, p.seq_lens[v - NG]);
   };
   if (warp == 0) {
     const int per = (V + 31) / 32;
@@ -391,10 +397,9 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
   __syncthreads();
 
   if constexpr (!FUSED) {
-    // The merge kernel reads the tile counts, and may be scheduled early:
-    // it waits for this whole grid to finish before reading anything.
-    if (blockIdx.x == 0)
-      for (int v = tid; v <= V; v += Cfg::kThreads) p.ws_prefix[v] = prefix[v];
+    // The merge kernel may be scheduled from here on (this grid is past its
+    // own dependency wait); it waits for this whole grid to finish before it
+    // reads any partial.
     griddep_launch_dependents();
   }
 
@@ -782,26 +787,43 @@ __device__ __forceinline__ int cta_of_tile(int64_t x, int64_t W, int G) {
 template <int MODE>
 __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ GqaParams p,
                                                         int G) {
-  griddep_wait();
-  griddep_launch_dependents();  // the next kernels may start their prologue
   const int lane = threadIdx.x & 31;
   const int rps = p.g * p.q_len;
   const int nrb = (rps + kMergeRows - 1) / kMergeRows;
   const int64_t item = int64_t(blockIdx.x) * 4 + (threadIdx.x >> 5);
-  if (item >= int64_t(p.B) * p.Hkv * nrb) return;
-  const int64_t unit = item / nrb;  // b * Hkv + kv head
+  const bool live = item < int64_t(p.B) * p.Hkv * nrb;
+  const int64_t unit = live ? item / nrb : 0;  // b * Hkv + kv head
+  const int b = int(unit / p.Hkv), kvh = int(unit % p.Hkv);
+  // Before waiting for the attention grid: the tile line, from seq_lens alone.
+  // seq_lens is an input of the call; the attention grid let this kernel
+  // launch only after its own dependency wait, so it is final here. Units are
+  // the ng prefix groups (prefix_tiles tiles each), then the sequences.
+  const int NG = MODE == kModeShared ? p.ng : 0;
+  int before = 0, all = 0;  // tiles of sequences before b, of every sequence
+  if (live) {
+    for (int s = lane; s < p.B; s += 32) {
+      const int t = seq_unit_tiles<MODE>(p, p.seq_lens[s]);
+      all += t;
+      before += s < b ? t : 0;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      all += __shfl_xor_sync(0xffffffffu, all, off);
+      before += __shfl_xor_sync(0xffffffffu, before, off);
+    }
+  }
+  const int n = live ? seq_unit_tiles<MODE>(p, p.seq_lens[b]) : 0;
+  griddep_wait();
+  griddep_launch_dependents();  // the next kernels may start their prologue
+  if (!live) return;
   const int r0 = int(item % nrb) * kMergeRows;
   const int nrows = min(kMergeRows, rps - r0);
-  const int b = int(unit / p.Hkv), kvh = int(unit % p.Hkv);
   const int hg = kvh / p.hpc, w = kvh % p.hpc;
   const int head0 = kvh * p.g;
-  const int* prefix = p.ws_prefix;
-  const int NG = MODE == kModeShared ? p.ng : 0;
-  const int64_t W = int64_t(p.nhg) * prefix[NG + p.B];
+  const int PT = MODE == kModeShared ? p.prefix_tiles : 0;
+  const int64_t W = int64_t(p.nhg) * (int64_t(NG) * PT + all);
   const TileCut cut{W / G, uint32_t(W % G), uint32_t(G)};
-  const int vs = NG + b;  // the sequence's own unit
-  const int n = prefix[vs + 1] - prefix[vs];
-  const int64_t U0 = int64_t(p.nhg) * prefix[vs] + int64_t(hg) * n;
+  const int64_t U0 = int64_t(p.nhg) * (int64_t(NG) * PT + before) + int64_t(hg) * n;
   const int c_lo = n ? cta_of_tile(U0, W, G) : 0, c_hi = n ? cta_of_tile(U0 + n - 1, W, G) : 0;
   if constexpr (MODE == kModePlain) {
     if (n == 0 || c_lo == c_hi) return;
@@ -811,9 +833,9 @@ __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ 
     MergeAcc m;
     m.init();
     {
-      const int vp = b / p.sgs;  // the group's prefix unit
-      const int np = prefix[vp + 1] - prefix[vp];
-      const int64_t P0 = int64_t(p.nhg) * prefix[vp] + int64_t(hg) * np;
+      const int vp = b / p.sgs;  // the group's prefix unit (each has PT tiles)
+      const int np = PT;
+      const int64_t P0 = int64_t(p.nhg) * (int64_t(vp) * PT) + int64_t(hg) * np;
       const int p_lo = cta_of_tile(P0, W, G), p_hi = cta_of_tile(P0 + np - 1, W, G);
       if (p_lo == p_hi)
         merge_add_store(m, p, p.pre_o, p.pre_lse, b, head0, r0, nrows, lane);

@@ -23,7 +23,6 @@ struct GqaParams {
   const int32_t* seq_lens;
   int64_t bt_stride;
   unsigned long long* ws_count;  // [B * Hkv] arrivals per split unit: epoch << 32 | count
-  int32_t* ws_prefix;  // [B + 1] tile prefix sums, written by CTA 0 for the merge kernel
   float* ws_o;         // [G][2][HPC][g * q_len][128] normalised partial outputs
   float* ws_lse;       // [G][2][HPC][g * q_len] base-2 lse of the partials (NaN = bad piece)
   uint32_t* err_flags; // or nullptr
