@@ -380,9 +380,8 @@ def run_ours(args, world, rank, local):
     else:
         ms = sum(a.elapsed_time(b) for a, b in step_evs) / args.steps
     ms = max_over_ranks(ms, world, dev)
-    # attention + merge: one launch with ZL_DECODE_SINGLE_LAUNCH, else two (MLA and
-    # shared-prefix calls: two)
-    launches = args.steps * (1 if (kind == "gqa" and args.single_launch) else 2)
+    # the library's own count per call: attention (+ merge) per token group
+    launches = args.steps * (2 if w.mla else zl.launches(p))
     if ap is not None:
         launches += args.steps                              # the KV append
     if flush is not None:

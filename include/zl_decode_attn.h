@@ -166,7 +166,9 @@ typedef struct {
  *   g * q_len > 16 the call runs one attention launch (and merge) per group of
  *   16 / g query tokens, each reading the KV again; attn_begin is recorded
  *   before the first and attn_end after the last attention launch. With
- *   shared_prefix_pages > 0, g * q_len <= 16. A query row that
+ *   shared_prefix_pages > 0, g * q_len <= 16. When max_seq_len shows that
+ *   every (sequence, head group) is short (at most 512 KB of K and V), each
+ *   gets a CTA of its own and no merge is launched. A query row that
  *   sees no token (seq_lens[b] < q_len) gives out = 0 and lse = -inf. A bad
  *   page id zeroes every query row of its sequence and kv head.
  *   Anything else returns ZL_ERR_UNSUPPORTED (or ZL_ERR_INVALID_ARG when the
@@ -193,6 +195,14 @@ zl_status zl_decode_attn_mla(const zl_decode_attn_params* params, zl_stream_t st
    Needs a current CUDA device (the default grid depends on its SM count). */
 zl_status zl_decode_attn_workspace_size(const zl_decode_attn_params* params, size_t* bytes);
 zl_status zl_decode_attn_mla_workspace_size(const zl_decode_attn_params* params, size_t* bytes);
+
+/* Kernel launches one zl_decode_attn call with these params enqueues: per
+   group of query tokens (see zl_decode_attn), the attention kernel and, unless
+   no unit is cut (short contexts given a CTA per unit, known from max_seq_len)
+   or ZL_DECODE_SINGLE_LAUNCH merges inside it, the merge kernel. The same
+   inputs and rules as zl_decode_attn_workspace_size. (zl_decode_attn_mla
+   always enqueues two.) */
+zl_status zl_decode_attn_launches(const zl_decode_attn_params* params, int32_t* launches);
 
 /*
  * zl_decode_attn without a caller-provided workspace, for callers that cannot

@@ -128,6 +128,8 @@ def lib():
                 fn = getattr(handle, name)
                 fn.restype = ctypes.c_int
                 fn.argtypes = [P, ctypes.POINTER(ctypes.c_size_t)]
+            handle.zl_decode_attn_launches.restype = ctypes.c_int
+            handle.zl_decode_attn_launches.argtypes = [P, ctypes.POINTER(ctypes.c_int32)]
             handle.zl_kv_append.restype = ctypes.c_int
             handle.zl_kv_append.argtypes = [ctypes.POINTER(AppendParams), ctypes.c_void_p]
             handle.zl_status_string.restype = ctypes.c_char_p
@@ -234,6 +236,14 @@ def _workspace(device, nbytes, kind, counters=0):
         buf[:counters].zero_()
     _ws_cache[key] = (buf, (nbytes, counters) if counters else None)
     return buf
+
+
+def launches(params: Params) -> int:
+    """Kernel launches one zl_decode_attn call with these params enqueues."""
+    n = ctypes.c_int32(0)
+    _check(lib().zl_decode_attn_launches(ctypes.byref(params), ctypes.byref(n)),
+           "zl_decode_attn_launches")
+    return int(n.value)
 
 
 def call_noalloc(params: Params, stream=None):

@@ -85,6 +85,7 @@ struct GqaPlan {
   // shared-prefix calls: prefix tiles, sequences per group, groups
   int prefix_tiles = 0, sgs = 0, ng = 0;
   int q_group = 1;  // query tokens per launch (the call runs ceil(q_len / q_group))
+  bool unit_cut = false;  // one CTA per (sequence, head group): no cut unit, no merge
   size_t off_lse = 0, off_o = 0, off_pre_lse = 0, off_pre_o = 0;
   size_t off_suf_lse = 0, off_suf_o = 0, bytes = 0;
 };
@@ -92,6 +93,10 @@ struct GqaPlan {
 // Query tokens per sequence one call takes (the GQA path runs ceil(q_len /
 // (16 / g)) launches for them).
 constexpr int kMaxQueryTokens = 128;
+// A call whose longest (sequence, head group) unit has at most this many K and
+// V bytes (known from max_seq_len) gives each unit a CTA of its own and skips
+// the merge: one CTA streams that in about the time a merge launch takes.
+constexpr int64_t kUnitCutBytes = 512 * 1024;
 
 zl_status gqa_validate_shape(const zl_decode_attn_params* a) {
   if (!a || a->struct_size != sizeof(zl_decode_attn_params)) return ZL_ERR_INVALID_ARG;
@@ -147,10 +152,21 @@ zl_status gqa_plan(const zl_decode_attn_params* a, GqaPlan* plan) {
     if (per_sm < 1) return ZL_ERR_CUDA;
     grid = dev.sms * per_sm;
     if (a->max_seq_len > 0 && plan->prefix_tiles == 0) {
-      // No more CTAs than tiles: B * head groups * ceil(max_seq_len / 16).
-      const int64_t tiles = int64_t(a->B) * plan->nhg *
-                            ((int64_t(a->max_seq_len) + zl::kGqaTile - 1) / zl::kGqaTile);
-      if (tiles < grid) grid = int(tiles < 1 ? 1 : tiles);
+      const int64_t max_tiles = (int64_t(a->max_seq_len) + zl::kGqaTile - 1) / zl::kGqaTile;
+      const int64_t units = int64_t(a->B) * plan->nhg;
+      // K and V bytes of the longest unit (sequence, head group).
+      const int64_t unit_bytes = max_tiles * zl::kGqaTile * plan->hpc * zl::kGqaHeadDim * 2 * 2;
+      if (units <= grid && unit_bytes <= kUnitCutBytes) {
+        // Short contexts: one CTA per whole unit. Streaming the longest unit
+        // alone costs less than cutting units and merging their pieces.
+        plan->unit_cut = true;
+        plan->fused = false;
+        grid = int(units);
+      } else {
+        // No more CTAs than tiles: B * head groups * ceil(max_seq_len / 16).
+        const int64_t tiles = units * max_tiles;
+        if (tiles < grid) grid = int(tiles < 1 ? 1 : tiles);
+      }
     }
   }
   plan->grid = grid;
@@ -308,6 +324,16 @@ zl_status zl_decode_attn_workspace_size(const zl_decode_attn_params* a, size_t* 
   return ZL_OK;
 }
 
+zl_status zl_decode_attn_launches(const zl_decode_attn_params* a, int32_t* launches) {
+  if (!launches) return ZL_ERR_INVALID_ARG;
+  GqaPlan plan;
+  const zl_status st = gqa_plan(a, &plan);
+  if (st != ZL_OK) return st;
+  const int groups = (a->q_len + plan.q_group - 1) / plan.q_group;
+  *launches = groups * ((plan.fused || plan.unit_cut) ? 1 : 2);
+  return ZL_OK;
+}
+
 zl_status zl_decode_attn(const zl_decode_attn_params* a, zl_stream_t stream) {
   zl_status st = gqa_validate_shape(a);
   if (st != ZL_OK) return st;
@@ -335,6 +361,7 @@ zl_status zl_decode_attn(const zl_decode_attn_params* a, zl_stream_t stream) {
   p.epoch = next_epoch();
   p.test_stall = (a->flags & ZL_DECODE_TEST_STALL) ? 1 : 0;
   p.B = a->B;
+  p.unit_cut = plan.unit_cut ? 1 : 0;
   p.q_total = a->q_len;
   p.Hq = a->Hq;
   p.Hkv = a->Hkv;

@@ -60,7 +60,7 @@ cudaError_t gqa_decode_launch(const GqaParams& p, int grid, bool fused, cudaStre
   e = dispatch<Launch>(p.hpc, r16, p.q_total > 1, fused, &p, grid, stream);
   if (e != cudaSuccess) return e;
   if (attn_end && (e = cudaEventRecord(attn_end, stream)) != cudaSuccess) return e;
-  if (fused) return cudaSuccess;
+  if (fused || p.unit_cut) return cudaSuccess;  // nothing left to merge
   // The merge as a programmatic dependent launch: its CTAs may become resident
   // before the attention grid ends and wait in griddepcontrol.wait.
   const int64_t items = int64_t(p.B) * p.Hkv * ((p.g * p.q_len + kMergeRows - 1) / kMergeRows);

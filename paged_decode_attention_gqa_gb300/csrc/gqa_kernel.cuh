@@ -407,8 +407,17 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
   const int nhg = p.nhg;
   const int64_t W = int64_t(nhg) * prefix[V];
   const TileCut cut{W / G, uint32_t(W % G), uint32_t(G)};
-  const int64_t s_c = cut.start(c);
-  const int64_t e_c = cut.start(c + 1);
+  int64_t s_c = cut.start(c);
+  int64_t e_c = cut.start(c + 1);
+  if (MODE == kModePlain && p.unit_cut) {
+    // Unit (v, hg) holds tiles [nhg * prefix[v] + hg * n, + n) of the line.
+    s_c = e_c = 0;
+    if (c < int64_t(V) * nhg) {
+      const int v = c / nhg, n = prefix[v + 1] - prefix[v];
+      s_c = int64_t(nhg) * prefix[v] + int64_t(c % nhg) * n;
+      e_c = s_c + n;
+    }
+  }
 
   if (warp == HPC) {
     // ------------------------------------------------------------ producer

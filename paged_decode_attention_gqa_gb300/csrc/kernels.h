@@ -43,6 +43,10 @@ struct GqaParams {
   // of the q_total each sequence has (q, out and lse rows are [B, q_total, Hq]).
   // A call with g * q_total > 16 runs one launch per group of 16 / g tokens.
   int q_total, q_tok0;
+  // 1: CTA c takes unit c (sequence c / nhg, head group c % nhg) whole, so no
+  // unit is cut and there is nothing to merge (the host picks this for short
+  // contexts, where a merge launch would cost more than the attention).
+  int unit_cut;
   int hpc;             // kv heads per CTA
   int nhg;             // Hkv / hpc head groups
   float scale_log2;    // scale * log2(e)

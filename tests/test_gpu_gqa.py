@@ -210,3 +210,39 @@ def test_cuda_graph_capture_of_the_default_path():
         assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
     ref, _, _ = run_oracle(w)
     assert_close(out.float().cpu().numpy().astype(np.float64), ref, "graph replay")
+
+
+def _launches(w, **kw):
+    d = device_inputs(w)
+    out = torch.empty((w.B, w.q_len, w.Hq, 128), dtype=torch.bfloat16, device="cuda")
+    p = zl.make_params(d["q"], d["k"], d["v"], d["bt"], d["sl"], out, page_size=w.page_size,
+                       scale=w.scale, Hkv=w.Hkv, D_v=128, max_seq_len=w.max_seq_len, **kw)
+    return zl.launches(p)
+
+
+def test_short_contexts_take_one_cta_per_unit():
+    """max_seq_len shows every (sequence, head group) is short (here 7 tiles x
+    64 KB of K and V): one CTA each, one launch, nothing to merge."""
+    w = wl.random_case(410, B=6, Hq=32, Hkv=8, max_len=100)
+    assert _launches(w) == 1
+    assert _launches(w, num_ctas=152) == 2  # an explicit grid cuts as usual
+    _parity(w)
+
+
+def test_longer_contexts_are_cut_and_merged():
+    w = wl.random_case(411, B=6, Hq=32, Hkv=8, lens=[3000, 40, 900, 1, 2500, 128])
+    assert _launches(w) == 2
+    _parity(w)
+
+
+def test_short_contexts_with_empty_and_bad_sequences():
+    w = wl.random_case(412, B=5, Hq=16, Hkv=4, lens=[0, 70, 1, 33, 64])
+    d = device_inputs(w)
+    bt = w.block_table.copy()
+    bt[3, 1] = -1
+    assert _launches(w) == 1
+    g = run_gpu(w, d, block_table=torch.from_numpy(bt).cuda())
+    assert int(g.err.item()) & zl.DEVERR_BAD_PAGE
+    assert (g.out[0] == 0).all() and (g.out[3, :, 4:8] == 0).all()
+    ref, _, _ = run_oracle(w, block_table=bt)
+    assert_close(g.out64(), ref, "short contexts, empty and bad")
