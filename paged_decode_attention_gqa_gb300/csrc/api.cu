@@ -187,6 +187,13 @@ zl_status gqa_plan(const zl_decode_attn_params* a, GqaPlan* plan) {
   return ZL_OK;
 }
 
+// A call with several groups of query tokens runs them in one launch, side by
+// side, unless it merges inside the attention kernel (its arrival counters
+// are per sequence and kv head) or has a shared prefix (one group only).
+bool groups_together(const GqaPlan& plan, int q_len) {
+  return plan.q_group < q_len && !plan.fused && plan.prefix_tiles == 0;
+}
+
 // ------------------------------------------------------------------ MLA plan
 struct MlaPlan {
   int clusters = 0;
@@ -329,8 +336,9 @@ zl_status zl_decode_attn_launches(const zl_decode_attn_params* a, int32_t* launc
   GqaPlan plan;
   const zl_status st = gqa_plan(a, &plan);
   if (st != ZL_OK) return st;
+  const int per_launch = (plan.fused || plan.unit_cut) ? 1 : 2;
   const int groups = (a->q_len + plan.q_group - 1) / plan.q_group;
-  *launches = groups * ((plan.fused || plan.unit_cut) ? 1 : 2);
+  *launches = groups_together(plan, a->q_len) ? per_launch : groups * per_launch;
   return ZL_OK;
 }
 
@@ -379,10 +387,28 @@ zl_status zl_decode_attn(const zl_decode_attn_params* a, zl_stream_t stream) {
   p.suf_lse = reinterpret_cast<float*>(ws + plan.off_suf_lse);
   p.suf_o = reinterpret_cast<float*>(ws + plan.off_suf_o);
 
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int ngroups = (a->q_len + plan.q_group - 1) / plan.q_group;
+  if (groups_together(plan, a->q_len)) {
+    // Every group of q_group query tokens in one launch, side by side: the
+    // grid's CTAs are split between the groups, and each group cuts the same
+    // tile line, so the groups read each K/V tile at about the same time (the
+    // second read is served by L2). One merge launch covers every group.
+    p.q_tok0 = 0;
+    p.q_len = plan.q_group;
+    p.ngroups = ngroups;
+    p.group_ctas = plan.unit_cut ? plan.grid : std::max(1, plan.grid / ngroups);
+    const cudaError_t e = zl::gqa_decode_launch(
+        p, p.group_ctas * ngroups, false, s, reinterpret_cast<cudaEvent_t>(a->attn_begin),
+        reinterpret_cast<cudaEvent_t>(a->attn_end));
+    return e == cudaSuccess ? ZL_OK : ZL_ERR_CUDA;
+  }
   // One launch (attention, then its merge) per group of q_group query tokens;
   // attn_begin is recorded before the first, attn_end after the last
   // attention launch. The launches share the workspace: each reads it only
   // after the one before has finished (programmatic dependent launches).
+  p.ngroups = 1;
+  p.group_ctas = plan.grid;
   for (int tok0 = 0; tok0 < a->q_len; tok0 += plan.q_group) {
     p.q_tok0 = tok0;
     p.q_len = std::min(plan.q_group, a->q_len - tok0);
@@ -390,12 +416,9 @@ zl_status zl_decode_attn(const zl_decode_attn_params* a, zl_stream_t stream) {
     const bool first = tok0 == 0, last = tok0 + p.q_len == a->q_len;
     cudaEvent_t begin = first ? reinterpret_cast<cudaEvent_t>(a->attn_begin) : nullptr;
     cudaEvent_t end = last ? reinterpret_cast<cudaEvent_t>(a->attn_end) : nullptr;
-    const cudaError_t e =
-        plan.prefix_tiles > 0
-            ? zl::gqa_shared_launch(p, plan.grid, reinterpret_cast<cudaStream_t>(stream), begin,
-                                    end)
-            : zl::gqa_decode_launch(p, plan.grid, plan.fused,
-                                    reinterpret_cast<cudaStream_t>(stream), begin, end);
+    const cudaError_t e = plan.prefix_tiles > 0
+                              ? zl::gqa_shared_launch(p, plan.grid, s, begin, end)
+                              : zl::gqa_decode_launch(p, plan.grid, plan.fused, s, begin, end);
     if (e != cudaSuccess) return ZL_ERR_CUDA;
   }
   return ZL_OK;

@@ -63,7 +63,8 @@ cudaError_t gqa_decode_launch(const GqaParams& p, int grid, bool fused, cudaStre
   if (fused || p.unit_cut) return cudaSuccess;  // nothing left to merge
   // The merge as a programmatic dependent launch: its CTAs may become resident
   // before the attention grid ends and wait in griddepcontrol.wait.
-  const int64_t items = int64_t(p.B) * p.Hkv * ((p.g * p.q_len + kMergeRows - 1) / kMergeRows);
+  const int64_t items =
+      int64_t(p.ngroups) * p.B * p.Hkv * ((p.g * p.q_len + kMergeRows - 1) / kMergeRows);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned((items + 3) / 4));
   cfg.blockDim = dim3(128);
@@ -74,7 +75,7 @@ cudaError_t gqa_decode_launch(const GqaParams& p, int grid, bool fused, cudaStre
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gqa_merge_kernel<kModePlain>, p, grid);
+  return cudaLaunchKernelEx(&cfg, gqa_merge_kernel<kModePlain>, p, p.group_ctas);
 }
 
 }  // namespace zl

@@ -199,9 +199,9 @@ struct MergeAcc {
 // (one L2 round trip per batch).
 template <int kMergePieces>
 __device__ __forceinline__ void merge_add_pieces(MergeAcc& m, const GqaParams& p,
-                                                 const TileCut& cut, int64_t U0, int c_lo,
-                                                 int c_hi, int w, int R, int row_off, int r0,
-                                                 int nrows, int lane) {
+                                                 const TileCut& cut, int cta0, int64_t U0,
+                                                 int c_lo, int c_hi, int w, int R, int row_off,
+                                                 int r0, int nrows, int lane) {
   for (int cb = c_lo; cb <= c_hi; cb += kMergePieces) {
     float lv[kMergePieces][kMergeRows];
     float4 ov[kMergePieces][kMergeRows];
@@ -212,7 +212,7 @@ __device__ __forceinline__ void merge_add_pieces(MergeAcc& m, const GqaParams& p
       const int64_t s_cc = cut.start(cc);
       use[q] = cc <= c_hi && s_cc < cut.start(cc + 1);
       const int sl = (cc == c_lo && U0 > s_cc) ? 1 : 0;
-      const int64_t base = ((int64_t(cc) * 2 + sl) * p.hpc + w) * R + row_off + r0;
+      const int64_t base = ((int64_t(cta0 + cc) * 2 + sl) * p.hpc + w) * R + row_off + r0;
 #pragma unroll
       for (int k = 0; k < kMergeRows; ++k) {
         if (use[q] && k < nrows) {
@@ -234,14 +234,14 @@ __device__ __forceinline__ void merge_add_pieces(MergeAcc& m, const GqaParams& p
 // head0) from an fp32 store of whole-unit results.
 __device__ __forceinline__ void merge_add_store(MergeAcc& m, const GqaParams& p,
                                                 const float* st_o, const float* st_lse, int b,
-                                                int head0, int r0, int nrows, int lane) {
+                                                int tok0, int head0, int r0, int nrows, int lane) {
   float lv[kMergeRows];
   float4 ov[kMergeRows];
 #pragma unroll
   for (int k = 0; k < kMergeRows; ++k) {
     if (k < nrows) {
       const int r = r0 + k;
-      const int64_t orow = (int64_t(b) * p.q_total + p.q_tok0 + r / p.g) * p.Hq + head0 + r % p.g;
+      const int64_t orow = (int64_t(b) * p.q_total + tok0 + r / p.g) * p.Hq + head0 + r % p.g;
       lv[k] = __ldcg(st_lse + orow);
       ov[k] = __ldcg(reinterpret_cast<const float4*>(st_o + orow * kGqaHeadDim) + lane);
     }
@@ -251,15 +251,17 @@ __device__ __forceinline__ void merge_add_store(MergeAcc& m, const GqaParams& p,
     if (k < nrows) m.add(k, lv[k], ov[k]);
 }
 
-// Writes the merged rows of sequence b as bf16 out and natural-log lse; a bad
-// source or a row with no weight gives zeros and lse = -inf.
+// Writes the merged rows of sequence b (rows of query tokens from tok0) as bf16
+// out and natural-log lse; a bad source or a row with no weight gives zeros
+// and lse = -inf.
 __device__ __forceinline__ void merge_write_out(const MergeAcc& m, const GqaParams& p, int b,
-                                                int head0, int r0, int nrows, int lane) {
+                                                int tok0, int head0, int r0, int nrows,
+                                                int lane) {
 #pragma unroll
   for (int k = 0; k < kMergeRows; ++k) {
     if (k < nrows) {
       const int r = r0 + k;
-      const int64_t orow = (int64_t(b) * p.q_total + p.q_tok0 + r / p.g) * p.Hq + head0 + r % p.g;
+      const int64_t orow = (int64_t(b) * p.q_total + tok0 + r / p.g) * p.Hq + head0 + r % p.g;
       const bool none = m.bad || !(m.den[k] > 0.f);
       const float inv = none ? 0.f : 1.f / m.den[k];
       uint2 packed = make_uint2(0u, 0u);
@@ -277,16 +279,16 @@ __device__ __forceinline__ void merge_write_out(const MergeAcc& m, const GqaPara
 // A plain unit (sequence b, kv head w of the CTA group, first tile U0) cut
 // between CTAs c_lo..c_hi: merge rows [r_begin, r_end) and write them.
 template <int kMergePieces>
-__device__ __forceinline__ void merge_split_rows(const GqaParams& p, const TileCut& cut,
-                                                 int64_t U0, int c_lo, int c_hi, int b, int w,
-                                                 int head0, int R, int r_begin, int r_end,
+__device__ __forceinline__ void merge_split_rows(const GqaParams& p, const TileCut& cut, int cta0,
+                                                 int64_t U0, int c_lo, int c_hi, int b, int tok0,
+                                                 int w, int head0, int R, int r_begin, int r_end,
                                                  int lane) {
   for (int r0 = r_begin; r0 < r_end; r0 += kMergeRows) {
     const int nrows = min(kMergeRows, r_end - r0);
     MergeAcc m;
     m.init();
-    merge_add_pieces<kMergePieces>(m, p, cut, U0, c_lo, c_hi, w, R, 0, r0, nrows, lane);
-    merge_write_out(m, p, b, head0, r0, nrows, lane);
+    merge_add_pieces<kMergePieces>(m, p, cut, cta0, U0, c_lo, c_hi, w, R, 0, r0, nrows, lane);
+    merge_write_out(m, p, b, tok0, head0, r0, nrows, lane);
   }
 }
 
@@ -298,7 +300,7 @@ template <int MODE>
 __device__ __forceinline__ int seq_unit_tiles(const GqaParams& p, int L) {
   const int64_t cap = p.bt_stride * int64_t(p.page_size);
   if (!(L >= 0 && int64_t(L) <= cap)) return 0;
-  const int unseen = p.q_total - p.q_tok0 - p.q_len;
+  const int unseen = p.ngroups > 1 ? 0 : p.q_total - p.q_tok0 - p.q_len;
   const int t = (L - unseen + kGqaTile - 1) / kGqaTile - (MODE == kModeShared ? p.prefix_tiles : 0);
   return t > 0 ? t : 0;
 }
@@ -403,7 +405,12 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
     griddep_launch_dependents();
   }
 
-  const int G = gridDim.x, c = blockIdx.x;
+  // This CTA's group of query tokens (tokens [tok0, tok0 + qlen)) and its
+  // place c among the group's G CTAs, which cut the tile line between them.
+  const int tg = blockIdx.x / p.group_ctas;
+  const int G = p.group_ctas, c = blockIdx.x - tg * p.group_ctas;
+  const int tok0 = p.q_tok0 + tg * p.q_len;
+  const int qlen = min(p.q_len, p.q_total - tok0);
   const int nhg = p.nhg;
   const int64_t W = int64_t(nhg) * prefix[V];
   const TileCut cut{W / G, uint32_t(W % G), uint32_t(G)};
@@ -527,21 +534,21 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
     const int L = pre ? PT * kGqaTile : p.seq_lens[b];
     const int head0 = (hg * HPC + w) * g;  // first query head of this kv head
     // m16 tile rows are (sequence b + r / rps, query token i, head head0 + j)
-    // with rps = g * q_len rows per sequence, r % rps = i * g + j; R rows per
-    // partial slot, R_act of them exist, the rest are zero. Query i (token
-    // q_tok0 + i of the q_total) sees tokens t < L - q_total + 1 + q_tok0 + i
-    // (the new tokens are in the cache; each sees itself and what precedes
-    // it); every row sees all of a shared prefix.
-    const int rps = g * p.q_len;
-    const int R = MODE == kModeShared ? p.sgs * rps : rps;
+    // with rps = g * qlen rows per sequence, r % rps = i * g + j; R rows per
+    // partial slot (the largest group's), R_act of them exist, the rest are
+    // zero. Query i (token tok0 + i of the q_total) sees tokens
+    // t < L - q_total + 1 + tok0 + i (the new tokens are in the cache; each
+    // sees itself and what precedes it); every row sees all of a shared prefix.
+    const int rps = g * qlen;
+    const int R = MODE == kModeShared ? p.sgs * rps : g * p.q_len;
     const int R_act = pre ? min(p.sgs, B - b) * rps : rps;
     const int ra = gid, rb = gid + 8;
-    const int lim0 = L - p.q_total + 1 + p.q_tok0;
+    const int lim0 = L - p.q_total + 1 + tok0;
     const int lim_a = pre ? (1 << 30) : lim0 + ra / g;
     const int lim_b = pre ? (1 << 30) : lim0 + rb / g;
     auto qrow_index = [&](int r) -> int64_t {
       const int rr = r % rps;
-      return (int64_t(b + r / rps) * p.q_total + p.q_tok0 + rr / g) * p.Hq + head0 + rr % g;
+      return (int64_t(b + r / rps) * p.q_total + tok0 + rr / g) * p.Hq + head0 + rr % g;
     };
 
     uint32_t qa[8][4];
@@ -714,7 +721,8 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
               none ? 0u : pack_bf16x2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
         if (p.lse && t4 == 0) p.lse[orow] = lse2 * 0.69314718055994531f;
       } else {
-        const int64_t wrow = ((int64_t(c) * 2 + slot) * HPC + w) * R + r;
+        // partial slots are per CTA of the whole grid (every group has its own)
+        const int64_t wrow = ((int64_t(blockIdx.x) * 2 + slot) * HPC + w) * R + r;
         float2* dst = reinterpret_cast<float2*>(p.ws_o + wrow * kGqaHeadDim);
 #pragma unroll
         for (int nt = 0; nt < 16; ++nt)
@@ -756,8 +764,8 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
     const int64_t U0 = int64_t(nhg) * prefix[b] + int64_t(hg) * n;
     int c_lo, c_hi;
     split_cta_span(cut, U0, n, c, c_lo, c_hi);
-    merge_split_rows<4>(p, cut, U0, c_lo, c_hi, b, w, (hg * HPC + w) * g, g * p.q_len, 0,
-                        g * p.q_len, lane);
+    merge_split_rows<4>(p, cut, blockIdx.x - c, U0, c_lo, c_hi, b, tok0, w, (hg * HPC + w) * g,
+                        g * p.q_len, 0, g * qlen, lane);
   }
   }
 
@@ -765,9 +773,9 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
     // Sequences with no tiles (empty or invalid length): zeros, lse = -inf.
     for (int b = c; b < B; b += G) {
       if (prefix[b + 1] != prefix[b]) continue;
-      // this launch's rows of sequence b: tokens [q_tok0, q_tok0 + q_len)
-      const int64_t rows = int64_t(p.q_len) * p.Hq;
-      const int64_t row0 = (int64_t(b) * p.q_total + p.q_tok0) * p.Hq;
+      // the group's rows of sequence b: tokens [tok0, tok0 + qlen)
+      const int64_t rows = int64_t(qlen) * p.Hq;
+      const int64_t row0 = (int64_t(b) * p.q_total + tok0) * p.Hq;
       uint4* dst = reinterpret_cast<uint4*>(p.out + row0 * kGqaHeadDim);
       const int64_t n16 = rows * kGqaHeadDim * 2 / 16;
       for (int64_t i = tid; i < n16; i += HPC * 32) dst[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -797,12 +805,18 @@ template <int MODE>
 __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ GqaParams p,
                                                         int G) {
   const int lane = threadIdx.x & 31;
-  const int rps = p.g * p.q_len;
-  const int nrb = (rps + kMergeRows - 1) / kMergeRows;
+  const int rmax = p.g * p.q_len;  // rows of a partial slot (the largest group's)
+  const int nrb = (rmax + kMergeRows - 1) / kMergeRows;
+  // items: (token group, sequence, kv head, block of kMergeRows rows)
+  const int64_t per_group = int64_t(p.B) * p.Hkv * nrb;
   const int64_t item = int64_t(blockIdx.x) * 4 + (threadIdx.x >> 5);
-  const bool live = item < int64_t(p.B) * p.Hkv * nrb;
-  const int64_t unit = live ? item / nrb : 0;  // b * Hkv + kv head
+  const bool live = item < per_group * p.ngroups;
+  const int tg = live ? int(item / per_group) : 0;
+  const int64_t gitem = item - tg * per_group;
+  const int64_t unit = live ? gitem / nrb : 0;  // b * Hkv + kv head
   const int b = int(unit / p.Hkv), kvh = int(unit % p.Hkv);
+  const int tok0 = p.q_tok0 + tg * p.q_len;
+  const int rps = p.g * min(p.q_len, p.q_total - tok0);  // this group's rows per sequence
   // Before waiting for the attention grid: the tile line, from seq_lens alone.
   // seq_lens is an input of the call; the attention grid let this kernel
   // launch only after its own dependency wait, so it is final here. Units are
@@ -824,9 +838,10 @@ __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ 
   const int n = live ? seq_unit_tiles<MODE>(p, p.seq_lens[b]) : 0;
   griddep_wait();
   griddep_launch_dependents();  // the next kernels may start their prologue
-  if (!live) return;
-  const int r0 = int(item % nrb) * kMergeRows;
+  const int r0 = int(gitem % nrb) * kMergeRows;
+  if (!live || r0 >= rps) return;
   const int nrows = min(kMergeRows, rps - r0);
+  const int cta0 = tg * G;  // the group's first CTA (G = CTAs per group)
   const int hg = kvh / p.hpc, w = kvh % p.hpc;
   const int head0 = kvh * p.g;
   const int PT = MODE == kModeShared ? p.prefix_tiles : 0;
@@ -836,7 +851,8 @@ __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ 
   const int c_lo = n ? cta_of_tile(U0, W, G) : 0, c_hi = n ? cta_of_tile(U0 + n - 1, W, G) : 0;
   if constexpr (MODE == kModePlain) {
     if (n == 0 || c_lo == c_hi) return;
-    merge_split_rows<2>(p, cut, U0, c_lo, c_hi, b, w, head0, rps, r0, r0 + nrows, lane);
+    merge_split_rows<2>(p, cut, cta0, U0, c_lo, c_hi, b, tok0, w, head0, rmax, r0, r0 + nrows,
+                        lane);
   } else {
     const int R = p.sgs * rps;  // rows of a partial slot
     MergeAcc m;
@@ -847,17 +863,18 @@ __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ 
       const int64_t P0 = int64_t(p.nhg) * (int64_t(vp) * PT) + int64_t(hg) * np;
       const int p_lo = cta_of_tile(P0, W, G), p_hi = cta_of_tile(P0 + np - 1, W, G);
       if (p_lo == p_hi)
-        merge_add_store(m, p, p.pre_o, p.pre_lse, b, head0, r0, nrows, lane);
+        merge_add_store(m, p, p.pre_o, p.pre_lse, b, tok0, head0, r0, nrows, lane);
       else
-        merge_add_pieces<2>(m, p, cut, P0, p_lo, p_hi, w, R, (b % p.sgs) * rps, r0, nrows, lane);
+        merge_add_pieces<2>(m, p, cut, cta0, P0, p_lo, p_hi, w, R, (b % p.sgs) * rps, r0, nrows,
+                            lane);
     }
     if (n > 0) {
       if (c_lo == c_hi)
-        merge_add_store(m, p, p.suf_o, p.suf_lse, b, head0, r0, nrows, lane);
+        merge_add_store(m, p, p.suf_o, p.suf_lse, b, tok0, head0, r0, nrows, lane);
       else
-        merge_add_pieces<2>(m, p, cut, U0, c_lo, c_hi, w, R, 0, r0, nrows, lane);
+        merge_add_pieces<2>(m, p, cut, cta0, U0, c_lo, c_hi, w, R, 0, r0, nrows, lane);
     }
-    merge_write_out(m, p, b, head0, r0, nrows, lane);
+    merge_write_out(m, p, b, tok0, head0, r0, nrows, lane);
   }
 }
 

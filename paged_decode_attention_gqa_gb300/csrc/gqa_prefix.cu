@@ -73,7 +73,7 @@ cudaError_t gqa_shared_launch(const GqaParams& p, int grid, cudaStream_t stream,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gqa_merge_kernel<kModeShared>, p, grid);
+  return cudaLaunchKernelEx(&cfg, gqa_merge_kernel<kModeShared>, p, p.group_ctas);
 }
 
 }  // namespace zl

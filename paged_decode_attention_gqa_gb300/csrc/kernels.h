@@ -39,10 +39,14 @@ struct GqaParams {
   float* suf_lse;
   int test_stall;      // failure-detection test hook: stall the producer until its wait runs out
   int B, q_len, Hq, Hkv, g, page_size, num_pages;
-  // Query tokens: q_len of them in this launch, tokens [q_tok0, q_tok0 + q_len)
-  // of the q_total each sequence has (q, out and lse rows are [B, q_total, Hq]).
-  // A call with g * q_total > 16 runs one launch per group of 16 / g tokens.
-  int q_total, q_tok0;
+  // Query tokens: q_total per sequence (q, out and lse rows are [B, q_total,
+  // Hq]). A launch covers ngroups groups of up to q_len tokens starting at
+  // q_tok0: CTAs [k * group_ctas, (k + 1) * group_ctas) take group k, tokens
+  // [q_tok0 + k * q_len, + q_len) (fewer in the last group), and cut the same
+  // tile line (every sequence's whole context) so that the groups read each
+  // K/V tile at about the same time. With ngroups = 1 the line ends where the
+  // group's last token stops seeing.
+  int q_total, q_tok0, ngroups, group_ctas;
   // 1: CTA c takes unit c (sequence c / nhg, head group c % nhg) whole, so no
   // unit is cut and there is nothing to merge (the host picks this for short
   // contexts, where a merge launch would cost more than the attention).

@@ -163,9 +163,11 @@ def test_token_groups_single_launch():
     assert_close(lse.double().cpu().numpy(), ref_lse, "single launch, token groups lse")
 
 
-def test_token_groups_last_row_equals_single_token_call():
-    """The last of 8 query tokens (in the second launch) sees the whole cache:
-    the same row as a q_len = 1 call with that query, bit for bit."""
+def test_token_groups_last_row_matches_single_token_call():
+    """The last of 8 query tokens (in the second group) sees the whole cache:
+    the same row as a q_len = 1 call with that query. The groups split the
+    grid's CTAs, so the cut (and the rounding order) differs from the one-token
+    call: equal within the tolerance, not bit for bit."""
     w = wl.random_case(940, B=5, Hq=32, Hkv=8, max_len=400, q_len=8)
     d = device_inputs(w)
     g = run_gpu(w, d)
@@ -173,4 +175,5 @@ def test_token_groups_last_row_equals_single_token_call():
     out1 = zl.decode_attn(q1, d["k"], d["v"], d["bt"], d["sl"], page_size=w.page_size,
                           scale=w.scale, max_seq_len=w.max_seq_len)
     torch.cuda.synchronize()
-    assert torch.equal(g.out[:, -1].view(torch.int16), out1[:, 0].view(torch.int16))
+    assert_close(g.out[:, -1].double().cpu().numpy(), out1[:, 0].double().cpu().numpy(),
+                 "last of 8 tokens vs a one-token call")
