@@ -163,10 +163,11 @@ typedef struct {
  *   Supported: D_qk = D_v = 128; Hq % Hkv == 0; g = Hq/Hkv <= 16;
  *   1 <= q_len <= 128; page_size a multiple of 16 (<= 1024); 1 <= B <= 4096.
  *   The query rows one kv head serves share a 16-row tensor-core tile: when
- *   g * q_len > 16 the call runs one attention launch (and merge) per group of
- *   16 / g query tokens, each reading the KV again; attn_begin is recorded
- *   before the first and attn_end after the last attention launch. With
- *   shared_prefix_pages > 0, g * q_len <= 16. When max_seq_len shows that
+ *   g * q_len > 16 the tokens go in groups of 16 / g, which run side by side
+ *   in one attention launch (each group reads the K/V, mostly from L2 for all
+ *   but the first); with ZL_DECODE_SINGLE_LAUNCH, one launch per group, and
+ *   attn_begin is recorded before the first and attn_end after the last.
+ *   With shared_prefix_pages > 0, g * q_len <= 16. When max_seq_len shows that
  *   every (sequence, head group) is short (at most 512 KB of K and V), each
  *   gets a CTA of its own and no merge is launched. A query row that
  *   sees no token (seq_lens[b] < q_len) gives out = 0 and lse = -inf. A bad
@@ -196,12 +197,13 @@ zl_status zl_decode_attn_mla(const zl_decode_attn_params* params, zl_stream_t st
 zl_status zl_decode_attn_workspace_size(const zl_decode_attn_params* params, size_t* bytes);
 zl_status zl_decode_attn_mla_workspace_size(const zl_decode_attn_params* params, size_t* bytes);
 
-/* Kernel launches one zl_decode_attn call with these params enqueues: per
-   group of query tokens (see zl_decode_attn), the attention kernel and, unless
-   no unit is cut (short contexts given a CTA per unit, known from max_seq_len)
-   or ZL_DECODE_SINGLE_LAUNCH merges inside it, the merge kernel. The same
-   inputs and rules as zl_decode_attn_workspace_size. (zl_decode_attn_mla
-   always enqueues two.) */
+/* Kernel launches one zl_decode_attn call with these params enqueues: the
+   attention kernel and, unless no unit is cut (short contexts given a CTA per
+   unit, known from max_seq_len) or ZL_DECODE_SINGLE_LAUNCH merges inside it,
+   the merge kernel; with ZL_DECODE_SINGLE_LAUNCH or a shared prefix, that
+   once per group of query tokens (see zl_decode_attn). The same inputs and
+   rules as zl_decode_attn_workspace_size. (zl_decode_attn_mla always
+   enqueues two.) */
 zl_status zl_decode_attn_launches(const zl_decode_attn_params* params, int32_t* launches);
 
 /*
