@@ -603,7 +603,8 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
       const uint32_t phase = (it / NS) & 1;
       const int tok0 = (MODE == kModeShared && !pre ? PT * kGqaTile : 0) + (j0 + t) * kGqaTile;
       const int valid = min(kGqaTile, L - tok0);  // tokens in the cache (V rows to keep)
-      if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag)) {
+      // every lane leaves together (the mma.sync below is warp-wide)
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full[stage]), phase, abort_flag))) {
         if (lane == 0) {
           raise_error(p.err_flags, kErrTimeout);
           *abort_flag = 1;

@@ -473,6 +473,11 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     // copied into its final place. Phase 1 (q_stage) may start as soon as
     // every QK of the previous piece is done; phase 2 (q_finish) publishes Q
     // to the MMA issuer (Q_FULL).
+    // Waits of the softmax warps end the same way on every lane (the TMEM
+    // loads and stores after them are warp-wide).
+    auto wait_all = [&](uint32_t b, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(b, parity, abort_flag));
+    };
     auto q_base = [&](int v) -> const uint4* {
       return reinterpret_cast<const uint4*>(p.q + int64_t(v) * kRows * kMlaDqk);
     };
@@ -490,7 +495,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       const uint4* qb = q_base(v);
       cp_async_wait_all();
       mbar_arrive(bar(B_Q_STAGED));  // every staged row has landed
-      if (!mbar_wait(bar(B_Q_STAGED), qn & 1, abort_flag)) return false;
+      if (!wait_all(bar(B_Q_STAGED), qn & 1)) return false;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         uint32_t r32[32];
@@ -506,7 +511,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         tmem_st32(tl + kTmemQ + 32 * i, r32);
       }
       mbar_arrive(bar(B_Q_USED));  // the staging rows are consumed
-      if (!mbar_wait(bar(B_Q_USED), qn & 1, abort_flag)) return false;
+      if (!wait_all(bar(B_Q_USED), qn & 1)) return false;
       ++qn;
       // the other latent half, straight into the swizzled operand layout
 #pragma unroll 8
@@ -577,7 +582,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         bad |= (page_cur < 0 || page_cur >= p.num_pages) ? 1 : 0;
 
         // S of this tile: TMEM -> registers, then hand the columns back
-        if (!mbar_wait(bar(B_S_FULL), it & 1, abort_flag)) { ok = false; break; }
+        if (!wait_all(bar(B_S_FULL), it & 1)) { ok = false; break; }
         tc_fence_after();
         float x[kTile];
         {
@@ -647,7 +652,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
 
         // The P tile in TMEM is free (and O stable for a rescale) once PV(it - 1)
         // finished.
-        if (it >= 1 && !mbar_wait(bar(B_PV_DONE), (it - 1) & 1, abort_flag)) { ok = false; break; }
+        if (it >= 1 && !wait_all(bar(B_PV_DONE), (it - 1) & 1)) { ok = false; break; }
         tc_fence_after();
         // tcgen05.ld/st are warp-wide: rescale when any row of the warp needs it
         // (rows that do not need it multiply by exactly 1).
@@ -672,7 +677,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       if (!ok) break;
 
       // ---- epilogue of the piece: O / l
-      if (!mbar_wait(bar(B_PV_DONE), (it - 1) & 1, abort_flag)) {
+      if (!wait_all(bar(B_PV_DONE), (it - 1) & 1)) {
         ok = false;
         break;
       }
