@@ -23,6 +23,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -119,7 +120,10 @@ class ClockSampler:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{index}.csv")
+        # the raw samples go to $ZL_CLOCKS_DIR when it is set (to keep them),
+        # else to a temporary directory
+        out_dir = os.environ.get("ZL_CLOCKS_DIR") or tempfile.mkdtemp(prefix="zl_clocks_")
+        self.path = os.path.join(out_dir, f"clocks_gpu{index}.csv")
 
     def start(self):
         try:
