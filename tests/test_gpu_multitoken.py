@@ -114,8 +114,9 @@ def test_full_size_llama3_8b_mtp_sampled():
     assert_close(g.lse64()[bs], ref_lse, "sampled lse")
 
 
-# More query rows than one tensor-core tile holds (g * q_len > 16): the call
-# runs one launch per group of 16 / g tokens, each with its own causal limits.
+# More query rows than one tensor-core tile holds (g * q_len > 16): the tokens
+# go in groups of 16 / g that run side by side in one launch (one launch per
+# group in single-launch mode), each group with its own causal limits.
 @pytest.mark.parametrize("Hq,Hkv,q_len", [
     (32, 8, 8), (32, 8, 5), (32, 8, 13),     # group of 4: 4 + 4, 4 + 1, 4 + 4 + 4 + 1
     (64, 8, 3),                              # group of 8: 2 + 1
