@@ -852,7 +852,9 @@ __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ 
   const int c_lo = n ? cta_of_tile(U0, W, G) : 0, c_hi = n ? cta_of_tile(U0 + n - 1, W, G) : 0;
   if constexpr (MODE == kModePlain) {
     if (n == 0 || c_lo == c_hi) return;
-    merge_split_rows<2>(p, cut, cta0, U0, c_lo, c_hi, b, tok0, w, head0, rmax, r0, r0 + nrows,
+    // Pieces in batches of 6: a unit cut into up to 6 pieces (2-6 at the
+    // Llama-3-8B shape) costs one round trip to L2.
+    merge_split_rows<6>(p, cut, cta0, U0, c_lo, c_hi, b, tok0, w, head0, rmax, r0, r0 + nrows,
                         lane);
   } else {
     const int R = p.sgs * rps;  // rows of a partial slot
