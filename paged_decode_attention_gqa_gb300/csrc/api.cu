@@ -85,6 +85,7 @@ struct GqaPlan {
   // shared-prefix calls: prefix tiles, sequences per group, groups
   int prefix_tiles = 0, sgs = 0, ng = 0;
   int q_group = 1;  // query tokens per launch (the call runs ceil(q_len / q_group))
+  int tg = 1;       // token groups per CTA (2: both groups of a two-group call in every CTA)
   bool unit_cut = false;  // one CTA per (sequence, head group): no cut unit, no merge
   size_t off_lse = 0, off_o = 0, off_pre_lse = 0, off_pre_o = 0;
   size_t off_suf_lse = 0, off_suf_o = 0, bytes = 0;
@@ -135,6 +136,15 @@ zl_status gqa_plan(const zl_decode_attn_params* a, GqaPlan* plan) {
   plan->hpc = zl::gqa_heads_per_cta(a->Hkv);
   plan->nhg = a->Hkv / plan->hpc;
   plan->q_group = std::min(a->q_len, 16 / plan->g);  // query tokens per launch
+  // Exactly two token groups, side by side: every CTA takes both (half the kv
+  // heads per CTA, the same number of warps), so that one shared-memory stage
+  // serves both groups and each K/V tile crosses from L2 once.
+  if ((a->q_len + plan->q_group - 1) / plan->q_group == 2 && !plan->fused &&
+      a->shared_prefix_pages == 0) {
+    plan->tg = 2;
+    plan->hpc = std::max(1, plan->hpc / 2);
+    plan->nhg = a->Hkv / plan->hpc;
+  }
   const int rps = plan->g * plan->q_group;
   if (a->shared_prefix_pages > 0) {
     plan->prefix_tiles = a->shared_prefix_pages * a->page_size / zl::kGqaTile;
@@ -148,7 +158,8 @@ zl_status gqa_plan(const zl_decode_attn_params* a, GqaPlan* plan) {
     const int per_sm =
         plan->prefix_tiles > 0
             ? zl::gqa_shared_ctas_per_sm(plan->hpc, rows_per_warp > 8, a->q_len > 1, dev.device)
-            : zl::gqa_ctas_per_sm(plan->hpc, rps > 8, a->q_len > 1, plan->fused, dev.device);
+            : zl::gqa_ctas_per_sm(plan->hpc, rps > 8, a->q_len > 1, plan->fused, plan->tg,
+                                  dev.device);
     if (per_sm < 1) return ZL_ERR_CUDA;
     grid = dev.sms * per_sm;
     if (a->max_seq_len > 0 && plan->prefix_tiles == 0) {
@@ -170,7 +181,8 @@ zl_status gqa_plan(const zl_decode_attn_params* a, GqaPlan* plan) {
     }
   }
   plan->grid = grid;
-  const size_t rows = size_t(grid) * 2 * plan->hpc * rows_per_warp;  // partial slots
+  // partial slots: 2 per (token group, CTA) pair and consumer warp
+  const size_t rows = size_t(grid) * plan->tg * 2 * plan->hpc * rows_per_warp;
   const size_t store_rows = plan->prefix_tiles > 0 ? size_t(a->B) * a->q_len * a->Hq : 0;
   // [0, off_lse): one arrival counter (8 bytes) per (sequence, kv head); then
   // the partials' lse and outputs; then (shared prefix) each query row's
@@ -397,9 +409,12 @@ zl_status zl_decode_attn(const zl_decode_attn_params* a, zl_stream_t stream) {
     p.q_tok0 = 0;
     p.q_len = plan.q_group;
     p.ngroups = ngroups;
-    p.group_ctas = plan.unit_cut ? plan.grid : std::max(1, plan.grid / ngroups);
+    p.tg = plan.tg;
+    // two groups per CTA: each group has every CTA; else the grid is split
+    p.group_ctas = plan.unit_cut || plan.tg == 2 ? plan.grid : std::max(1, plan.grid / ngroups);
+    const int launch_grid = plan.tg == 2 ? plan.grid : p.group_ctas * ngroups;
     const cudaError_t e = zl::gqa_decode_launch(
-        p, p.group_ctas * ngroups, false, s, reinterpret_cast<cudaEvent_t>(a->attn_begin),
+        p, launch_grid, false, s, reinterpret_cast<cudaEvent_t>(a->attn_begin),
         reinterpret_cast<cudaEvent_t>(a->attn_end));
     return e == cudaSuccess ? ZL_OK : ZL_ERR_CUDA;
   }
@@ -408,6 +423,7 @@ zl_status zl_decode_attn(const zl_decode_attn_params* a, zl_stream_t stream) {
   // attention launch. The launches share the workspace: each reads it only
   // after the one before has finished (programmatic dependent launches).
   p.ngroups = 1;
+  p.tg = 1;
   p.group_ctas = plan.grid;
   for (int tok0 = 0; tok0 < a->q_len; tok0 += plan.q_group) {
     p.q_tok0 = tok0;

@@ -44,9 +44,65 @@ struct Launch {
   }
 };
 
+// Two token groups per CTA: causal rows, merge launch, heads per CTA 1/2/4
+// (half of a one-group CTA's).
+template <int HPC, bool R16>
+struct TwoGroups {
+  static cudaError_t launch(const GqaParams& p, int grid, cudaStream_t stream) {
+    return launch_attn<HPC, R16, true, false, kModePlain, 2>(p, grid, stream);
+  }
+  static int ctas_per_sm(int device) {
+    return occupancy<HPC, R16, true, false, kModePlain, 2>(device);
+  }
+};
+
+cudaError_t launch_two_groups(const GqaParams& p, bool r16, int grid, cudaStream_t stream) {
+  switch (p.hpc * 2 + (r16 ? 1 : 0)) {
+    case 2: return TwoGroups<1, false>::launch(p, grid, stream);
+    case 3: return TwoGroups<1, true>::launch(p, grid, stream);
+    case 4: return TwoGroups<2, false>::launch(p, grid, stream);
+    case 5: return TwoGroups<2, true>::launch(p, grid, stream);
+    case 8: return TwoGroups<4, false>::launch(p, grid, stream);
+    case 9: return TwoGroups<4, true>::launch(p, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+int two_groups_ctas_per_sm(int hpc, bool r16, int device) {
+  switch (hpc * 2 + (r16 ? 1 : 0)) {
+    case 2: return TwoGroups<1, false>::ctas_per_sm(device);
+    case 3: return TwoGroups<1, true>::ctas_per_sm(device);
+    case 4: return TwoGroups<2, false>::ctas_per_sm(device);
+    case 5: return TwoGroups<2, true>::ctas_per_sm(device);
+    case 8: return TwoGroups<4, false>::ctas_per_sm(device);
+    case 9: return TwoGroups<4, true>::ctas_per_sm(device);
+    default: return 0;
+  }
+}
+
+// Pieces per L2 round trip in the merge: 6 (one round trip for a unit cut
+// into up to 6 pieces) when the merge grid fits in one wave at the registers
+// that takes, else 2 (twice the warps resident; a merge of every row of many
+// query tokens has thousands of warps). Both give the same bits.
+int merge_pieces(int64_t blocks) {
+  static int one_wave[kMaxDevices] = {};  // blocks of the 6-piece merge per wave
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices) return 2;
+  if (one_wave[device] == 0) {
+    int per_sm = 0, sms = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gqa_merge_kernel<kModePlain, 6>,
+                                                      128, 0) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+      return 2;
+    one_wave[device] = per_sm * sms > 0 ? per_sm * sms : 1;
+  }
+  return blocks <= one_wave[device] ? 6 : 2;
+}
+
 }  // namespace
 
-int gqa_ctas_per_sm(int hpc, bool rows16, bool causal, bool fused, int device) {
+int gqa_ctas_per_sm(int hpc, bool rows16, bool causal, bool fused, int tg, int device) {
+  if (tg == 2) return causal && !fused ? two_groups_ctas_per_sm(hpc, rows16, device) : 0;
   return dispatch<Occupancy>(hpc, rows16, causal, fused, device);
 }
 
@@ -57,7 +113,12 @@ cudaError_t gqa_decode_launch(const GqaParams& p, int grid, bool fused, cudaStre
   const bool r16 = p.g * p.q_len > 8;
   const bool known = p.hpc == 1 || p.hpc == 2 || p.hpc == 4 || p.hpc == 8;
   if (!known) return cudaErrorInvalidValue;
-  e = dispatch<Launch>(p.hpc, r16, p.q_total > 1, fused, &p, grid, stream);
+  if (p.tg == 2) {
+    if (fused || p.q_total < 2) return cudaErrorInvalidValue;
+    e = launch_two_groups(p, r16, grid, stream);
+  } else {
+    e = dispatch<Launch>(p.hpc, r16, p.q_total > 1, fused, &p, grid, stream);
+  }
   if (e != cudaSuccess) return e;
   if (attn_end && (e = cudaEventRecord(attn_end, stream)) != cudaSuccess) return e;
   if (fused || p.unit_cut) return cudaSuccess;  // nothing left to merge
@@ -65,8 +126,9 @@ cudaError_t gqa_decode_launch(const GqaParams& p, int grid, bool fused, cudaStre
   // before the attention grid ends and wait in griddepcontrol.wait.
   const int64_t items =
       int64_t(p.ngroups) * p.B * p.Hkv * ((p.g * p.q_len + kMergeRows - 1) / kMergeRows);
+  const int64_t blocks = (items + 3) / 4;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned((items + 3) / 4));
+  cfg.gridDim = dim3(unsigned(blocks));
   cfg.blockDim = dim3(128);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
@@ -75,7 +137,9 @@ cudaError_t gqa_decode_launch(const GqaParams& p, int grid, bool fused, cudaStre
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gqa_merge_kernel<kModePlain>, p, p.group_ctas);
+  return merge_pieces(blocks) == 6
+             ? cudaLaunchKernelEx(&cfg, gqa_merge_kernel<kModePlain, 6>, p, p.group_ctas)
+             : cudaLaunchKernelEx(&cfg, gqa_merge_kernel<kModePlain, 2>, p, p.group_ctas);
 }
 
 }  // namespace zl

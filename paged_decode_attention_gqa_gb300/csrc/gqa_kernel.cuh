@@ -54,16 +54,21 @@ constexpr int kModePlain = 0;   // every sequence over all of its own pages
 constexpr int kModeShared = 1;
 constexpr uint64_t kTestStallNs = 50ull * 1000 * 1000;  // bound of the test-hook wait
 
-template <int HPC>
+template <int HPC, int TG = 1>
 struct GqaCfg {
   static constexpr int kHalfBytes = HPC * kGqaTile * 64 * 2;  // one 64-column half of K or V
   static constexpr int kStageBytes = 4 * kHalfBytes;           // K lo | K hi | V lo | V hi
-  static constexpr int kStages = HPC == 8 ? 3 : HPC == 4 ? 4 : HPC == 2 ? 6 : 8;
-  static constexpr int kThreads = (HPC + 1) * 32;
+  // Two token groups per CTA (half the heads of a one-group CTA, the same
+  // warps): 192 KB of stages in flight, as at HPC = 8.
+  static constexpr int kStages =
+      TG > 1 ? 192 * 1024 / kStageBytes : HPC == 8 ? 3 : HPC == 4 ? 4 : HPC == 2 ? 6 : 8;
+  static constexpr int kConsumers = HPC * TG;  // consumer warps
+  static constexpr int kThreads = (kConsumers + 1) * 32;
   // 1 KB alignment slack + stages + barriers + per-stage flags + abort flag + prefix table
   // + split-piece records (2 per consumer warp)
   static constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStageBytes + kStages * 16 +
-                                       kStages * 4 + 16 + (kMaxBatch + 1) * 4 + HPC * 2 * 4;
+                                       kStages * 4 + 16 + (kMaxBatch + 1) * 4 +
+                                       kConsumers * 2 * 4;
 };
 
 __device__ __forceinline__ void raise_error(uint32_t* flags, uint32_t bits) {
@@ -305,11 +310,13 @@ __device__ __forceinline__ int seq_unit_tiles(const GqaParams& p, int L) {
   return t > 0 ? t : 0;
 }
 
-template <int HPC, bool ROWS16, bool CAUSAL, bool FUSED, int MODE = kModePlain>
-__global__ void __launch_bounds__(GqaCfg<HPC>::kThreads, 1)
+template <int HPC, bool ROWS16, bool CAUSAL, bool FUSED, int MODE = kModePlain, int TG = 1>
+__global__ void __launch_bounds__(GqaCfg<HPC, TG>::kThreads, 1)
 gqa_decode_kernel(const __grid_constant__ GqaParams p) {
   static_assert(MODE == kModePlain || !FUSED, "the in-kernel merge is for plain launches");
-  using Cfg = GqaCfg<HPC>;
+  static_assert(TG == 1 || (MODE == kModePlain && !FUSED && CAUSAL),
+                "two token groups per CTA: plain launches of multi-token calls");
+  using Cfg = GqaCfg<HPC, TG>;
   constexpr int NS = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -329,12 +336,12 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), HPC);
+      mbar_init(smem_u32(&empty[s]), Cfg::kConsumers);
     }
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == HPC && lane == 0) {
+  if (warp == Cfg::kConsumers && lane == 0) {
     tma_prefetch_desc(&p.tmap_k);
     tma_prefetch_desc(&p.tmap_v);
   }
@@ -405,10 +412,15 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
     griddep_launch_dependents();
   }
 
-  // This CTA's group of query tokens (tokens [tok0, tok0 + qlen)) and its
-  // place c among the group's G CTAs, which cut the tile line between them.
-  const int tg = blockIdx.x / p.group_ctas;
-  const int G = p.group_ctas, c = blockIdx.x - tg * p.group_ctas;
+  // This warp's group of query tokens (tokens [tok0, tok0 + qlen)) and the
+  // CTA's place c among the group's G CTAs, which cut the tile line between
+  // them. One group per CTA: CTAs [tg G, (tg + 1) G) take group tg. Two per
+  // CTA: every CTA takes both, consumer warp w group w / HPC. Either way
+  // vcta = tg G + c numbers the (group, CTA) pairs for the partial slots.
+  const int tg = TG > 1 ? min(warp / HPC, TG - 1) : int(blockIdx.x) / p.group_ctas;
+  const int G = TG > 1 ? int(gridDim.x) : p.group_ctas;
+  const int c = TG > 1 ? int(blockIdx.x) : int(blockIdx.x) - tg * p.group_ctas;
+  const int vcta = tg * G + c;
   const int tok0 = p.q_tok0 + tg * p.q_len;
   const int qlen = min(p.q_len, p.q_total - tok0);
   const int nhg = p.nhg;
@@ -426,7 +438,7 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
     }
   }
 
-  if (warp == HPC) {
+  if (warp == Cfg::kConsumers) {
     // ------------------------------------------------------------ producer
     if (p.test_stall) {
       // Failure-detection test hook: wait on a word nothing sets until the
@@ -508,7 +520,7 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
   }
 
   // -------------------------------------------------------------- consumers
-  const int w = warp;                 // kv head within the group
+  const int w = TG > 1 ? warp % HPC : warp;  // kv head within the CTA's head group
   const int gid = lane >> 2, t4 = lane & 3;
   const int g = p.g;
   const float scale_log2 = p.scale_log2;
@@ -722,8 +734,8 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
               none ? 0u : pack_bf16x2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
         if (p.lse && t4 == 0) p.lse[orow] = lse2 * 0.69314718055994531f;
       } else {
-        // partial slots are per CTA of the whole grid (every group has its own)
-        const int64_t wrow = ((int64_t(blockIdx.x) * 2 + slot) * HPC + w) * R + r;
+        // partial slots are per (token group, CTA) pair: every group has its own
+        const int64_t wrow = ((int64_t(vcta) * 2 + slot) * HPC + w) * R + r;
         float2* dst = reinterpret_cast<float2*>(p.ws_o + wrow * kGqaHeadDim);
 #pragma unroll
         for (int nt = 0; nt < 16; ++nt)
@@ -765,23 +777,26 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
     const int64_t U0 = int64_t(nhg) * prefix[b] + int64_t(hg) * n;
     int c_lo, c_hi;
     split_cta_span(cut, U0, n, c, c_lo, c_hi);
-    merge_split_rows<4>(p, cut, blockIdx.x - c, U0, c_lo, c_hi, b, tok0, w, (hg * HPC + w) * g,
+    merge_split_rows<4>(p, cut, vcta - c, U0, c_lo, c_hi, b, tok0, w, (hg * HPC + w) * g,
                         g * p.q_len, 0, g * qlen, lane);
   }
   }
 
   if constexpr (MODE == kModePlain) {
-    // Sequences with no tiles (empty or invalid length): zeros, lse = -inf.
+    // Sequences with no tiles (empty or invalid length): zeros, lse = -inf,
+    // for the rows of the CTA's groups of sequence b: tokens [ztok0, + zlen).
+    const int ztok0 = TG > 1 ? p.q_tok0 : tok0;
+    const int zlen = TG > 1 ? min(TG * p.q_len, p.q_total - p.q_tok0) : qlen;
+    constexpr int kStride = Cfg::kConsumers * 32;  // the consumer threads
     for (int b = c; b < B; b += G) {
       if (prefix[b + 1] != prefix[b]) continue;
-      // the group's rows of sequence b: tokens [tok0, tok0 + qlen)
-      const int64_t rows = int64_t(qlen) * p.Hq;
-      const int64_t row0 = (int64_t(b) * p.q_total + tok0) * p.Hq;
+      const int64_t rows = int64_t(zlen) * p.Hq;
+      const int64_t row0 = (int64_t(b) * p.q_total + ztok0) * p.Hq;
       uint4* dst = reinterpret_cast<uint4*>(p.out + row0 * kGqaHeadDim);
       const int64_t n16 = rows * kGqaHeadDim * 2 / 16;
-      for (int64_t i = tid; i < n16; i += HPC * 32) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+      for (int64_t i = tid; i < n16; i += kStride) dst[i] = make_uint4(0u, 0u, 0u, 0u);
       if (p.lse)
-        for (int64_t i = tid; i < rows; i += HPC * 32) p.lse[row0 + i] = -CUDART_INF_F;
+        for (int64_t i = tid; i < rows; i += kStride) p.lse[row0 + i] = -CUDART_INF_F;
     }
   }
 }
@@ -802,7 +817,7 @@ __device__ __forceinline__ int cta_of_tile(int64_t x, int64_t W, int G) {
 // Launched as a programmatic dependent of the attention kernel: it may start
 // early and waits here until that grid has finished and its writes are
 // visible.
-template <int MODE>
+template <int MODE, int PIECES = 2>
 __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ GqaParams p,
                                                         int G) {
   const int lane = threadIdx.x & 31;
@@ -852,10 +867,10 @@ __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ 
   const int c_lo = n ? cta_of_tile(U0, W, G) : 0, c_hi = n ? cta_of_tile(U0 + n - 1, W, G) : 0;
   if constexpr (MODE == kModePlain) {
     if (n == 0 || c_lo == c_hi) return;
-    // Pieces in batches of 6: a unit cut into up to 6 pieces (2-6 at the
-    // Llama-3-8B shape) costs one round trip to L2.
-    merge_split_rows<6>(p, cut, cta0, U0, c_lo, c_hi, b, tok0, w, head0, rmax, r0, r0 + nrows,
-                        lane);
+    // PIECES pieces per round trip to L2 (the host takes 6 when the merge grid
+    // fits in one wave at the registers that needs, else 2).
+    merge_split_rows<PIECES>(p, cut, cta0, U0, c_lo, c_hi, b, tok0, w, head0, rmax, r0,
+                             r0 + nrows, lane);
   } else {
     const int R = p.sgs * rps;  // rows of a partial slot
     MergeAcc m;
@@ -884,24 +899,24 @@ __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ 
 constexpr int kMaxDevices = 64;
 
 // Raise the dynamic shared-memory limit of one kernel instance, once per device.
-template <int HPC, bool R16, bool C, bool U, int MODE = kModePlain>
+template <int HPC, bool R16, bool C, bool U, int MODE = kModePlain, int TG = 1>
 cudaError_t configure(int device) {
   static bool done[kMaxDevices] = {};
   if (device >= 0 && device < kMaxDevices && done[device]) return cudaSuccess;
-  const cudaError_t e = cudaFuncSetAttribute(gqa_decode_kernel<HPC, R16, C, U, MODE>,
+  const cudaError_t e = cudaFuncSetAttribute(gqa_decode_kernel<HPC, R16, C, U, MODE, TG>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             int(GqaCfg<HPC>::kSmemBytes));
+                                             int(GqaCfg<HPC, TG>::kSmemBytes));
   if (e == cudaSuccess && device >= 0 && device < kMaxDevices) done[device] = true;
   return e;
 }
 
-template <int HPC, bool R16, bool C, bool U, int MODE = kModePlain>
+template <int HPC, bool R16, bool C, bool U, int MODE = kModePlain, int TG = 1>
 cudaError_t launch_attn(const GqaParams& p, int grid, cudaStream_t stream) {
-  using Cfg = GqaCfg<HPC>;
+  using Cfg = GqaCfg<HPC, TG>;
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
-  if ((e = configure<HPC, R16, C, U, MODE>(device)) != cudaSuccess) return e;
+  if ((e = configure<HPC, R16, C, U, MODE, TG>(device)) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(grid));
   cfg.blockDim = dim3(Cfg::kThreads);
@@ -912,19 +927,20 @@ cudaError_t launch_attn(const GqaParams& p, int grid, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gqa_decode_kernel<HPC, R16, C, U, MODE>, p);
+  return cudaLaunchKernelEx(&cfg, gqa_decode_kernel<HPC, R16, C, U, MODE, TG>, p);
 }
 
-template <int HPC, bool R16, bool C, bool U, int MODE = kModePlain>
+template <int HPC, bool R16, bool C, bool U, int MODE = kModePlain, int TG = 1>
 int occupancy(int device) {
-  using Cfg = GqaCfg<HPC>;
+  using Cfg = GqaCfg<HPC, TG>;
   // Queried once per device (it does not change), not on every call.
   static int cached[kMaxDevices] = {};
   if (device >= 0 && device < kMaxDevices && cached[device] > 0) return cached[device];
-  if (configure<HPC, R16, C, U, MODE>(device) != cudaSuccess) return 0;
+  if (configure<HPC, R16, C, U, MODE, TG>(device) != cudaSuccess) return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_decode_kernel<HPC, R16, C, U, MODE>,
-                                                    Cfg::kThreads, Cfg::kSmemBytes) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          &n, gqa_decode_kernel<HPC, R16, C, U, MODE, TG>, Cfg::kThreads, Cfg::kSmemBytes) !=
+      cudaSuccess)
     return 0;
   if (device >= 0 && device < kMaxDevices) cached[device] = n;
   return n;

@@ -47,6 +47,11 @@ struct GqaParams {
   // K/V tile at about the same time. With ngroups = 1 the line ends where the
   // group's last token stops seeing.
   int q_total, q_tok0, ngroups, group_ctas;
+  // Token groups per CTA (1 or 2). With 2, every CTA takes both groups of a
+  // two-group launch (consumer warp w: kv head w % hpc, group w / hpc), so a
+  // K/V stage serves both; group_ctas is then the whole grid, and group k's
+  // CTA c is counted as CTA k * group_ctas + c for its partial slots.
+  int tg;
   // 1: CTA c takes unit c (sequence c / nhg, head group c % nhg) whole, so no
   // unit is cut and there is nothing to merge (the host picks this for short
   // contexts, where a merge launch would cost more than the attention).
@@ -91,7 +96,7 @@ cudaError_t mla_decode_launch(const MlaParams& p, int clusters, cudaStream_t str
 // kv heads handled by one CTA for this Hkv (largest of 8, 4, 2, 1 dividing it).
 int gqa_heads_per_cta(int Hkv);
 // CTAs of the attention kernel that fit on one SM (0 on error).
-int gqa_ctas_per_sm(int hpc, bool rows16, bool causal, bool fused, int device);
+int gqa_ctas_per_sm(int hpc, bool rows16, bool causal, bool fused, int tg, int device);
 // Shared-prefix decode: CTAs per SM of its attention kernel, and its two
 // launches (attention over prefix groups and suffixes, then the merge).
 int gqa_shared_ctas_per_sm(int hpc, bool rows16, bool causal, int device);

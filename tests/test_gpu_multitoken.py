@@ -116,12 +116,16 @@ def test_full_size_llama3_8b_mtp_sampled():
 
 # More query rows than one tensor-core tile holds (g * q_len > 16): the tokens
 # go in groups of 16 / g that run side by side in one launch (one launch per
-# group in single-launch mode), each group with its own causal limits.
+# group in single-launch mode), each group with its own causal limits. Two
+# groups run in every CTA (half the kv heads per CTA); more groups split the
+# grid's CTAs between them.
 @pytest.mark.parametrize("Hq,Hkv,q_len", [
     (32, 8, 8), (32, 8, 5), (32, 8, 13),     # group of 4: 4 + 4, 4 + 1, 4 + 4 + 4 + 1
     (64, 8, 3),                              # group of 8: 2 + 1
-    (128, 8, 2),                             # group of 16: one token per launch
+    (128, 8, 2),                             # group of 16: one token per group
     (16, 8, 17),                             # group of 2: 8 + 8 + 1
+    (8, 1, 3),                               # one kv head (1 per CTA): 2 + 1
+    (16, 4, 5),                              # four kv heads (2 per CTA): 4 + 1
 ])
 def test_token_groups(Hq, Hkv, q_len):
     w = wl.random_case(900 + 31 * Hq + 7 * Hkv + q_len, B=5, Hq=Hq, Hkv=Hkv, max_len=300,
@@ -166,9 +170,10 @@ def test_token_groups_single_launch():
 
 def test_token_groups_last_row_matches_single_token_call():
     """The last of 8 query tokens (in the second group) sees the whole cache:
-    the same row as a q_len = 1 call with that query. The groups split the
-    grid's CTAs, so the cut (and the rounding order) differs from the one-token
-    call: equal within the tolerance, not bit for bit."""
+    the same row as a q_len = 1 call with that query. The two-group launch
+    cuts the tile line with its own plan (half the kv heads per CTA), so the
+    rounding order differs from the one-token call: equal within the
+    tolerance, not bit for bit."""
     w = wl.random_case(940, B=5, Hq=32, Hkv=8, max_len=400, q_len=8)
     d = device_inputs(w)
     g = run_gpu(w, d)
