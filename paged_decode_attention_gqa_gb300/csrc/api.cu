@@ -91,8 +91,8 @@ struct GqaPlan {
   size_t off_suf_lse = 0, off_suf_o = 0, bytes = 0;
 };
 
-// Query tokens per sequence one call takes (the GQA path runs ceil(q_len /
-// (16 / g)) launches for them).
+// Query tokens per sequence one call takes (the GQA path takes them in
+// ceil(q_len / (16 / g)) groups, side by side in one launch).
 constexpr int kMaxQueryTokens = 128;
 // A call whose longest (sequence, head group) unit has at most this many K and
 // V bytes (known from max_seq_len) gives each unit a CTA of its own and skips
@@ -112,9 +112,9 @@ zl_status gqa_validate_shape(const zl_decode_attn_params* a) {
   if (!(a->scale > 0.f) || !std::isfinite(a->scale)) return ZL_ERR_INVALID_ARG;
   if (a->D_qk != zl::kGqaHeadDim || a->D_v != zl::kGqaHeadDim) return ZL_ERR_UNSUPPORTED;
   // (query token, head) rows of one kv head share an m16 tile: at most 16 per
-  // launch, so g <= 16; a call with g * q_len > 16 runs one launch per group
-  // of 16 / g query tokens (each group reads the KV again). A shared-prefix
-  // call keeps all its tokens in one launch.
+  // group, so g <= 16; a call with g * q_len > 16 takes its query tokens in
+  // groups of 16 / g (side by side in one launch; one launch per group in
+  // single-launch mode). A shared-prefix call keeps all its tokens in one group.
   if (a->Hq / a->Hkv > 16 || a->q_len > kMaxQueryTokens) return ZL_ERR_UNSUPPORTED;
   if (a->shared_prefix_pages > 0 && a->Hq / a->Hkv * a->q_len > 16) return ZL_ERR_UNSUPPORTED;
   if (a->page_size % zl::kGqaTile != 0 || a->page_size > 1024) return ZL_ERR_UNSUPPORTED;

@@ -23,8 +23,9 @@ struct GqaParams {
   const int32_t* seq_lens;
   int64_t bt_stride;
   unsigned long long* ws_count;  // [B * Hkv] arrivals per split unit: epoch << 32 | count
-  float* ws_o;         // [G][2][HPC][g * q_len][128] normalised partial outputs
-  float* ws_lse;       // [G][2][HPC][g * q_len] base-2 lse of the partials (NaN = bad piece)
+  // Partial slots: [(token group, CTA) pairs][2][HPC][g * q_len], pair k * group_ctas + c
+  float* ws_o;         // [..][128] normalised partial outputs
+  float* ws_lse;       // base-2 lse of the partials (NaN = bad piece)
   uint32_t* err_flags; // or nullptr
   uint32_t epoch;      // nonzero, different for every host call
   // Shared-prefix decode (zero otherwise): the first prefix_tiles tiles of
