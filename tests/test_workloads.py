@@ -78,3 +78,32 @@ def test_random_case_structure():
                        h.k_pool.permute(0, 2, 1, 3).contiguous().view(torch.int16))
     m = wl.random_case(8, B=2, Hq=16, Hkv=1, D=576, D_v=512, mla=True, page_size=64)
     assert m.mla and m.v_pool is None and m.k_pool.shape[1:] == (64, 1, 576)
+
+
+def _bench_module():
+    import importlib.util
+    import os
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "bench.py")
+    spec = importlib.util.spec_from_file_location("zl_bench", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def test_roofline_bytes_count_shared_pages_once():
+    """bench.py's roofline bytes: distinct (page, slot) rows, checked against a
+    plain loop; equal to the logical bytes when no page is shared."""
+    bench = _bench_module()
+    for name in ("tiny_gqa", "llama70b_prefix_decode"):
+        w = wl.WORKLOADS[name]()
+        seen = set()
+        for b in range(w.B):
+            L = int(w.seq_lens[b])
+            for t in range(L):
+                seen.add((int(w.block_table[b, t // w.page_size]), t % w.page_size))
+        want = len(seen) * w.Hkv * 2 * w.D_qk * 2
+        assert bench.unique_kv_bytes(w) == want
+        if name == "tiny_gqa":
+            assert want == bench.kv_bytes(w)
+        else:
+            assert want < bench.kv_bytes(w) / 4  # the 2048-token prefix is shared by 128
