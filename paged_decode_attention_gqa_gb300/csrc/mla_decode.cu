@@ -754,9 +754,12 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
 
 // One warp per (unit, head) row of a unit cut between clusters: log-sum-exp
 // merge of its normalised partials, in cluster order. The loads of a batch of
-// up to four partials (split bounds, lse, rows) are independent, so a warp
-// waits on memory about twice per batch. A programmatic dependent launch of the
-// attention kernel: it waits here until that grid is done.
+// up to three partials (split bounds, lse, rows) are independent, so a warp
+// waits on memory about twice per batch. Three covers the 2-3 pieces a unit
+// usually has, at 78 registers: the merge's one warp per row runs in several
+// waves, and four (94 registers, fewer warps resident) was 1.4 us slower per
+// step. A programmatic dependent launch of the attention kernel: it waits here
+// until that grid is done.
 __global__ void __launch_bounds__(128) mla_merge_kernel(const __grid_constant__ MlaParams p,
                                                         int NC) {
   griddep_wait();
@@ -772,7 +775,7 @@ __global__ void __launch_bounds__(128) mla_merge_kernel(const __grid_constant__ 
   // (always in range unless the attention kernel gave up early, which it
   // reports through err_flags; the check keeps every read in bounds)
   if (span.x < 0 || c_lo == c_hi || c_hi >= NC || c_lo > c_hi) return;
-  constexpr int kBatch = 4;
+  constexpr int kBatch = 3;
   float M = -CUDART_INF_F, den = 0.f, acc[16] = {};
   bool bad = false;
   for (int c0 = c_lo; c0 <= c_hi; c0 += kBatch) {
