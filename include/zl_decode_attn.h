@@ -160,14 +160,16 @@ typedef struct {
 
 /*
  * GQA / MHA / MQA decode over separate K and V pools.
- *   Supported: D_qk = D_v = 128; Hq % Hkv == 0; g = Hq/Hkv <= 16;
+ *   Supported: D_qk = D_v = 128; Hq % Hkv == 0; g = Hq/Hkv <= 128;
  *   1 <= q_len <= 128; page_size a multiple of 16 (<= 1024); 1 <= B <= 4096.
- *   The query rows one kv head serves share a 16-row tensor-core tile: when
- *   g * q_len > 16 the tokens go in groups of 16 / g, which run side by side
- *   in one attention launch (two groups share every CTA and each K/V tile;
- *   with more, each group reads the K/V, mostly from L2 for all but the
- *   first); with ZL_DECODE_SINGLE_LAUNCH, one launch per group, and
- *   attn_begin is recorded before the first and attn_end after the last.
+ *   The (query token, head) rows one kv head serves go in row groups of at
+ *   most 16, one 16-row tensor-core tile: when g * q_len > 16 the tokens go in
+ *   groups of 16 / g, and when g > 16 each token's g heads go in ceil(g / 16)
+ *   chunks (MQA with many query heads). The groups run side by side in one
+ *   attention launch (two groups share every CTA and each K/V tile; with
+ *   more, each group reads the K/V, mostly from L2 for all but the first);
+ *   with ZL_DECODE_SINGLE_LAUNCH, one launch per group, and attn_begin is
+ *   recorded before the first and attn_end after the last.
  *   With shared_prefix_pages > 0, g * q_len <= 16. When max_seq_len shows that
  *   every (sequence, head group) is short (at most 512 KB of K and V), each
  *   gets a CTA of its own and no merge is launched. A query row that

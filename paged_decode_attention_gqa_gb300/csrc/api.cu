@@ -84,16 +84,19 @@ struct GqaPlan {
   bool fused = false;
   // shared-prefix calls: prefix tiles, sequences per group, groups
   int prefix_tiles = 0, sgs = 0, ng = 0;
-  int q_group = 1;  // query tokens per launch (the call runs ceil(q_len / q_group))
+  int q_group = 1;  // query tokens per row group
+  int gh = 0, hchunks = 1;  // query heads per row group, head chunks per kv head
+  int ngroups = 1;          // row groups: ceil(q_len / q_group) x hchunks
   int tg = 1;       // token groups per CTA (2: both groups of a two-group call in every CTA)
   bool unit_cut = false;  // one CTA per (sequence, head group): no cut unit, no merge
   size_t off_lse = 0, off_o = 0, off_pre_lse = 0, off_pre_o = 0;
   size_t off_suf_lse = 0, off_suf_o = 0, bytes = 0;
 };
 
-// Query tokens per sequence one call takes (the GQA path takes them in
-// ceil(q_len / (16 / g)) groups, side by side in one launch).
+// Query tokens per sequence one call takes, and query heads per kv head (the
+// GQA path takes the (token, head) rows of a kv head in groups of at most 16).
 constexpr int kMaxQueryTokens = 128;
+constexpr int kMaxGroupHeads = 128;
 // A call whose longest (sequence, head group) unit has at most this many K and
 // V bytes (known from max_seq_len) gives each unit a CTA of its own and skips
 // the merge: one CTA streams that in about the time a merge launch takes.
@@ -112,10 +115,11 @@ zl_status gqa_validate_shape(const zl_decode_attn_params* a) {
   if (!(a->scale > 0.f) || !std::isfinite(a->scale)) return ZL_ERR_INVALID_ARG;
   if (a->D_qk != zl::kGqaHeadDim || a->D_v != zl::kGqaHeadDim) return ZL_ERR_UNSUPPORTED;
   // (query token, head) rows of one kv head share an m16 tile: at most 16 per
-  // group, so g <= 16; a call with g * q_len > 16 takes its query tokens in
-  // groups of 16 / g (side by side in one launch; one launch per group in
-  // single-launch mode). A shared-prefix call keeps all its tokens in one group.
-  if (a->Hq / a->Hkv > 16 || a->q_len > kMaxQueryTokens) return ZL_ERR_UNSUPPORTED;
+  // row group. A call with g * q_len > 16 takes its query tokens in groups of
+  // 16 / g, or with g > 16 each token's heads in ceil(g / 16) chunks (side by
+  // side in one launch; one launch per group in single-launch mode). A
+  // shared-prefix call keeps all its rows in one group.
+  if (a->Hq / a->Hkv > kMaxGroupHeads || a->q_len > kMaxQueryTokens) return ZL_ERR_UNSUPPORTED;
   if (a->shared_prefix_pages > 0 && a->Hq / a->Hkv * a->q_len > 16) return ZL_ERR_UNSUPPORTED;
   if (a->page_size % zl::kGqaTile != 0 || a->page_size > 1024) return ZL_ERR_UNSUPPORTED;
   if (a->B > zl::kMaxBatch) return ZL_ERR_UNSUPPORTED;
@@ -135,17 +139,25 @@ zl_status gqa_plan(const zl_decode_attn_params* a, GqaPlan* plan) {
   plan->fused = (a->flags & ZL_DECODE_SINGLE_LAUNCH) != 0;
   plan->hpc = zl::gqa_heads_per_cta(a->Hkv);
   plan->nhg = a->Hkv / plan->hpc;
-  plan->q_group = std::min(a->q_len, 16 / plan->g);  // query tokens per launch
-  // Exactly two token groups, side by side: every CTA takes both (half the kv
+  if (plan->g <= 16) {  // every head of a token in one group
+    plan->gh = plan->g;
+    plan->hchunks = 1;
+    plan->q_group = std::min(a->q_len, 16 / plan->g);
+  } else {  // one token per group, its heads in chunks of at most 16
+    plan->hchunks = (plan->g + 15) / 16;
+    plan->gh = (plan->g + plan->hchunks - 1) / plan->hchunks;
+    plan->q_group = 1;
+  }
+  plan->ngroups = (a->q_len + plan->q_group - 1) / plan->q_group * plan->hchunks;
+  // Exactly two row groups, side by side: every CTA takes both (half the kv
   // heads per CTA, the same number of warps), so that one shared-memory stage
   // serves both groups and each K/V tile crosses from L2 once.
-  if ((a->q_len + plan->q_group - 1) / plan->q_group == 2 && !plan->fused &&
-      a->shared_prefix_pages == 0) {
+  if (plan->ngroups == 2 && !plan->fused && a->shared_prefix_pages == 0) {
     plan->tg = 2;
     plan->hpc = std::max(1, plan->hpc / 2);
     plan->nhg = a->Hkv / plan->hpc;
   }
-  const int rps = plan->g * plan->q_group;
+  const int rps = plan->gh * plan->q_group;
   if (a->shared_prefix_pages > 0) {
     plan->prefix_tiles = a->shared_prefix_pages * a->page_size / zl::kGqaTile;
     plan->sgs = 16 / rps > 0 ? 16 / rps : 1;
@@ -202,8 +214,8 @@ zl_status gqa_plan(const zl_decode_attn_params* a, GqaPlan* plan) {
 // A call with several groups of query tokens runs them in one launch, side by
 // side, unless it merges inside the attention kernel (its arrival counters
 // are per sequence and kv head) or has a shared prefix (one group only).
-bool groups_together(const GqaPlan& plan, int q_len) {
-  return plan.q_group < q_len && !plan.fused && plan.prefix_tiles == 0;
+bool groups_together(const GqaPlan& plan) {
+  return plan.ngroups > 1 && !plan.fused && plan.prefix_tiles == 0;
 }
 
 // ------------------------------------------------------------------ MLA plan
@@ -349,8 +361,7 @@ zl_status zl_decode_attn_launches(const zl_decode_attn_params* a, int32_t* launc
   const zl_status st = gqa_plan(a, &plan);
   if (st != ZL_OK) return st;
   const int per_launch = (plan.fused || plan.unit_cut) ? 1 : 2;
-  const int groups = (a->q_len + plan.q_group - 1) / plan.q_group;
-  *launches = groups_together(plan, a->q_len) ? per_launch : groups * per_launch;
+  *launches = groups_together(plan) ? per_launch : plan.ngroups * per_launch;
   return ZL_OK;
 }
 
@@ -386,6 +397,9 @@ zl_status zl_decode_attn(const zl_decode_attn_params* a, zl_stream_t stream) {
   p.Hq = a->Hq;
   p.Hkv = a->Hkv;
   p.g = plan.g;
+  p.gh = plan.gh;
+  p.hchunks = plan.hchunks;
+  p.hc0 = 0;
   p.page_size = a->page_size;
   p.num_pages = a->num_pages;
   p.hpc = plan.hpc;
@@ -400,12 +414,13 @@ zl_status zl_decode_attn(const zl_decode_attn_params* a, zl_stream_t stream) {
   p.suf_o = reinterpret_cast<float*>(ws + plan.off_suf_o);
 
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const int ngroups = (a->q_len + plan.q_group - 1) / plan.q_group;
-  if (groups_together(plan, a->q_len)) {
-    // Every group of q_group query tokens in one launch, side by side: the
-    // grid's CTAs are split between the groups, and each group cuts the same
-    // tile line, so the groups read each K/V tile at about the same time (the
-    // second read is served by L2). One merge launch covers every group.
+  const int ngroups = plan.ngroups;
+  if (groups_together(plan)) {
+    // Every row group (q_group query tokens, gh heads of each kv head) in one
+    // launch, side by side: two share every CTA; more split the grid's CTAs
+    // between them, and each cuts the same tile line, so the groups read each
+    // K/V tile at about the same time (all but the first read are served by
+    // L2). One merge launch covers every group.
     p.q_tok0 = 0;
     p.q_len = plan.q_group;
     p.ngroups = ngroups;
@@ -418,18 +433,21 @@ zl_status zl_decode_attn(const zl_decode_attn_params* a, zl_stream_t stream) {
         reinterpret_cast<cudaEvent_t>(a->attn_end));
     return e == cudaSuccess ? ZL_OK : ZL_ERR_CUDA;
   }
-  // One launch (attention, then its merge) per group of q_group query tokens;
-  // attn_begin is recorded before the first, attn_end after the last
-  // attention launch. The launches share the workspace: each reads it only
-  // after the one before has finished (programmatic dependent launches).
+  // One launch (attention, then its merge) per row group: group gg is query
+  // tokens from (gg / hchunks) * q_group, head chunk gg % hchunks. attn_begin
+  // is recorded before the first, attn_end after the last attention launch.
+  // The launches share the workspace: each reads it only after the one before
+  // has finished (programmatic dependent launches).
   p.ngroups = 1;
   p.tg = 1;
   p.group_ctas = plan.grid;
-  for (int tok0 = 0; tok0 < a->q_len; tok0 += plan.q_group) {
+  for (int gg = 0; gg < ngroups; ++gg) {
+    const int tok0 = gg / plan.hchunks * plan.q_group;
     p.q_tok0 = tok0;
     p.q_len = std::min(plan.q_group, a->q_len - tok0);
-    if (tok0 > 0) p.epoch = next_epoch();
-    const bool first = tok0 == 0, last = tok0 + p.q_len == a->q_len;
+    p.hc0 = gg % plan.hchunks;
+    if (gg > 0) p.epoch = next_epoch();
+    const bool first = gg == 0, last = gg == ngroups - 1;
     cudaEvent_t begin = first ? reinterpret_cast<cudaEvent_t>(a->attn_begin) : nullptr;
     cudaEvent_t end = last ? reinterpret_cast<cudaEvent_t>(a->attn_end) : nullptr;
     const cudaError_t e = plan.prefix_tiles > 0

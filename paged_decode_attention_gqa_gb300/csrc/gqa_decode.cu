@@ -44,8 +44,9 @@ struct Launch {
   }
 };
 
-// Two token groups per CTA: causal rows, merge launch, heads per CTA 1/2/4
-// (half of a one-group CTA's).
+// Two row groups per CTA: causal rows (correct for one query token too: the
+// limit is then the whole cache), merge launch, heads per CTA 1/2/4 (half of
+// a one-group CTA's).
 template <int HPC, bool R16>
 struct TwoGroups {
   static cudaError_t launch(const GqaParams& p, int grid, cudaStream_t stream) {
@@ -102,7 +103,9 @@ int merge_pieces(int64_t blocks) {
 }  // namespace
 
 int gqa_ctas_per_sm(int hpc, bool rows16, bool causal, bool fused, int tg, int device) {
-  if (tg == 2) return causal && !fused ? two_groups_ctas_per_sm(hpc, rows16, device) : 0;
+  // (two groups per CTA always run the causal instances: with one query token
+  // every row's limit is the whole cache)
+  if (tg == 2) return fused ? 0 : two_groups_ctas_per_sm(hpc, rows16, device);
   return dispatch<Occupancy>(hpc, rows16, causal, fused, device);
 }
 
@@ -110,11 +113,11 @@ cudaError_t gqa_decode_launch(const GqaParams& p, int grid, bool fused, cudaStre
                               cudaEvent_t attn_begin, cudaEvent_t attn_end) {
   cudaError_t e = cudaSuccess;
   if (attn_begin && (e = cudaEventRecord(attn_begin, stream)) != cudaSuccess) return e;
-  const bool r16 = p.g * p.q_len > 8;
+  const bool r16 = p.gh * p.q_len > 8;
   const bool known = p.hpc == 1 || p.hpc == 2 || p.hpc == 4 || p.hpc == 8;
   if (!known) return cudaErrorInvalidValue;
   if (p.tg == 2) {
-    if (fused || p.q_total < 2) return cudaErrorInvalidValue;
+    if (fused) return cudaErrorInvalidValue;
     e = launch_two_groups(p, r16, grid, stream);
   } else {
     e = dispatch<Launch>(p.hpc, r16, p.q_total > 1, fused, &p, grid, stream);
@@ -125,7 +128,7 @@ cudaError_t gqa_decode_launch(const GqaParams& p, int grid, bool fused, cudaStre
   // The merge as a programmatic dependent launch: its CTAs may become resident
   // before the attention grid ends and wait in griddepcontrol.wait.
   const int64_t items =
-      int64_t(p.ngroups) * p.B * p.Hkv * ((p.g * p.q_len + kMergeRows - 1) / kMergeRows);
+      int64_t(p.ngroups) * p.B * p.Hkv * ((p.gh * p.q_len + kMergeRows - 1) / kMergeRows);
   const int64_t blocks = (items + 3) / 4;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(blocks));

@@ -235,18 +235,19 @@ __device__ __forceinline__ void merge_add_pieces(MergeAcc& m, const GqaParams& p
   }
 }
 
-// Adds rows (sequence b, tile rows r0 + k of g * q_len, head group starting at
-// head0) from an fp32 store of whole-unit results.
+// Adds rows (sequence b, tile rows r0 + k of gh * q_len: token r / gh, head
+// head0 + r % gh) from an fp32 store of whole-unit results.
 __device__ __forceinline__ void merge_add_store(MergeAcc& m, const GqaParams& p,
                                                 const float* st_o, const float* st_lse, int b,
-                                                int tok0, int head0, int r0, int nrows, int lane) {
+                                                int tok0, int head0, int gh, int r0, int nrows,
+                                                int lane) {
   float lv[kMergeRows];
   float4 ov[kMergeRows];
 #pragma unroll
   for (int k = 0; k < kMergeRows; ++k) {
     if (k < nrows) {
       const int r = r0 + k;
-      const int64_t orow = (int64_t(b) * p.q_total + tok0 + r / p.g) * p.Hq + head0 + r % p.g;
+      const int64_t orow = (int64_t(b) * p.q_total + tok0 + r / gh) * p.Hq + head0 + r % gh;
       lv[k] = __ldcg(st_lse + orow);
       ov[k] = __ldcg(reinterpret_cast<const float4*>(st_o + orow * kGqaHeadDim) + lane);
     }
@@ -256,17 +257,17 @@ __device__ __forceinline__ void merge_add_store(MergeAcc& m, const GqaParams& p,
     if (k < nrows) m.add(k, lv[k], ov[k]);
 }
 
-// Writes the merged rows of sequence b (rows of query tokens from tok0) as bf16
-// out and natural-log lse; a bad source or a row with no weight gives zeros
-// and lse = -inf.
+// Writes the merged rows of sequence b (row r: token tok0 + r / gh, head
+// head0 + r % gh) as bf16 out and natural-log lse; a bad source or a row with
+// no weight gives zeros and lse = -inf.
 __device__ __forceinline__ void merge_write_out(const MergeAcc& m, const GqaParams& p, int b,
-                                                int tok0, int head0, int r0, int nrows,
+                                                int tok0, int head0, int gh, int r0, int nrows,
                                                 int lane) {
 #pragma unroll
   for (int k = 0; k < kMergeRows; ++k) {
     if (k < nrows) {
       const int r = r0 + k;
-      const int64_t orow = (int64_t(b) * p.q_total + tok0 + r / p.g) * p.Hq + head0 + r % p.g;
+      const int64_t orow = (int64_t(b) * p.q_total + tok0 + r / gh) * p.Hq + head0 + r % gh;
       const bool none = m.bad || !(m.den[k] > 0.f);
       const float inv = none ? 0.f : 1.f / m.den[k];
       uint2 packed = make_uint2(0u, 0u);
@@ -286,14 +287,14 @@ __device__ __forceinline__ void merge_write_out(const MergeAcc& m, const GqaPara
 template <int kMergePieces>
 __device__ __forceinline__ void merge_split_rows(const GqaParams& p, const TileCut& cut, int cta0,
                                                  int64_t U0, int c_lo, int c_hi, int b, int tok0,
-                                                 int w, int head0, int R, int r_begin, int r_end,
-                                                 int lane) {
+                                                 int w, int head0, int gh, int R, int r_begin,
+                                                 int r_end, int lane) {
   for (int r0 = r_begin; r0 < r_end; r0 += kMergeRows) {
     const int nrows = min(kMergeRows, r_end - r0);
     MergeAcc m;
     m.init();
     merge_add_pieces<kMergePieces>(m, p, cut, cta0, U0, c_lo, c_hi, w, R, 0, r0, nrows, lane);
-    merge_write_out(m, p, b, tok0, head0, r0, nrows, lane);
+    merge_write_out(m, p, b, tok0, head0, gh, r0, nrows, lane);
   }
 }
 
@@ -310,12 +311,29 @@ __device__ __forceinline__ int seq_unit_tiles(const GqaParams& p, int L) {
   return t > 0 ? t : 0;
 }
 
+// Row group k of a launch: query tokens [tok0, tok0 + qlen) and, of each kv
+// head's g query heads, heads [hoff, hoff + gh). Tile row r of the group is
+// token tok0 + r / gh, head hoff + r % gh.
+struct RowGroup {
+  int tok0, qlen, hoff, gh;
+};
+__device__ __forceinline__ RowGroup row_group(const GqaParams& p, int k) {
+  const int gg = p.hc0 + k;
+  const int tt = gg / p.hchunks, hc = gg - tt * p.hchunks;
+  RowGroup r;
+  r.tok0 = p.q_tok0 + tt * p.q_len;
+  r.qlen = min(p.q_len, p.q_total - r.tok0);
+  r.hoff = hc * p.gh;
+  r.gh = min(p.gh, p.g - r.hoff);
+  return r;
+}
+
 template <int HPC, bool ROWS16, bool CAUSAL, bool FUSED, int MODE = kModePlain, int TG = 1>
 __global__ void __launch_bounds__(GqaCfg<HPC, TG>::kThreads, 1)
 gqa_decode_kernel(const __grid_constant__ GqaParams p) {
   static_assert(MODE == kModePlain || !FUSED, "the in-kernel merge is for plain launches");
   static_assert(TG == 1 || (MODE == kModePlain && !FUSED && CAUSAL),
-                "two token groups per CTA: plain launches of multi-token calls");
+                "two row groups per CTA: plain launches, causal instances, merge launch");
   using Cfg = GqaCfg<HPC, TG>;
   constexpr int NS = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -421,8 +439,10 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
   const int G = TG > 1 ? int(gridDim.x) : p.group_ctas;
   const int c = TG > 1 ? int(blockIdx.x) : int(blockIdx.x) - tg * p.group_ctas;
   const int vcta = tg * G + c;
-  const int tok0 = p.q_tok0 + tg * p.q_len;
-  const int qlen = min(p.q_len, p.q_total - tok0);
+  // the group's query tokens [tok0, tok0 + qlen) and heads [hoff, hoff + gh)
+  // of each kv head's g
+  const RowGroup rg = row_group(p, tg);
+  const int tok0 = rg.tok0, qlen = rg.qlen, gh = rg.gh;
   const int nhg = p.nhg;
   const int64_t W = int64_t(nhg) * prefix[V];
   const TileCut cut{W / G, uint32_t(W % G), uint32_t(G)};
@@ -544,23 +564,23 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
     const int b = pre ? v * p.sgs : v - NG;
     // Tokens the unit's tiles cover end at L (a prefix unit: the whole prefix).
     const int L = pre ? PT * kGqaTile : p.seq_lens[b];
-    const int head0 = (hg * HPC + w) * g;  // first query head of this kv head
+    const int head0 = (hg * HPC + w) * g + rg.hoff;  // the group's first query head
     // m16 tile rows are (sequence b + r / rps, query token i, head head0 + j)
-    // with rps = g * qlen rows per sequence, r % rps = i * g + j; R rows per
+    // with rps = gh * qlen rows per sequence, r % rps = i * gh + j; R rows per
     // partial slot (the largest group's), R_act of them exist, the rest are
     // zero. Query i (token tok0 + i of the q_total) sees tokens
     // t < L - q_total + 1 + tok0 + i (the new tokens are in the cache; each
     // sees itself and what precedes it); every row sees all of a shared prefix.
-    const int rps = g * qlen;
-    const int R = MODE == kModeShared ? p.sgs * rps : g * p.q_len;
+    const int rps = gh * qlen;
+    const int R = MODE == kModeShared ? p.sgs * rps : p.gh * p.q_len;
     const int R_act = pre ? min(p.sgs, B - b) * rps : rps;
     const int ra = gid, rb = gid + 8;
     const int lim0 = L - p.q_total + 1 + tok0;
-    const int lim_a = pre ? (1 << 30) : lim0 + ra / g;
-    const int lim_b = pre ? (1 << 30) : lim0 + rb / g;
+    const int lim_a = pre ? (1 << 30) : lim0 + ra / gh;
+    const int lim_b = pre ? (1 << 30) : lim0 + rb / gh;
     auto qrow_index = [&](int r) -> int64_t {
       const int rr = r % rps;
-      return (int64_t(b + r / rps) * p.q_total + tok0 + rr / g) * p.Hq + head0 + rr % g;
+      return (int64_t(b + r / rps) * p.q_total + tok0 + rr / gh) * p.Hq + head0 + rr % gh;
     };
 
     uint32_t qa[8][4];
@@ -777,16 +797,17 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
     const int64_t U0 = int64_t(nhg) * prefix[b] + int64_t(hg) * n;
     int c_lo, c_hi;
     split_cta_span(cut, U0, n, c, c_lo, c_hi);
-    merge_split_rows<4>(p, cut, vcta - c, U0, c_lo, c_hi, b, tok0, w, (hg * HPC + w) * g,
-                        g * p.q_len, 0, g * qlen, lane);
+    merge_split_rows<4>(p, cut, vcta - c, U0, c_lo, c_hi, b, tok0, w,
+                        (hg * HPC + w) * g + rg.hoff, gh, p.gh * p.q_len, 0, gh * qlen, lane);
   }
   }
 
   if constexpr (MODE == kModePlain) {
     // Sequences with no tiles (empty or invalid length): zeros, lse = -inf,
-    // for the rows of the CTA's groups of sequence b: tokens [ztok0, + zlen).
-    const int ztok0 = TG > 1 ? p.q_tok0 : tok0;
-    const int zlen = TG > 1 ? min(TG * p.q_len, p.q_total - p.q_tok0) : qlen;
+    // for every head of the tokens of the CTA's groups: [ztok0, + zlen).
+    const RowGroup zlast = row_group(p, TG - 1);
+    const int ztok0 = TG > 1 ? row_group(p, 0).tok0 : tok0;
+    const int zlen = TG > 1 ? zlast.tok0 + zlast.qlen - ztok0 : qlen;
     constexpr int kStride = Cfg::kConsumers * 32;  // the consumer threads
     for (int b = c; b < B; b += G) {
       if (prefix[b + 1] != prefix[b]) continue;
@@ -821,9 +842,9 @@ template <int MODE, int PIECES = 2>
 __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ GqaParams p,
                                                         int G) {
   const int lane = threadIdx.x & 31;
-  const int rmax = p.g * p.q_len;  // rows of a partial slot (the largest group's)
+  const int rmax = p.gh * p.q_len;  // rows of a partial slot (the largest group's)
   const int nrb = (rmax + kMergeRows - 1) / kMergeRows;
-  // items: (token group, sequence, kv head, block of kMergeRows rows)
+  // items: (row group, sequence, kv head, block of kMergeRows rows)
   const int64_t per_group = int64_t(p.B) * p.Hkv * nrb;
   const int64_t item = int64_t(blockIdx.x) * 4 + (threadIdx.x >> 5);
   const bool live = item < per_group * p.ngroups;
@@ -831,8 +852,9 @@ __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ 
   const int64_t gitem = item - tg * per_group;
   const int64_t unit = live ? gitem / nrb : 0;  // b * Hkv + kv head
   const int b = int(unit / p.Hkv), kvh = int(unit % p.Hkv);
-  const int tok0 = p.q_tok0 + tg * p.q_len;
-  const int rps = p.g * min(p.q_len, p.q_total - tok0);  // this group's rows per sequence
+  const RowGroup rg = row_group(p, tg);
+  const int tok0 = rg.tok0, gh = rg.gh;
+  const int rps = gh * rg.qlen;  // this group's rows per sequence
   // Before waiting for the attention grid: the tile line, from seq_lens alone.
   // seq_lens is an input of the call; the attention grid let this kernel
   // launch only after its own dependency wait, so it is final here. Units are
@@ -859,7 +881,7 @@ __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ 
   const int nrows = min(kMergeRows, rps - r0);
   const int cta0 = tg * G;  // the group's first CTA (G = CTAs per group)
   const int hg = kvh / p.hpc, w = kvh % p.hpc;
-  const int head0 = kvh * p.g;
+  const int head0 = kvh * p.g + rg.hoff;  // the group's first query head
   const int PT = MODE == kModeShared ? p.prefix_tiles : 0;
   const int64_t W = int64_t(p.nhg) * (int64_t(NG) * PT + all);
   const TileCut cut{W / G, uint32_t(W % G), uint32_t(G)};
@@ -869,7 +891,7 @@ __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ 
     if (n == 0 || c_lo == c_hi) return;
     // PIECES pieces per round trip to L2 (the host takes 6 when the merge grid
     // fits in one wave at the registers that needs, else 2).
-    merge_split_rows<PIECES>(p, cut, cta0, U0, c_lo, c_hi, b, tok0, w, head0, rmax, r0,
+    merge_split_rows<PIECES>(p, cut, cta0, U0, c_lo, c_hi, b, tok0, w, head0, gh, rmax, r0,
                              r0 + nrows, lane);
   } else {
     const int R = p.sgs * rps;  // rows of a partial slot
@@ -881,18 +903,18 @@ __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ 
       const int64_t P0 = int64_t(p.nhg) * (int64_t(vp) * PT) + int64_t(hg) * np;
       const int p_lo = cta_of_tile(P0, W, G), p_hi = cta_of_tile(P0 + np - 1, W, G);
       if (p_lo == p_hi)
-        merge_add_store(m, p, p.pre_o, p.pre_lse, b, tok0, head0, r0, nrows, lane);
+        merge_add_store(m, p, p.pre_o, p.pre_lse, b, tok0, head0, gh, r0, nrows, lane);
       else
         merge_add_pieces<2>(m, p, cut, cta0, P0, p_lo, p_hi, w, R, (b % p.sgs) * rps, r0, nrows,
                             lane);
     }
     if (n > 0) {
       if (c_lo == c_hi)
-        merge_add_store(m, p, p.suf_o, p.suf_lse, b, tok0, head0, r0, nrows, lane);
+        merge_add_store(m, p, p.suf_o, p.suf_lse, b, tok0, head0, gh, r0, nrows, lane);
       else
         merge_add_pieces<2>(m, p, cut, cta0, U0, c_lo, c_hi, w, R, 0, r0, nrows, lane);
     }
-    merge_write_out(m, p, b, tok0, head0, r0, nrows, lane);
+    merge_write_out(m, p, b, tok0, head0, gh, r0, nrows, lane);
   }
 }
 

@@ -56,12 +56,12 @@ cudaError_t gqa_shared_launch(const GqaParams& p, int grid, cudaStream_t stream,
   if (!known) return cudaErrorInvalidValue;
   cudaError_t e = cudaSuccess;
   if (attn_begin && (e = cudaEventRecord(attn_begin, stream)) != cudaSuccess) return e;
-  const bool r16 = p.sgs * p.g * p.q_len > 8;
+  const bool r16 = p.sgs * p.gh * p.q_len > 8;
   if ((e = dispatch_mode<Launch, kModeShared>(p.hpc, r16, p.q_total > 1, &p, grid, stream)) !=
       cudaSuccess)
     return e;
   if (attn_end && (e = cudaEventRecord(attn_end, stream)) != cudaSuccess) return e;
-  const int rps = p.g * p.q_len;
+  const int rps = p.gh * p.q_len;
   const int64_t items = int64_t(p.B) * p.Hkv * ((rps + kMergeRows - 1) / kMergeRows);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned((items + 3) / 4));

@@ -23,7 +23,7 @@ struct GqaParams {
   const int32_t* seq_lens;
   int64_t bt_stride;
   unsigned long long* ws_count;  // [B * Hkv] arrivals per split unit: epoch << 32 | count
-  // Partial slots: [(token group, CTA) pairs][2][HPC][g * q_len], pair k * group_ctas + c
+  // Partial slots: [(row group, CTA) pairs][2][HPC][gh * q_len], pair k * group_ctas + c
   float* ws_o;         // [..][128] normalised partial outputs
   float* ws_lse;       // base-2 lse of the partials (NaN = bad piece)
   uint32_t* err_flags; // or nullptr
@@ -48,6 +48,13 @@ struct GqaParams {
   // K/V tile at about the same time. With ngroups = 1 the line ends where the
   // group's last token stops seeing.
   int q_total, q_tok0, ngroups, group_ctas;
+  // Query heads per row group (gh <= 16) and head chunks per kv head: with g <=
+  // 16 a group holds all g heads of its tokens (gh = g, hchunks = 1); with g >
+  // 16 each token's g heads go in hchunks = ceil(g / 16) chunks of gh heads
+  // (the last may have fewer), one token per group. Group k of a launch is
+  // token group (hc0 + k) / hchunks (counted from q_tok0) and head chunk
+  // (hc0 + k) % hchunks.
+  int gh, hchunks, hc0;
   // Token groups per CTA (1 or 2). With 2, every CTA takes both groups of a
   // two-group launch (consumer warp w: kv head w % hpc, group w / hpc), so a
   // K/V stage serves both; group_ctas is then the whole grid, and group k's

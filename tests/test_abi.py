@@ -55,7 +55,7 @@ def _params(**over):
     (dict(q=(1 << 20) + 2), zl.ERR_INVALID_ARG),  # misaligned
     (dict(token_stride=100), zl.ERR_INVALID_ARG),  # not a multiple of 8 elements
     (dict(D_qk=64, D_v=64), zl.ERR_UNSUPPORTED),
-    (dict(Hq=8 * 32), zl.ERR_UNSUPPORTED),         # group of 32 heads
+    (dict(Hq=8 * 129), zl.ERR_UNSUPPORTED),        # 129 query heads per kv head
     (dict(q_len=129), zl.ERR_UNSUPPORTED),         # more query tokens than one call takes
     (dict(q_len=5, shared_prefix_pages=1), zl.ERR_UNSUPPORTED),  # 4 x 5 rows, shared prefix
     (dict(q_len=0), zl.ERR_INVALID_ARG),

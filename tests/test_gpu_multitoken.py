@@ -183,3 +183,56 @@ def test_token_groups_last_row_matches_single_token_call():
     torch.cuda.synchronize()
     assert_close(g.out[:, -1].double().cpu().numpy(), out1[:, 0].double().cpu().numpy(),
                  "last of 8 tokens vs a one-token call")
+
+
+# More than 16 query heads per kv head (many-head MQA, wide GQA): each token's
+# g heads go in ceil(g / 16) chunks of at most 16 rows (the last may be
+# smaller), one row group per (token, chunk); two groups share every CTA, more
+# split the grid.
+@pytest.mark.parametrize("Hq,Hkv,q_len", [
+    (32, 1, 1),                              # MQA, 32 heads: two chunks of 16
+    (48, 1, 1),                              # three chunks of 16
+    (17, 1, 1),                              # chunks of 9 and 8
+    (71, 1, 1),                              # five chunks: 15, 15, 15, 15, 11
+    (64, 2, 1),                              # g = 32 over two kv heads
+    (32, 1, 3),                              # 3 tokens x 2 chunks: six groups
+    (40, 2, 2),                              # g = 20: chunks of 10, 2 tokens
+])
+def test_many_heads_per_kv_head(Hq, Hkv, q_len):
+    w = wl.random_case(950 + 13 * Hq + 5 * Hkv + q_len, B=5, Hq=Hq, Hkv=Hkv, max_len=300,
+                       q_len=q_len)
+    _parity(w)
+
+
+@pytest.mark.parametrize("num_ctas", [1, 3, 152, 777])
+def test_many_heads_any_split(num_ctas):
+    w = wl.random_case(960, B=4, Hq=32, Hkv=1, max_len=600, q_len=2)
+    _parity(w, num_ctas=num_ctas)
+
+
+def test_many_heads_short_contexts():
+    """One CTA per unit (no merge) with head chunks; lengths at tile edges and
+    rows that see nothing."""
+    lens = [0, 1, 2, 15, 16, 17, 33, 40]
+    w = wl.random_case(970, B=len(lens), Hq=48, Hkv=1, lens=lens, q_len=2)
+    g = _parity(w)
+    out = g.out.float().cpu()
+    assert torch.all(out[0] == 0) and torch.all(torch.isneginf(g.lse[0].cpu()))
+    assert torch.all(out[1, 0] == 0)  # token 0 of a 1-token cache sees nothing
+
+
+def test_many_heads_single_launch():
+    """Single-launch mode: one launch per (token, head chunk) group, each with
+    its merge inside the attention kernel."""
+    w = wl.random_case(980, B=6, Hq=32, Hkv=1, max_len=700, q_len=2)
+    d = device_inputs(w)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lse = torch.empty((w.B, w.q_len, w.Hq), dtype=torch.float32, device="cuda")
+    out = zl.decode_attn(d["q"], d["k"], d["v"], d["bt"], d["sl"], page_size=w.page_size,
+                         scale=w.scale, lse=lse, err_flags=err, max_seq_len=w.max_seq_len,
+                         single_launch=True)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref, ref_lse, _ = run_oracle(w)
+    assert_close(out.float().cpu().numpy(), ref, "single launch, head chunks")
+    assert_close(lse.double().cpu().numpy(), ref_lse, "single launch, head chunks lse")
