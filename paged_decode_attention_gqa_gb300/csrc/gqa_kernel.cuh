@@ -58,12 +58,14 @@ template <int HPC, int TG = 1>
 struct GqaCfg {
   static constexpr int kHalfBytes = HPC * kGqaTile * 64 * 2;  // one 64-column half of K or V
   static constexpr int kStageBytes = 4 * kHalfBytes;           // K lo | K hi | V lo | V hi
-  // Two token groups per CTA (half the heads of a one-group CTA, the same
-  // warps): 192 KB of stages in flight, as at HPC = 8.
-  static constexpr int kStages =
-      TG > 1 ? 192 * 1024 / kStageBytes : HPC == 8 ? 3 : HPC == 4 ? 4 : HPC == 2 ? 6 : 8;
+  // Two row groups per CTA: six stages, and as many CTAs per SM as make 8
+  // consumer warps (one at HPC = 4, four at HPC = 1), so that an SM has
+  // 192 KB of stages in flight and 8 consumer warps to hide each tile's
+  // latency, as at HPC = 8.
+  static constexpr int kStages = TG > 1 ? 6 : HPC == 8 ? 3 : HPC == 4 ? 4 : HPC == 2 ? 6 : 8;
   static constexpr int kConsumers = HPC * TG;  // consumer warps
   static constexpr int kThreads = (kConsumers + 1) * 32;
+  static constexpr int kMinBlocks = TG > 1 && kConsumers < 8 ? 8 / kConsumers : 1;
   // 1 KB alignment slack + stages + barriers + per-stage flags + abort flag + prefix table
   // + split-piece records (2 per consumer warp)
   static constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStageBytes + kStages * 16 +
@@ -329,7 +331,7 @@ __device__ __forceinline__ RowGroup row_group(const GqaParams& p, int k) {
 }
 
 template <int HPC, bool ROWS16, bool CAUSAL, bool FUSED, int MODE = kModePlain, int TG = 1>
-__global__ void __launch_bounds__(GqaCfg<HPC, TG>::kThreads, 1)
+__global__ void __launch_bounds__(GqaCfg<HPC, TG>::kThreads, GqaCfg<HPC, TG>::kMinBlocks)
 gqa_decode_kernel(const __grid_constant__ GqaParams p) {
   static_assert(MODE == kModePlain || !FUSED, "the in-kernel merge is for plain launches");
   static_assert(TG == 1 || (MODE == kModePlain && !FUSED && CAUSAL),

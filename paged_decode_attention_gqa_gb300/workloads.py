@@ -243,6 +243,22 @@ def llama3_8b_decode(seed=1002, layout="NHD", poison=True, B=64, values=True,
                           values=values, q_len=q_len)
 
 
+def mqa32_decode(seed=1006, layout="NHD", poison=True, B=64, values=True,
+                 q_len=1) -> Workload:
+    """Many-head multi-query attention: the Llama-3-8B lengths (64 seqs,
+    U[512, 4096], page 16, pool 1.25x) with 32 query heads on one KV head, D
+    128 -- more than 16 heads per KV head, so two row groups of 16."""
+    rng = _structure_rng(seed)
+    lens = rng.integers(512, 4096, size=B, endpoint=True).astype(np.int32)
+    pages = int(((lens + 15) // 16).sum())
+    num_pages = _pool_for(pages)
+    table = place_pages(rng, lens, 16, num_pages)
+    return build_workload("mqa32_decode", seed, B=B, Hq=32, Hkv=1, D_qk=128, page_size=16,
+                          seq_lens=lens, block_table=table, num_pages=num_pages,
+                          scale=1.0 / math.sqrt(128), layout=layout, poison=poison,
+                          values=values, q_len=q_len)
+
+
 def llama70b_prefix_decode(seed=1003, layout="NHD", poison=True, sigma=1.0, values=True,
                            B=128) -> Workload:
     """70B attention shape with prefix sharing: 128 seqs, 64 query / 8 KV heads,
@@ -301,6 +317,7 @@ WORKLOADS = {
     "llama70b_prefix_decode": llama70b_prefix_decode,
     "long_context_decode": long_context_decode,
     "mla_decode": mla_decode,
+    "mqa32_decode": mqa32_decode,
 }
 
 

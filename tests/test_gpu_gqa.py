@@ -185,6 +185,12 @@ def test_long_context_full():
     _parity(wl.long_context_decode())
 
 
+def test_mqa32_full():
+    """32 query heads on one kv head (two row groups of 16 heads, both in every
+    CTA), the Llama-3-8B lengths, the whole output against the oracle."""
+    _parity(wl.mqa32_decode())
+
+
 def test_cuda_graph_capture_of_the_default_path():
     """The default call (attention kernel + merge kernel as a programmatic
     dependent launch) captures into a CUDA graph; replays give the eager bits."""

@@ -61,6 +61,11 @@ def test_structures_of_large_workloads():
     assert c5.mla and c5.Hkv == 1 and c5.D_qk == 576 and c5.D_v == 512
     assert abs(c5.scale - 192 ** -0.5) < 1e-15
 
+    m = wl.mqa32_decode(values=False)
+    assert m.B == 64 and m.Hq == 32 and m.Hkv == 1 and m.page_size == 16 and not m.mla
+    assert m.seq_lens.min() >= 512 and m.seq_lens.max() <= 4096
+    assert m.num_pages == int(np.ceil(1.25 * ((m.seq_lens + 15) // 16).sum()))
+
 
 def test_pages_are_distinct_without_prefix():
     c2 = wl.llama3_8b_decode(values=False)
