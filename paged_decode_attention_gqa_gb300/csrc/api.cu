@@ -425,7 +425,11 @@ zl_status zl_decode_attn(const zl_decode_attn_params* a, zl_stream_t stream) {
     p.q_len = plan.q_group;
     p.ngroups = ngroups;
     p.tg = plan.tg;
-    // two groups per CTA: each group has every CTA; else the grid is split
+    // two groups per CTA: each group has every CTA; else the grid is split.
+    // The partial slots are sized for plan.grid (group, CTA) pairs: with
+    // floor(grid / ngroups) >= 1 CTAs per group the pairs are at most that; a
+    // group with one CTA (more groups than CTAs) takes the whole tile line,
+    // so it cuts no unit and writes no partial (nor does a unit-cut launch).
     p.group_ctas = plan.unit_cut || plan.tg == 2 ? plan.grid : std::max(1, plan.grid / ngroups);
     const int launch_grid = plan.tg == 2 ? plan.grid : p.group_ctas * ngroups;
     const cudaError_t e = zl::gqa_decode_launch(
