@@ -236,3 +236,35 @@ def test_many_heads_single_launch():
     ref, ref_lse, _ = run_oracle(w)
     assert_close(out.float().cpu().numpy(), ref, "single launch, head chunks")
     assert_close(lse.double().cpu().numpy(), ref_lse, "single launch, head chunks lse")
+
+
+@pytest.mark.parametrize("Hq,Hkv,q_len,num_ctas", [
+    (128, 1, 60, 0),     # 480 row groups: more than the default grid's CTAs
+    (32, 1, 2, 3),       # 4 groups over 3 CTAs: one CTA each
+    (32, 8, 13, 7),      # 4 token groups over 7 CTAs: one CTA each
+    (32, 1, 3, 13),      # 6 groups, 2 CTAs each
+    (32, 8, 8, 5),       # two groups in every CTA
+])
+def test_row_groups_stay_inside_the_workspace(Hq, Hkv, q_len, num_ctas):
+    """A workspace of exactly the reported size, followed by a guard region:
+    every launch plan of row groups (one CTA per group when there are more
+    groups than CTAs) leaves the guard untouched and matches the oracle."""
+    w = wl.random_case(990 + Hq + 3 * q_len + num_ctas, B=4, Hq=Hq, Hkv=Hkv, max_len=400,
+                       q_len=q_len)
+    d = device_inputs(w)
+    out = torch.empty((w.B, w.q_len, w.Hq, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.B, w.q_len, w.Hq), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kw = dict(page_size=w.page_size, scale=w.scale, Hkv=w.Hkv, D_v=128, lse=lse,
+              err_flags=err, num_ctas=num_ctas)
+    n = zl.workspace_size(zl.make_params(d["q"], d["k"], d["v"], d["bt"], d["sl"], out, **kw))
+    guard = 1 << 20
+    buf = torch.full((n + guard,), 0xA5, dtype=torch.uint8, device="cuda")
+    p = zl.make_params(d["q"], d["k"], d["v"], d["bt"], d["sl"], out, workspace=buf[:n], **kw)
+    zl.call(p, mla=False)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert bool(torch.all(buf[n:] == 0xA5)), "a launch wrote past the workspace"
+    ref, ref_lse, _ = run_oracle(w)
+    assert_close(out.double().cpu().numpy(), ref, "row groups, exact workspace")
+    assert_close(lse.double().cpu().numpy(), ref_lse, "row groups, exact workspace lse")
