@@ -203,8 +203,9 @@ zl_status zl_decode_attn_mla_workspace_size(const zl_decode_attn_params* params,
 /* Kernel launches one zl_decode_attn call with these params enqueues: the
    attention kernel and, unless no unit is cut (short contexts given a CTA per
    unit, known from max_seq_len) or ZL_DECODE_SINGLE_LAUNCH merges inside it,
-   the merge kernel; with ZL_DECODE_SINGLE_LAUNCH or a shared prefix, that
-   once per group of query tokens (see zl_decode_attn). The same inputs and
+   the merge kernel; with ZL_DECODE_SINGLE_LAUNCH, that once per row group
+   (group of query tokens, or of heads when g > 16; see zl_decode_attn). A
+   shared-prefix call has one row group. The same inputs and
    rules as zl_decode_attn_workspace_size. (zl_decode_attn_mla always
    enqueues two.) */
 zl_status zl_decode_attn_launches(const zl_decode_attn_params* params, int32_t* launches);
