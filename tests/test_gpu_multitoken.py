@@ -268,3 +268,31 @@ def test_row_groups_stay_inside_the_workspace(Hq, Hkv, q_len, num_ctas):
     ref, ref_lse, _ = run_oracle(w)
     assert_close(out.double().cpu().numpy(), ref, "row groups, exact workspace")
     assert_close(lse.double().cpu().numpy(), ref_lse, "row groups, exact workspace lse")
+
+
+@pytest.mark.parametrize("Hq,Hkv,q_len", [(32, 8, 8), (32, 1, 1)])
+def test_two_groups_per_cta_capture_into_a_cuda_graph(Hq, Hkv, q_len):
+    """A two-group call (8 tokens at g = 4; 32 heads on one kv head) and its
+    merge launch capture into a CUDA graph; replays give the eager bits."""
+    w = wl.random_case(1010 + Hq + q_len, B=6, Hq=Hq, Hkv=Hkv, max_len=1500, q_len=q_len)
+    d = device_inputs(w)
+    out = torch.empty((w.B, w.q_len, w.Hq, 128), dtype=torch.bfloat16, device="cuda")
+    p = zl.make_params(d["q"], d["k"], d["v"], d["bt"], d["sl"], out, page_size=w.page_size,
+                       scale=w.scale, Hkv=w.Hkv, D_v=128)
+    ws = torch.zeros(zl.workspace_size(p), dtype=torch.uint8, device="cuda")
+    p.workspace, p.workspace_bytes = ws.data_ptr(), ws.numel()
+    zl.call(p, mla=False)
+    torch.cuda.synchronize()
+    eager = out.clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        zl.call(p, mla=False, stream=s)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    ref, _, _ = run_oracle(w)
+    assert_close(out.double().cpu().numpy(), ref, "two groups per CTA, graph replay")
