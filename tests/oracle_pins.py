@@ -135,6 +135,9 @@ def pin_sdpa_dense(oracle):
         ([17, 5, 29], 8, 1, 128, 16),
         ([40], 4, 2, 128, 8),
         ([3, 31], 16, 4, 16, 4),
+        ([9, 23], 32, 1, 8, 4),     # many-head MQA (32 query heads on one kv head)
+        ([14], 71, 1, 8, 8),        # 71 heads: no even split into chunks of 16
+        ([30, 5], 40, 2, 8, 16),    # 20 query heads per kv head
     ]
     for lens, Hq, Hkv, D, P in shapes:
         case = PagedCase(rng, lens, Hq, Hkv, D, P)
@@ -348,11 +351,11 @@ def pin_mla_absorption(oracle):
 def pin_multi_token_causal(oracle):
     """q_len > 1: query i sees tokens t <= L - q_len + i (bottom-right causal)."""
     rng = np.random.default_rng(24)
-    for q_len in (2, 4):
-        case = PagedCase(rng, [20, 9, 33], 8, 2, 16, 8, q_len=q_len)
+    for q_len, Hq, Hkv in ((2, 8, 2), (4, 8, 2), (3, 32, 1)):
+        case = PagedCase(rng, [20, 9, 33], Hq, Hkv, 16, 8, q_len=q_len)
         out, _, _ = case.run(oracle)
         for b in range(3):
-            _close(out[b], case.sdpa(b), 1e-12, f"causal q_len={q_len}")
+            _close(out[b], case.sdpa(b), 1e-12, f"causal q_len={q_len} Hq={Hq}")
 
 
 def pin_degenerate(oracle):
