@@ -305,6 +305,325 @@ def config_of(w, world):
             "parallelism": f"replicas x{world}"}
 
 
+class Case:
+    """One workload on the device, ready to call: inputs, output buffers, the
+    C-ABI params and workspace, the optional KV append and L2 flush."""
+
+    def __init__(self, w, dev, *, single_launch=False, shared_prefix=False, with_append=False,
+                 hint=True):
+        import paged_decode_attention_gqa_gb300 as zl
+        self.zl, self.w, self.dev = zl, w, dev
+        self.kind = "mla" if w.mla else "gqa"
+        self.q, self.k = w.q.to(dev), w.k_pool.to(dev)
+        self.v = None if w.mla else w.v_pool.to(dev)
+        self.bt = torch.from_numpy(w.block_table).to(dev)
+        self.sl = torch.from_numpy(w.seq_lens).to(dev)
+        self.out = torch.empty(w.B, w.q_len, w.Hq, w.D_v, dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty(w.B, w.q_len, w.Hq, dtype=torch.float32, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.npref = 0
+        if shared_prefix:
+            self.npref = int(w.notes.get("shared_prefix_tokens", 0)) // w.page_size
+            assert self.npref > 0, "--shared-prefix needs a workload with a shared prefix"
+        self.single_launch = single_launch and not w.mla
+        self.max_seq_len = w.max_seq_len if hint else 0
+        self.p = zl.make_params(self.q, self.k, self.v, self.bt, self.sl, self.out,
+                                page_size=w.page_size, scale=w.scale, Hkv=w.Hkv, D_v=w.D_v,
+                                lse=self.lse, err_flags=self.err, max_seq_len=self.max_seq_len,
+                                single_launch=self.single_launch, shared_prefix_pages=self.npref)
+        need = zl.workspace_size_mla(self.p) if w.mla else zl.workspace_size(self.p)
+        self.ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
+        self.p.workspace, self.p.workspace_bytes = self.ws.data_ptr(), self.ws.numel()
+        self.stream = torch.cuda.current_stream()
+        self.stream_ptr = ctypes.c_void_p(self.stream.cuda_stream)
+        # Small working sets are flushed from L2 between steps (a 2x L2 write).
+        self.flush = None
+        if kv_bytes(w) <= 4 * 129e6:
+            self.flush = torch.empty(int(2 * 129e6) // 4, dtype=torch.int32, device=dev)
+        # with_append: each step first writes the q_len new tokens' K/V rows
+        # into their page slots (zl_kv_append), then attends, as a decode step does.
+        self.ap = None
+        if with_append:
+            from paged_decode_attention_gqa_gb300 import workloads as _wl
+            k_new, v_new = _wl.new_token_rows(w.seed, w.B, w.q_len, w.Hkv, w.D_qk,
+                                              None if w.mla else w.D_v)
+            self.k_new = k_new.to(dev)
+            self.v_new = None if v_new is None else v_new.to(dev)
+            self.ap = zl.make_append_params(self.k_new, self.v_new, self.k, self.v, self.bt,
+                                            self.sl, page_size=w.page_size, layout=w.layout,
+                                            err_flags=self.err)
+
+    def call(self):
+        if self.ap is not None:
+            rc = self.zl.lib().zl_kv_append(ctypes.byref(self.ap), self.stream_ptr)
+            assert rc == self.zl.OK, rc
+        self.zl.call(self.p, mla=self.w.mla, stream=self.stream)
+
+    def step(self):
+        if self.flush is not None:
+            self.flush.zero_()
+        self.call()
+
+    def check_errors(self):
+        assert int(self.err.item()) == 0, f"device error flags {int(self.err.item())}"
+
+    def launches_per_step(self):
+        n = 2 if self.w.mla else self.zl.launches(self.p)
+        if self.ap is not None:
+            n += 1  # the KV append
+        if self.flush is not None:
+            n += 1  # the L2 flush memset
+        return n
+
+    def time_steps(self, steps):
+        """Mean ms per step over `steps` steps, CUDA events on the launching
+        stream. With an L2 flush between steps, each step's call is timed on
+        its own (events after the flush, around the call)."""
+        stream = self.stream
+        t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        step_evs = ([(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                     for _ in range(steps)] if self.flush is not None else None)
+        t_begin.record(stream)
+        for i in range(steps):
+            if self.flush is None:
+                self.call()
+            else:
+                self.flush.zero_()
+                step_evs[i][0].record(stream)
+                self.call()
+                step_evs[i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        if self.flush is None:
+            return t_begin.elapsed_time(t_end) / steps
+        return sum(a.elapsed_time(b) for a, b in step_evs) / steps
+
+    def time_kernel(self, n_ev):
+        """(attention-kernel ms, whole-call ms): the library records events
+        around the attention kernel alone, the bench around the call. Events
+        between the two launches would keep the merge from starting early, so
+        the timed steps carry none; this is a separate pass."""
+        stream = self.stream
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n_ev)]
+        # torch only reports elapsed time for events it has recorded itself;
+        # record each once here, the library re-records them around the kernel.
+        for a, b in evs:
+            a.record(stream)
+            b.record(stream)
+        call_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    for _ in range(n_ev)]
+        for i in range(n_ev):
+            self.p.attn_begin, self.p.attn_end = evs[i][0].cuda_event, evs[i][1].cuda_event
+            if self.flush is not None:
+                self.flush.zero_()
+            call_evs[i][0].record(stream)
+            self.call()
+            call_evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        self.p.attn_begin = self.p.attn_end = None
+        return (statistics.mean(a.elapsed_time(b) for a, b in evs),
+                statistics.mean(a.elapsed_time(b) for a, b in call_evs))
+
+    def host_enqueue_us(self, n_host=32):
+        """Host time to issue one call: a burst short enough that the launch
+        queue never fills (a long loop would pace the host at the GPU's rate)."""
+        h0 = time.perf_counter()
+        for _ in range(n_host):
+            self.call()
+        us = (time.perf_counter() - h0) / n_host * 1e6
+        torch.cuda.synchronize()
+        return us
+
+    def time_append(self, n_ev):
+        w = self.w
+        app_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(n_ev)]
+        for a, b in app_evs:
+            if self.flush is not None:
+                self.flush.zero_()
+            a.record(self.stream)
+            self.zl.lib().zl_kv_append(ctypes.byref(self.ap), self.stream_ptr)
+            b.record(self.stream)
+        torch.cuda.synchronize()
+        app_ms = statistics.mean(a.elapsed_time(b) for a, b in app_evs)
+        # new rows read once, written once into the pools
+        app_bytes = 2 * w.B * w.q_len * w.Hkv * (w.D_qk + (0 if w.mla else w.D_v)) * 2
+        return {"us_per_launch": app_ms * 1e3, "bytes_per_launch": app_bytes,
+                "GBs": app_bytes / (app_ms * 1e-3) / 1e9,
+                "note": "zl_kv_append alone, L2 flushed first when the step flushes"}
+
+    def e2e(self, steps, warm, world):
+        """End to end through the public API: host inputs in, host result out.
+        Every step copies its inputs (q, block table, seq_lens) in from pinned
+        host memory and its output back; steps are pipelined the way a serving
+        loop overlaps them: two device buffer sets, inputs copied on one stream,
+        the call on another, the output copied out on a third, ordered by
+        events. `warm` pipelined steps run first, untimed, so that the
+        pipeline is full and the streams and events are warm."""
+        zl, w = self.zl, self.w
+        pin_q = w.q.pin_memory()
+        pin_bt = torch.from_numpy(w.block_table).pin_memory()
+        pin_sl = torch.from_numpy(w.seq_lens).pin_memory()
+        pin_out = [torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+                   for _ in range(2)]
+        dq = [self.q, torch.empty_like(self.q)]
+        dbt = [self.bt, torch.empty_like(self.bt)]
+        dsl = [self.sl, torch.empty_like(self.sl)]
+        dout = [self.out, torch.empty_like(self.out)]
+        s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+        h2d = pin_q.numel() * 2 + pin_bt.numel() * 4 + pin_sl.numel() * 4
+        d2h = pin_out[0].numel() * 2
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_comp = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
+        torch.cuda.synchronize()
+        for e in ev_comp + ev_out:
+            e.record(s_comp)
+
+        def one(i):
+            j = i & 1
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(ev_comp[j])          # set j no longer read by step i - 2
+                dq[j].copy_(pin_q, non_blocking=True)
+                dbt[j].copy_(pin_bt, non_blocking=True)
+                dsl[j].copy_(pin_sl, non_blocking=True)
+                ev_in[j].record(s_in)
+            with torch.cuda.stream(s_comp):
+                s_comp.wait_event(ev_in[j])
+                s_comp.wait_event(ev_out[j])         # out j copied out by step i - 2
+                if self.flush is not None:
+                    self.flush.zero_()
+                if w.mla:
+                    zl.decode_attn_mla(dq[j], self.k, dbt[j], dsl[j], page_size=w.page_size,
+                                       scale=w.scale, D_v=w.D_v, out=dout[j], workspace=self.ws,
+                                       max_seq_len=self.max_seq_len, stream=s_comp)
+                else:
+                    zl.decode_attn(dq[j], self.k, self.v, dbt[j], dsl[j], page_size=w.page_size,
+                                   scale=w.scale, out=dout[j], workspace=self.ws,
+                                   max_seq_len=self.max_seq_len,
+                                   single_launch=self.single_launch,
+                                   shared_prefix_pages=self.npref, stream=s_comp)
+                ev_comp[j].record(s_comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_comp[j])
+                pin_out[j].copy_(dout[j], non_blocking=True)
+                ev_out[j].record(s_out)
+
+        for i in range(warm):
+            one(i)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(warm, warm + steps):
+            one(i)
+        torch.cuda.synchronize()
+        e2e_s = (time.perf_counter() - t0) / steps
+        return {"value": kv_bytes(w) * world / e2e_s / 1e9, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "us_per_step": e2e_s * 1e6, "steps": steps, "warmup_steps": warm,
+                "note": "every step copies q, block table and seq_lens in from pinned host memory "
+                        "and its output back (host wall clock, after the warm-up steps); steps "
+                        "pipelined over two buffer sets and three streams; the KV cache is "
+                        "device-resident state"
+                        + ("; includes the L2 flush" if self.flush is not None else "")}
+
+
+def roofline_bytes(w):
+    """(algorithmic bytes per launch, logical bytes per launch): the bytes HBM
+    has to deliver count a shared page once; logical counts every sequence's
+    reads."""
+    return unique_kv_bytes(w) + io_bytes(w), kv_bytes(w) + io_bytes(w)
+
+
+def mla_flops(w):
+    return 2.0 * int(w.seq_lens.astype(np.int64).sum()) * w.q_len * w.Hq * (w.D_qk + w.D_v)
+
+
+def bf16_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (burst)"
+    return 1900.0, "fallback (burst)"
+
+
+# Every other seeded configuration, timed in the same process after the
+# headline (each entry: name, workload, Case options).
+EXTRA_WORKLOADS = [
+    ("tiny_gqa", "tiny_gqa", {}),
+    ("tiny_gqa (no max_seq_len)", "tiny_gqa", {"hint": False}),
+    ("llama70b_prefix_decode", "llama70b_prefix_decode", {}),
+    ("llama70b_prefix_decode (shared prefix)", "llama70b_prefix_decode",
+     {"shared_prefix": True}),
+    ("long_context_decode", "long_context_decode", {}),
+    ("mla_decode", "mla_decode", {}),
+    ("mqa32_decode", "mqa32_decode", {}),
+    ("mqa32_decode (no max_seq_len)", "mqa32_decode", {"hint": False}),
+]
+
+
+def measure_extra(dev, steps, warmup, oracle_seconds):
+    """The other seeded configurations at full size: per call and per
+    attention kernel, algorithmic bytes and roofline fraction, parity of the
+    whole output against the oracle, and the oracle's own rate on the host."""
+    peak, peak_kind = measured_peaks()
+    tpeak, tpeak_kind = bf16_peak()
+    entries = {}
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    cache = {}
+    for label, name, opts in EXTRA_WORKLOADS:
+        w = cache.get(name) or make_workload(name)
+        cache = {name: w}  # keep one workload's host copy at a time
+        c = Case(w, dev, **opts)
+        for _ in range(warmup):
+            c.step()
+        torch.cuda.synchronize()
+        c.check_errors()
+        ms = c.time_steps(steps)
+        attn_ms, call_ms = c.time_kernel(max(10, min(steps, 200)))
+        c.check_errors()
+        algo, logical = roofline_bytes(w)
+        cpu_s, cpu_calls, cores, res = time_oracle(w, min_seconds=oracle_seconds, max_calls=3)
+        e = {"us_per_step": ms * 1e3, "us_per_call": call_ms * 1e3,
+             "attn_us_per_launch": attn_ms * 1e3,
+             "kv_GBs_per_step": kv_bytes(w) / (ms * 1e-3) / 1e9,
+             "algorithmic_bytes_per_launch": algo,
+             "roofline_frac": (algo / (attn_ms * 1e-3) / 1e9) / peak,
+             "launches_per_step": c.launches_per_step(),
+             "config": config_of(w, 1),
+             "parity": parity_summary(c.out, c.lse, res),
+             "oracle": {"GBs": kv_bytes(w) / cpu_s / 1e9, "us_per_call": cpu_s * 1e6,
+                        "cores": cores, "calls": cpu_calls, "kind": "oracle",
+                        "sample": "the whole workload per call"}}
+        if logical != algo:
+            e["logical_bytes_per_launch"] = logical
+            e["logical_GBs_attn"] = logical / (attn_ms * 1e-3) / 1e9
+            e["roofline_note"] = ("roofline_frac counts each distinct cache row once (the bytes "
+                                  "HBM must deliver); the shared prefix is served from L2, so "
+                                  "logical_GBs_attn is the rate the kernel consumes K/V at")
+        if opts.get("shared_prefix"):
+            e["shared_prefix_pages"] = c.npref
+        if not opts.get("hint", True):
+            e["max_seq_len"] = "not given (split plan decided on the device)"
+        if w.mla:
+            fl = mla_flops(w)
+            e["tensor"] = {"tflops": fl / (attn_ms * 1e-3) / 1e12, "flops_per_launch": fl,
+                           "frac_of_bf16_peak": fl / (attn_ms * 1e-3) / 1e12 / tpeak,
+                           "peak_tflops": tpeak, "peak_kind": tpeak_kind}
+        entries[label] = e
+        del c
+        torch.cuda.empty_cache()
+    clocks = sampler.stop()
+    return {"entries": entries, "peak_GBs": peak, "peak_kind": peak_kind, "clocks": clocks,
+            "steps": steps, "warmup": warmup,
+            "note": "each entry timed in this process after the headline, full-size inputs; "
+                    "us_per_step over the timed steps (L2 flushed between steps when the KV "
+                    "working set is under 4 x L2), attn_us_per_launch from events the library "
+                    "records around the attention kernel; parity is the whole output of the "
+                    "last call against the fp64 oracle"}
+
+
 def run_ours(args, world, rank, local):
     import paged_decode_attention_gqa_gb300 as zl
 
@@ -320,59 +639,14 @@ def run_ours(args, world, rank, local):
     zl.lib()
 
     w = make_workload(args.workload, args.batch, args.q_len)
-    kind = "mla" if w.mla else "gqa"
-    q, k = w.q.to(dev), w.k_pool.to(dev)
-    v = None if w.mla else w.v_pool.to(dev)
-    bt = torch.from_numpy(w.block_table).to(dev)
-    sl = torch.from_numpy(w.seq_lens).to(dev)
-    out = torch.empty(w.B, w.q_len, w.Hq, w.D_v, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty(w.B, w.q_len, w.Hq, dtype=torch.float32, device=dev)
-    err = torch.zeros(1, dtype=torch.int32, device=dev)
-    npref = 0
-    if args.shared_prefix:
-        npref = int(w.notes.get("shared_prefix_tokens", 0)) // w.page_size
-        assert npref > 0, "--shared-prefix needs a workload with a shared prefix"
-    p = zl.make_params(q, k, v, bt, sl, out, page_size=w.page_size, scale=w.scale, Hkv=w.Hkv,
-                       D_v=w.D_v, lse=lse, err_flags=err, max_seq_len=w.max_seq_len,
-                       single_launch=args.single_launch and not w.mla,
-                       shared_prefix_pages=npref)
-    need = zl.workspace_size_mla(p) if w.mla else zl.workspace_size(p)
-    ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
-    p.workspace, p.workspace_bytes = ws.data_ptr(), ws.numel()
-    stream = torch.cuda.current_stream()
-    # Small working sets are flushed from L2 between steps (a 2x L2 write).
-    flush = None
-    if kv_bytes(w) <= 4 * 129e6:
-        flush = torch.empty(int(2 * 129e6) // 4, dtype=torch.int32, device=dev)
-
-    # --with-append: each step first writes the q_len new tokens' K/V rows into
-    # their page slots (zl_kv_append), then attends, as a decode step does.
-    ap = None
-    if args.with_append:
-        from paged_decode_attention_gqa_gb300 import workloads as _wl
-        k_new, v_new = _wl.new_token_rows(w.seed, w.B, w.q_len, w.Hkv, w.D_qk,
-                                          None if w.mla else w.D_v)
-        k_new = k_new.to(dev)
-        v_new = None if v_new is None else v_new.to(dev)
-        ap = zl.make_append_params(k_new, v_new, k, v, bt, sl, page_size=w.page_size,
-                                   layout=w.layout, err_flags=err)
-    stream_ptr = ctypes.c_void_p(stream.cuda_stream)
-
-    def call():
-        if ap is not None:
-            rc = zl.lib().zl_kv_append(ctypes.byref(ap), stream_ptr)
-            assert rc == zl.OK, rc
-        zl.call(p, mla=w.mla, stream=stream)
-
-    def step():
-        if flush is not None:
-            flush.zero_()
-        call()
+    c = Case(w, dev, single_launch=args.single_launch, shared_prefix=args.shared_prefix,
+             with_append=args.with_append, hint=not args.no_hint)
+    kind = c.kind
 
     for _ in range(max(args.warmup, 3)):
-        step()
+        c.step()
     torch.cuda.synchronize()
-    assert int(err.item()) == 0, f"device error flags {int(err.item())}"
+    c.check_errors()
 
     # ---- timed region: K steps, CUDA events on the launching stream, clocks sampled
     sampler = ClockSampler(local)
@@ -382,148 +656,23 @@ def run_ours(args, world, rank, local):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    # With an L2 flush between steps, each step's call is timed on its own
-    # (events after the flush, around the call) and the flush is left out.
-    step_evs = ([(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                 for _ in range(args.steps)] if flush is not None else None)
-    t_begin.record(stream)
-    for i in range(args.steps):
-        if flush is None:
-            call()
-        else:
-            flush.zero_()
-            step_evs[i][0].record(stream)
-            call()
-            step_evs[i][1].record(stream)
-    t_end.record(stream)
-    torch.cuda.synchronize()
+    ms = c.time_steps(args.steps)
     clocks = sampler.stop()
-    if flush is None:
-        ms = t_begin.elapsed_time(t_end) / args.steps
-    else:
-        ms = sum(a.elapsed_time(b) for a, b in step_evs) / args.steps
     ms = max_over_ranks(ms, world, dev)
     # the library's own count per call: attention (+ merge) per token group
-    launches = args.steps * (2 if w.mla else zl.launches(p))
-    if ap is not None:
-        launches += args.steps                              # the KV append
-    if flush is not None:
-        launches += args.steps                              # the L2 flush memset
+    launches = args.steps * c.launches_per_step()
 
-    # ---- per-kernel timing, after the timed region: the library records
-    # events around the attention kernel alone, the bench around the call.
-    # (Events between the two launches would keep the merge from starting
-    # early, so the headline steps above carry none.)
-    n_ev = max(10, min(args.steps, 1000))
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(n_ev)]
-    # torch only reports elapsed time for events it has recorded itself; record
-    # each once here, the library re-records them around the attention kernel.
-    for a, b in evs:
-        a.record(stream)
-        b.record(stream)
-    call_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(n_ev)]
-    for i in range(n_ev):
-        p.attn_begin, p.attn_end = evs[i][0].cuda_event, evs[i][1].cuda_event
-        if flush is not None:
-            flush.zero_()
-        call_evs[i][0].record(stream)
-        call()
-        call_evs[i][1].record(stream)
-    torch.cuda.synchronize()
-    p.attn_begin = p.attn_end = None
-    # Host time to issue one call: a burst short enough that the launch queue
-    # never fills (a long loop would pace the host at the GPU's rate).
-    n_host = 32
-    h0 = time.perf_counter()
-    for _ in range(n_host):
-        call()
-    host_us = (time.perf_counter() - h0) / n_host * 1e6
-    torch.cuda.synchronize()
-    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
-    call_ms = statistics.mean(a.elapsed_time(b) for a, b in call_evs)
-    append = None
-    if ap is not None:
-        app_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(n_ev)]
-        for a, b in app_evs:
-            if flush is not None:
-                flush.zero_()
-            a.record(stream)
-            zl.lib().zl_kv_append(ctypes.byref(ap), stream_ptr)
-            b.record(stream)
-        torch.cuda.synchronize()
-        app_ms = statistics.mean(a.elapsed_time(b) for a, b in app_evs)
-        # new rows read once, written once into the pools
-        app_bytes = 2 * w.B * w.q_len * w.Hkv * (w.D_qk + (0 if w.mla else w.D_v)) * 2
-        append = {"us_per_launch": app_ms * 1e3, "bytes_per_launch": app_bytes,
-                  "GBs": app_bytes / (app_ms * 1e-3) / 1e9,
-                  "note": "zl_kv_append alone, L2 flushed first when the step flushes"}
-    assert int(err.item()) == 0, f"device error flags {int(err.item())}"
+    # ---- per-kernel timing, after the timed region
+    attn_ms, call_ms = c.time_kernel(max(10, min(args.steps, 1000)))
+    host_us = c.host_enqueue_us()
+    append = c.time_append(max(10, min(args.steps, 1000))) if c.ap is not None else None
+    c.check_errors()
 
-    # ---- end to end through the public API: host inputs in, host result out.
-    # Every step copies its inputs (q, block table, seq_lens) in from pinned host
-    # memory and its output back; steps are pipelined the way a serving loop
-    # overlaps them: two device buffer sets, inputs copied on one stream, the
-    # call on another, the output copied out on a third, ordered by events.
+    # ---- end to end through the public API (steady state: the pipeline is
+    # warmed up first, then at least 200 steps are timed)
     e2e = None
     if not args.no_e2e:
-        pin_q = w.q.pin_memory()
-        pin_bt = torch.from_numpy(w.block_table).pin_memory()
-        pin_sl = torch.from_numpy(w.seq_lens).pin_memory()
-        pin_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
-        dq = [q, torch.empty_like(q)]
-        dbt = [bt, torch.empty_like(bt)]
-        dsl = [sl, torch.empty_like(sl)]
-        dout = [out, torch.empty_like(out)]
-        s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-        e2e_steps = max(10, min(args.steps, 2000))
-        h2d = pin_q.numel() * 2 + pin_bt.numel() * 4 + pin_sl.numel() * 4
-        d2h = pin_out[0].numel() * 2
-        ev_in = [torch.cuda.Event() for _ in range(2)]
-        ev_comp = [torch.cuda.Event() for _ in range(2)]
-        ev_out = [torch.cuda.Event() for _ in range(2)]
-        torch.cuda.synchronize()
-        for e in ev_comp + ev_out:
-            e.record(s_comp)
-        t0 = time.perf_counter()
-        for i in range(e2e_steps):
-            j = i & 1
-            with torch.cuda.stream(s_in):
-                s_in.wait_event(ev_comp[j])          # set j no longer read by step i - 2
-                dq[j].copy_(pin_q, non_blocking=True)
-                dbt[j].copy_(pin_bt, non_blocking=True)
-                dsl[j].copy_(pin_sl, non_blocking=True)
-                ev_in[j].record(s_in)
-            with torch.cuda.stream(s_comp):
-                s_comp.wait_event(ev_in[j])
-                s_comp.wait_event(ev_out[j])         # out j copied out by step i - 2
-                if flush is not None:
-                    flush.zero_()
-                if w.mla:
-                    zl.decode_attn_mla(dq[j], k, dbt[j], dsl[j], page_size=w.page_size,
-                                       scale=w.scale, D_v=w.D_v, out=dout[j], workspace=ws,
-                                       max_seq_len=w.max_seq_len, stream=s_comp)
-                else:
-                    zl.decode_attn(dq[j], k, v, dbt[j], dsl[j], page_size=w.page_size,
-                                   scale=w.scale, out=dout[j], workspace=ws,
-                                   max_seq_len=w.max_seq_len, single_launch=args.single_launch,
-                                   shared_prefix_pages=npref, stream=s_comp)
-                ev_comp[j].record(s_comp)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(ev_comp[j])
-                pin_out[j].copy_(dout[j], non_blocking=True)
-                ev_out[j].record(s_out)
-        torch.cuda.synchronize()
-        e2e_s = (time.perf_counter() - t0) / e2e_steps
-        e2e = {"value": kv_bytes(w) * world / e2e_s / 1e9, "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "us_per_step": e2e_s * 1e6,
-               "note": "every step copies q, block table and seq_lens in from pinned host memory "
-                       "and its output back (host wall clock); steps pipelined over two buffer "
-                       "sets and three streams; the KV cache is device-resident state"
-                       + ("; includes the L2 flush" if flush is not None else "")}
+        e2e = c.e2e(max(200, min(args.steps, 2000)), 20, world)
 
     if rank != 0:
         if world > 1:
@@ -533,9 +682,7 @@ def run_ours(args, world, rank, local):
 
     kvb = kv_bytes(w)
     peak, peak_kind = measured_peaks()
-    # the roofline counts the bytes HBM has to deliver: a shared page once
-    algo = unique_kv_bytes(w) + io_bytes(w)
-    logical = kvb + io_bytes(w)
+    algo, logical = roofline_bytes(w)
     achieved = algo / (attn_ms * 1e-3) / 1e9
     cpu = None
     parity = None
@@ -543,8 +690,8 @@ def run_ours(args, world, rank, local):
         cpu_s, cpu_calls, cores, res = time_oracle(w)
         cpu = {"value": kvb / cpu_s / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"the whole workload per call, {cpu_calls} calls (median)"}
-        if ap is None:  # (with the append the device pools hold the new rows)
-            parity = parity_summary(out, lse, res)
+        if c.ap is None:  # (with the append the device pools hold the new rows)
+            parity = parity_summary(c.out, c.lse, res)
     line = {
         "metric": metric_name(args.workload, args.q_len),
         "value": kvb * world / (ms * 1e-3) / 1e9,
@@ -562,11 +709,7 @@ def run_ours(args, world, rank, local):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": dict(config_of(w, world), split_merge=(
-            "in the attention kernel (single launch)" if kind == "gqa" and args.single_launch
-            else "second launch (programmatic dependent launch)"),
-            step="kv append + attention" if ap is not None else "attention",
-            shared_prefix_pages=npref),
+        "config": config_of(w, world),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "kernel": f"{kind}_decode_kernel", "attn_us_per_launch": attn_ms * 1e3,
@@ -580,12 +723,30 @@ def run_ours(args, world, rank, local):
         "parity": parity,
         "e2e": e2e,
         "gpu_launches": launches,
-        "kv_append": append,
         "clocks": clocks,
     }
+    # options that change what a step is are named only when used
+    if kind == "gqa" and args.single_launch:
+        line["config"]["split_merge"] = "in the attention kernel (single launch)"
+    if c.ap is not None:
+        line["config"]["step"] = "kv append + attention"
+        line["kv_append"] = append
+    if c.npref:
+        line["config"]["shared_prefix_pages"] = c.npref
+    if args.no_hint:
+        line["config"]["max_seq_len"] = "not given"
     if w.mla:
-        flops = 2.0 * int(w.seq_lens.astype(np.int64).sum()) * w.q_len * w.Hq * (w.D_qk + w.D_v)
-        line["tensor"] = {"tflops": flops / (attn_ms * 1e-3) / 1e12, "flops_per_launch": flops}
+        fl = mla_flops(w)
+        tpeak, tpeak_kind = bf16_peak()
+        line["tensor"] = {"tflops": fl / (attn_ms * 1e-3) / 1e12, "flops_per_launch": fl,
+                          "frac_of_bf16_peak": fl / (attn_ms * 1e-3) / 1e12 / tpeak,
+                          "peak_kind": tpeak_kind}
+    if not args.no_workloads and world == 1 and args.workload == WORKLOAD and args.q_len == 1 \
+            and not (args.single_launch or args.with_append or args.shared_prefix or args.no_hint
+                     or args.batch):
+        del c
+        torch.cuda.empty_cache()
+        line["workloads"] = measure_extra(dev, 200, 5, oracle_seconds=3.0)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
@@ -610,6 +771,10 @@ def main():
                     help="GQA: merge split-KV partials inside the attention kernel")
     ap.add_argument("--q-len", type=int, default=1,
                     help="query tokens per sequence (llama3_8b_decode, mla_decode)")
+    ap.add_argument("--no-hint", action="store_true",
+                    help="pass no max_seq_len (the split plan is then decided on the device)")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="headline only: skip timing the other seeded configurations")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")

@@ -28,13 +28,17 @@
  * Conventions for every entry point:
  *   - Ownership: the caller owns every buffer. The library never allocates or
  *     frees device memory and never synchronises; it enqueues kernels on the
- *     given stream only. Its only state is host-side (per-device attributes).
+ *     given stream only. Its state is host-side (per-device attributes), with
+ *     one exception: the static scratch array of zl_decode_attn_noalloc
+ *     (ZL_NOALLOC_WORKSPACE_BYTES, held by every GPU that loads the library
+ *     until the process exits).
  *   - Host errors return synchronously and launch nothing.
  *   - Device data errors (a page id outside [0, num_pages), a seq_len outside
  *     [0, block_table_stride * page_size], a pipeline wait that timed out)
  *     cannot be returned without a sync: the kernel ORs a ZL_DEVERR_* bit into
  *     *err_flags (when err_flags is not NULL) and writes zeros (lse = -inf)
- *     for the affected sequence. Nothing traps.
+ *     for the affected query rows: every row of a sequence with a bad length,
+ *     and every row whose visible tokens reach a bad page. Nothing traps.
  *   - seq_lens[b] = 0 gives out = 0 and lse = -inf; that is not an error.
  *   - Results depend only on logical content: remapping pages gives
  *     bit-identical output, and repeated calls are bit-identical.
@@ -110,7 +114,9 @@ typedef struct {
      B * Hkv; counters left by a call that stopped on a device error are
      recognised (each call tags its counts) and ignored. Anything else
      written into that range (a call without the flag, a call with a larger
-     B * Hkv, other data) needs a new zero fill of it first.
+     B * Hkv, other data) needs a new zero fill of it first: the tag makes
+     such leftovers harmless unless their upper 32 bits happen to equal the
+     call's tag, and only a zero fill rules that out.
      Otherwise: contents need no initialisation. */
   void* workspace;
   size_t workspace_bytes;
@@ -120,7 +126,13 @@ typedef struct {
 
   /* Number of CTAs of the attention kernel; 0 = one wave on this device.
      Any value >= 1 gives the same result within fp32 rounding: the work is
-     split into that many equal token ranges and merged. */
+     split into that many equal token ranges (at most one per 16-token tile;
+     CTAs beyond that take none) and merged. With 0 (and no shared prefix),
+     zl_decode_attn also decides on the device, from seq_lens, whether every
+     (sequence, head group) is short enough for a CTA of its own, the rule
+     that max_seq_len lets the host apply before the launch (see
+     zl_decode_attn); decided on the device, the merge kernel is still
+     launched but has nothing to do. */
   int32_t num_ctas;
 
   /* Optional profiling events recorded on the stream immediately before and
@@ -174,7 +186,9 @@ typedef struct {
  *   every (sequence, head group) is short (at most 512 KB of K and V), each
  *   gets a CTA of its own and no merge is launched. A query row that
  *   sees no token (seq_lens[b] < q_len) gives out = 0 and lse = -inf. A bad
- *   page id zeroes every query row of its sequence and kv head.
+ *   page id zeroes (out = 0, lse = -inf) every query row whose visible tokens
+ *   reach that page, and only those: with q_len > 1, a bad page that holds
+ *   only the newest tokens zeroes only the rows of the queries that see them.
  *   Anything else returns ZL_ERR_UNSUPPORTED (or ZL_ERR_INVALID_ARG when the
  *   value is not meaningful at all, e.g. Hkv = 0).
  */
@@ -220,16 +234,22 @@ zl_status zl_decode_attn_launches(const zl_decode_attn_params* params, int32_t* 
  *     workspace_bytes are ignored.
  *   - The scratch is one array of ZL_NOALLOC_WORKSPACE_BYTES in the library's
  *     own device memory; every GPU that loads the library holds it until the
- *     process exits. A call whose zl_decode_attn_workspace_size() exceeds it
- *     returns ZL_ERR_WORKSPACE (a smaller num_ctas shrinks the need).
+ *     process exits. With num_ctas = 0, a call whose default grid needs more
+ *     workspace than that runs on the largest grid whose workspace fits (the
+ *     result is the same within fp32 rounding; only the split differs). With
+ *     num_ctas > 0, or when even one CTA does not fit, it returns
+ *     ZL_ERR_WORKSPACE.
  *   - The first call on each device looks up the array's device address (with
- *     that device current); make that first call before any stream capture.
+ *     that device current), and so does the first call in a new context on it
+ *     (after cudaDeviceReset); make those calls before any stream capture.
  *   - Calls allocate nothing: no cudaMalloc, cudaFree or allocating library
- *     routine. All calls share the one array, which starts zero-filled and
- *     keeps the last call's contents; every call leaves its arrival counters
- *     at zero, as the workspace contract of zl_decode_attn asks, so it never
- *     needs clearing. Calls that overlap on the GPU (other streams, other
- *     threads) race on it: serialise them.
+ *     routine. All calls share the one array, which keeps the last call's
+ *     contents. A call with ZL_DECODE_SINGLE_LAUNCH first zero-fills its
+ *     arrival counters (the first 8 * B * Hkv bytes of the array) with
+ *     cudaMemsetAsync on the stream, so whatever an earlier call left there
+ *     never matters; other calls need nothing cleared. Calls that overlap on
+ *     the GPU (other streams, other threads) race on the array: serialise
+ *     them.
  */
 #define ZL_NOALLOC_WORKSPACE_BYTES (8u << 20)
 zl_status zl_decode_attn_noalloc(const zl_decode_attn_params* params, zl_stream_t stream);

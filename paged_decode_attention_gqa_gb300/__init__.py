@@ -36,6 +36,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA = range(5)
 SINGLE_LAUNCH = 1  # ZL_DECODE_SINGLE_LAUNCH
 TEST_STALL = 0x80000000  # ZL_DECODE_TEST_STALL (failure-detection test hook)
 DEVERR_BAD_PAGE, DEVERR_BAD_SEQ_LEN, DEVERR_TIMEOUT, DEVERR_BAD_PREFIX = 1, 2, 4, 8
+NOALLOC_WORKSPACE_BYTES = 8 << 20  # ZL_NOALLOC_WORKSPACE_BYTES
 
 
 class ZlError(RuntimeError):

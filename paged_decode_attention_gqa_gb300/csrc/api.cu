@@ -97,10 +97,10 @@ struct GqaPlan {
 // GQA path takes the (token, head) rows of a kv head in groups of at most 16).
 constexpr int kMaxQueryTokens = 128;
 constexpr int kMaxGroupHeads = 128;
-// A call whose longest (sequence, head group) unit has at most this many K and
-// V bytes (known from max_seq_len) gives each unit a CTA of its own and skips
-// the merge: one CTA streams that in about the time a merge launch takes.
-constexpr int64_t kUnitCutBytes = 512 * 1024;
+// A call whose longest (sequence, head group) unit has at most
+// zl::kGqaUnitCutBytes of K and V (known from max_seq_len) gives each unit a
+// CTA of its own and skips the merge launch. Without max_seq_len the kernels
+// take the same decision on the device (GqaParams::auto_cut).
 
 zl_status gqa_validate_shape(const zl_decode_attn_params* a) {
   if (!a || a->struct_size != sizeof(zl_decode_attn_params)) return ZL_ERR_INVALID_ARG;
@@ -179,7 +179,7 @@ zl_status gqa_plan(const zl_decode_attn_params* a, GqaPlan* plan) {
       const int64_t units = int64_t(a->B) * plan->nhg;
       // K and V bytes of the longest unit (sequence, head group).
       const int64_t unit_bytes = max_tiles * zl::kGqaTile * plan->hpc * zl::kGqaHeadDim * 2 * 2;
-      if (units <= grid && unit_bytes <= kUnitCutBytes) {
+      if (units <= grid && unit_bytes <= zl::kGqaUnitCutBytes) {
         // Short contexts: one CTA per whole unit. Streaming the longest unit
         // alone costs less than cutting units and merging their pieces.
         plan->unit_cut = true;
@@ -393,6 +393,7 @@ zl_status zl_decode_attn(const zl_decode_attn_params* a, zl_stream_t stream) {
   p.test_stall = (a->flags & ZL_DECODE_TEST_STALL) ? 1 : 0;
   p.B = a->B;
   p.unit_cut = plan.unit_cut ? 1 : 0;
+  p.auto_cut = (a->num_ctas == 0 && !plan.unit_cut && plan.prefix_tiles == 0) ? 1 : 0;
   p.q_total = a->q_len;
   p.Hq = a->Hq;
   p.Hkv = a->Hkv;

@@ -92,14 +92,37 @@ __device__ __forceinline__ int locate_seq(const int* prefix, int B, int nhg, int
 // First tile of CTA cc's range when W tiles are cut into G ranges
 // [floor(cc W / G), floor((cc+1) W / G)), from Wq = W / G and Wr = W % G:
 // floor(cc W / G) = cc Wq + floor(cc Wr / G), and cc Wr < G^2 < 2^32 (G is
-// at most 65535), so no 64-bit division is needed.
+// at most 65535), so no 64-bit division is needed. The launches cut into
+// G = min(CTAs, W) ranges (at least 1), so every range below G holds a tile:
+// a unit cut between CTAs c_lo..c_hi has exactly c_hi - c_lo + 1 pieces, and
+// owner() finds c_lo and c_hi without walking the CTAs.
 struct TileCut {
   int64_t Wq;
   uint32_t Wr, G;
+  __device__ __forceinline__ TileCut(int64_t W, int ctas) {
+    const int64_t g = W < int64_t(ctas) ? (W > 0 ? W : 1) : int64_t(ctas);
+    G = uint32_t(g);
+    Wq = W / g;
+    Wr = uint32_t(W % g);
+  }
   __device__ __forceinline__ int64_t start(int cc) const {
     return int64_t(cc) * Wq + int64_t((uint32_t(cc) * Wr) / G);
   }
+  // The CTA whose range holds tile x: the largest cc with start(cc) <= x,
+  // i.e. ceil((x + 1) G / W) - 1.
+  __device__ __forceinline__ int owner(int64_t x) const {
+    const int64_t W = Wq * G + Wr;
+    return int(((x + 1) * int64_t(G) + W - 1) / W) - 1;
+  }
 };
+
+// Whether every unit of the launch is short enough for a CTA of its own (the
+// unit cut): at most kGqaUnitCutBytes of K and V in the longest unit (n_max
+// tiles of hpc kv heads), and no more units than the group's CTAs.
+__device__ __forceinline__ bool short_units(int64_t units, int n_max, int hpc, int ctas) {
+  const int64_t tile_bytes = int64_t(kGqaTile) * hpc * kGqaHeadDim * 2 * 2;
+  return units <= ctas && int64_t(n_max) * tile_bytes <= kGqaUnitCutBytes;
+}
 
 // 64-bit compare-and-swap with acquire-release semantics at GPU scope: the
 // arriving warp's partial rows (ordered before it by __syncwarp) are released
@@ -144,22 +167,14 @@ __device__ __forceinline__ bool arrive_last(unsigned long long* word, uint32_t e
   return false;
 }
 
-// The CTAs holding pieces of a split unit (first tile U0, n tiles) that CTA c
-// takes part in: c_lo owns tile U0, c_hi the last tile, c lies between them.
-// Returns how many of them have a non-empty range (one piece each).
-__device__ __forceinline__ int split_cta_span(const TileCut& cut, int64_t U0, int n, int c,
-                                              int& c_lo, int& c_hi) {
-  int pieces = 1;
-  c_lo = c_hi = c;
-  while (cut.start(c_lo) > U0) {
-    --c_lo;
-    pieces += cut.start(c_lo) < cut.start(c_lo + 1) ? 1 : 0;
-  }
-  while (cut.start(c_hi + 1) < U0 + n) {
-    ++c_hi;
-    pieces += cut.start(c_hi) < cut.start(c_hi + 1) ? 1 : 0;
-  }
-  return pieces;
+// The CTAs holding pieces of a split unit (first tile U0, n tiles): c_lo owns
+// tile U0, c_hi the last tile. Every range holds a tile, so each CTA from
+// c_lo to c_hi has one piece; returns their number.
+__device__ __forceinline__ int split_cta_span(const TileCut& cut, int64_t U0, int n, int& c_lo,
+                                              int& c_hi) {
+  c_lo = cut.owner(U0);
+  c_hi = cut.owner(U0 + n - 1);
+  return c_hi - c_lo + 1;
 }
 
 // Log-sum-exp merge of the R rows of kv head w (of CTA head group hg) over the
@@ -171,11 +186,12 @@ __device__ __forceinline__ int split_cta_span(const TileCut& cut, int64_t U0, in
 // Merging the same pieces with any batch size gives the same bits.
 // Running log-sum-exp merge of kMergeRows rows (base-2 lse): a running max,
 // the rescaled weight sum and the rescaled sum of normalised outputs. A
-// source with lse NaN (a bad page) marks the rows bad; lse -inf weighs 0.
+// source row with lse NaN (its piece met a bad page) marks that row bad (bit
+// k of `bad`); lse -inf weighs 0.
 struct MergeAcc {
   float mx[kMergeRows], den[kMergeRows];
   float4 acc[kMergeRows];
-  bool bad;
+  uint32_t bad;
   __device__ __forceinline__ void init() {
 #pragma unroll
     for (int k = 0; k < kMergeRows; ++k) {
@@ -183,10 +199,10 @@ struct MergeAcc {
       den[k] = 0.f;
       acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    bad = false;
+    bad = 0u;
   }
   __device__ __forceinline__ void add(int k, float l, float4 o) {
-    bad |= isnan(l);
+    bad |= isnan(l) ? 1u << k : 0u;
     const float mn = fmaxf(mx[k], l);
     if (mn != -CUDART_INF_F && !isnan(l)) {
       const float a = ex2_approx(mx[k] - mn), wgt = ex2_approx(l - mn);
@@ -270,7 +286,7 @@ __device__ __forceinline__ void merge_write_out(const MergeAcc& m, const GqaPara
     if (k < nrows) {
       const int r = r0 + k;
       const int64_t orow = (int64_t(b) * p.q_total + tok0 + r / gh) * p.Hq + head0 + r % gh;
-      const bool none = m.bad || !(m.den[k] > 0.f);
+      const bool none = ((m.bad >> k) & 1u) || !(m.den[k] > 0.f);
       const float inv = none ? 0.f : 1.f / m.den[k];
       uint2 packed = make_uint2(0u, 0u);
       if (!none) {
@@ -348,6 +364,7 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
   volatile int* abort_flag = stage_bad + NS;
   int* prefix = stage_bad + NS + 4;
   int* split_rec = prefix + kMaxBatch + 1;  // [HPC][2]: b | hg << 12 of a split piece, or -1
+  int* unit_max = stage_bad + NS + 1;       // tiles of the longest unit
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int B = p.B;
@@ -383,7 +400,7 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
   if (warp == 0) {
     const int per = (V + 31) / 32;
     const int v0 = lane * per;
-    int local = 0;
+    int local = 0, nmax = 0;
     for (int i = 0; i < per; ++i) {
       const int v = v0 + i;
       if (v < V) {
@@ -391,7 +408,9 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
           const int L = p.seq_lens[v - NG];
           if (!(L >= 0 && int64_t(L) <= cap)) raise_error(p.err_flags, kErrBadLen);
         }
-        local += unit_tiles(v);
+        const int n = unit_tiles(v);
+        local += n;
+        nmax = max(nmax, n);
       }
     }
     int incl = local;
@@ -399,7 +418,9 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
     for (int off = 1; off < 32; off <<= 1) {
       const int x = __shfl_up_sync(0xffffffffu, incl, off);
       if (lane >= off) incl += x;
+      nmax = max(nmax, __shfl_xor_sync(0xffffffffu, nmax, off));
     }
+    if (lane == 0) unit_max[0] = nmax;
     int run = incl - local;
     for (int i = 0; i < per; ++i) {
       const int v = v0 + i;
@@ -447,10 +468,14 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
   const int tok0 = rg.tok0, qlen = rg.qlen, gh = rg.gh;
   const int nhg = p.nhg;
   const int64_t W = int64_t(nhg) * prefix[V];
-  const TileCut cut{W / G, uint32_t(W % G), uint32_t(G)};
-  int64_t s_c = cut.start(c);
-  int64_t e_c = cut.start(c + 1);
-  if (MODE == kModePlain && p.unit_cut) {
+  const TileCut cut(W, G);
+  // CTAs past the cut's G (more CTAs than tiles) take no tiles.
+  int64_t s_c = c < int(cut.G) ? cut.start(c) : W;
+  int64_t e_c = c < int(cut.G) ? cut.start(c + 1) : W;
+  const bool unit_cut =
+      MODE == kModePlain &&
+      (p.unit_cut || (p.auto_cut && short_units(int64_t(V) * nhg, unit_max[0], HPC, G)));
+  if (unit_cut) {
     // Unit (v, hg) holds tiles [nhg * prefix[v] + hg * n, + n) of the line.
     s_c = e_c = 0;
     if (c < int64_t(V) * nhg) {
@@ -606,7 +631,9 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
     float o[16][4];
 #pragma unroll
     for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-    int bad = 0;
+    // Rows (a, b) of this thread whose visible tokens reach a tile over a bad
+    // page: those rows, and only those, are written as zeros.
+    bool bad_a = false, bad_b = false;
 
     // One row's online-softmax step in base 2 over this thread's four scores
     // (tokens 2t4, 2t4+1, 2t4+8, 2t4+9 of the tile; vis = visible tokens of
@@ -645,7 +672,10 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
         }
         return;
       }
-      bad |= stage_bad[stage];
+      if (stage_bad[stage]) {
+        bad_a |= !CAUSAL || tok0 < lim_a;
+        bad_b |= !CAUSAL || tok0 < lim_b;
+      }
       const uint32_t kbase = sbase + stage * Cfg::kStageBytes + w * (kGqaTile * 128);
       const uint32_t vbase = kbase + 2 * Cfg::kHalfBytes;
 
@@ -723,15 +753,16 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
       l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
       l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
     }
-    if (bad && lane == 0) raise_error(p.err_flags, kErrBadPage);
+    if (__any_sync(0xffffffffu, bad_a || bad_b) && lane == 0) raise_error(p.err_flags, kErrBadPage);
 #pragma unroll
     for (int half = 0; half < (ROWS16 ? 2 : 1); ++half) {
       const int r = half ? rb : ra;
       if (r >= R_act) continue;
       const float l = half ? l1 : l0;
       const float m = half ? m1 : m0;
-      // A piece that met a bad page, or a row that saw no token, is written as
-      // zeros with lse = -inf (weight 0 in the merge).
+      const bool bad = half ? bad_b : bad_a;
+      // A row whose piece met a bad page, or a row that saw no token, is
+      // written as zeros with lse = -inf (weight 0 in the merge).
       const bool none = bad || !(l > 0.f);
       const float inv = none ? 0.f : 1.f / l;
       const float lse2 = none ? -CUDART_INF_F : m + log2f(l);
@@ -784,7 +815,7 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
       const int b = rec & 4095, hg = rec >> 12;
       const int n = prefix[b + 1] - prefix[b];
       int c_lo, c_hi;
-      const int pieces = split_cta_span(cut, int64_t(nhg) * prefix[b] + int64_t(hg) * n, n, c,
+      const int pieces = split_cta_span(cut, int64_t(nhg) * prefix[b] + int64_t(hg) * n, n,
                                         c_lo, c_hi);
       if (arrive_last(p.ws_count + int64_t(b) * p.Hkv + hg * HPC + w, p.epoch, pieces,
                       p.err_flags))
@@ -798,7 +829,7 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
     const int n = prefix[b + 1] - prefix[b];
     const int64_t U0 = int64_t(nhg) * prefix[b] + int64_t(hg) * n;
     int c_lo, c_hi;
-    split_cta_span(cut, U0, n, c, c_lo, c_hi);
+    split_cta_span(cut, U0, n, c_lo, c_hi);
     merge_split_rows<4>(p, cut, vcta - c, U0, c_lo, c_hi, b, tok0, w,
                         (hg * HPC + w) * g + rg.hoff, gh, p.gh * p.q_len, 0, gh * qlen, lane);
   }
@@ -825,10 +856,6 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
 }
 
 
-// CTA that owns global tile x when W tiles are cut into G ranges.
-__device__ __forceinline__ int cta_of_tile(int64_t x, int64_t W, int G) {
-  return int(((x + 1) * G + W - 1) / W) - 1;
-}
 
 // Split-KV merge as its own launch (when the attention kernel runs without
 // FUSED), one warp per block of kMergeRows rows of a (sequence, kv head), with
@@ -862,17 +889,20 @@ __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ 
   // launch only after its own dependency wait, so it is final here. Units are
   // the ng prefix groups (prefix_tiles tiles each), then the sequences.
   const int NG = MODE == kModeShared ? p.ng : 0;
-  int before = 0, all = 0;  // tiles of sequences before b, of every sequence
+  // tiles of sequences before b, of every sequence, of the longest one
+  int before = 0, all = 0, nmax = 0;
   if (live) {
     for (int s = lane; s < p.B; s += 32) {
       const int t = seq_unit_tiles<MODE>(p, p.seq_lens[s]);
       all += t;
       before += s < b ? t : 0;
+      nmax = max(nmax, t);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       all += __shfl_xor_sync(0xffffffffu, all, off);
       before += __shfl_xor_sync(0xffffffffu, before, off);
+      nmax = max(nmax, __shfl_xor_sync(0xffffffffu, nmax, off));
     }
   }
   const int n = live ? seq_unit_tiles<MODE>(p, p.seq_lens[b]) : 0;
@@ -886,10 +916,13 @@ __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ 
   const int head0 = kvh * p.g + rg.hoff;  // the group's first query head
   const int PT = MODE == kModeShared ? p.prefix_tiles : 0;
   const int64_t W = int64_t(p.nhg) * (int64_t(NG) * PT + all);
-  const TileCut cut{W / G, uint32_t(W % G), uint32_t(G)};
+  const TileCut cut(W, G);
   const int64_t U0 = int64_t(p.nhg) * (int64_t(NG) * PT + before) + int64_t(hg) * n;
-  const int c_lo = n ? cta_of_tile(U0, W, G) : 0, c_hi = n ? cta_of_tile(U0 + n - 1, W, G) : 0;
+  const int c_lo = n ? cut.owner(U0) : 0, c_hi = n ? cut.owner(U0 + n - 1) : 0;
   if constexpr (MODE == kModePlain) {
+    // a unit-cut launch (chosen on the device, as the attention kernel did)
+    // left every unit whole
+    if (p.auto_cut && short_units(int64_t(p.B) * p.nhg, nmax, p.hpc, G)) return;
     if (n == 0 || c_lo == c_hi) return;
     // PIECES pieces per round trip to L2 (the host takes 6 when the merge grid
     // fits in one wave at the registers that needs, else 2).
@@ -903,7 +936,7 @@ __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ 
       const int vp = b / p.sgs;  // the group's prefix unit (each has PT tiles)
       const int np = PT;
       const int64_t P0 = int64_t(p.nhg) * (int64_t(vp) * PT) + int64_t(hg) * np;
-      const int p_lo = cta_of_tile(P0, W, G), p_hi = cta_of_tile(P0 + np - 1, W, G);
+      const int p_lo = cut.owner(P0), p_hi = cut.owner(P0 + np - 1);
       if (p_lo == p_hi)
         merge_add_store(m, p, p.pre_o, p.pre_lse, b, tok0, head0, gh, r0, nrows, lane);
       else

@@ -11,6 +11,10 @@ namespace zl {
 constexpr int kGqaTile = 16;     // tokens per pipeline stage of the GQA kernel
 constexpr int kGqaHeadDim = 128; // D_qk = D_v
 constexpr int kMaxBatch = 4096;  // sequences per call (prefix table lives in smem)
+// A call whose longest (sequence, head group) unit has at most this many K and
+// V bytes gives each unit a CTA of its own and merges nothing (when the units
+// fit in the grid): one CTA streams that in about the time a merge costs.
+constexpr int64_t kGqaUnitCutBytes = 512 * 1024;
 
 // Everything the GQA attention kernel reads.
 struct GqaParams {
@@ -64,6 +68,11 @@ struct GqaParams {
   // unit is cut and there is nothing to merge (the host picks this for short
   // contexts, where a merge launch would cost more than the attention).
   int unit_cut;
+  // 1: the grid is the default one and the host knew no length bound; the
+  // kernels then choose the unit cut above themselves, from seq_lens, when
+  // every unit is short and the units fit in the group's CTAs (the attention
+  // and merge kernels take the same decision from the same lengths).
+  int auto_cut;
   int hpc;             // kv heads per CTA
   int nhg;             // Hkv / hpc head groups
   float scale_log2;    // scale * log2(e)

@@ -37,7 +37,7 @@ def device_inputs(wl: Workload):
 
 
 def run_gpu(wl: Workload, inputs=None, *, num_ctas=0, max_seq_len=None, block_table=None,
-            seq_lens=None, shared_prefix_pages=0) -> GpuRun:
+            seq_lens=None, shared_prefix_pages=0, single_launch=False) -> GpuRun:
     d = inputs or device_inputs(wl)
     bt = d["bt"] if block_table is None else block_table
     sl = d["sl"] if seq_lens is None else seq_lens
@@ -52,7 +52,8 @@ def run_gpu(wl: Workload, inputs=None, *, num_ctas=0, max_seq_len=None, block_ta
         out = zl.decode_attn(d["q"], d["k"], d["v"], bt, sl, page_size=wl.page_size,
                              scale=wl.scale, lse=lse, err_flags=err, num_ctas=num_ctas,
                              max_seq_len=msl, layout=wl.layout,
-                             shared_prefix_pages=shared_prefix_pages)
+                             shared_prefix_pages=shared_prefix_pages,
+                             single_launch=single_launch)
     torch.cuda.synchronize()
     return GpuRun(out, lse, err)
 

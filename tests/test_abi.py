@@ -148,3 +148,21 @@ def test_append_null_params_and_no_cpu_fallback():
     for over in (dict(), dict(v_new=None, v_pool=None, D_k=576, D_v=0)):
         p = _append_params(**over)
         assert zl.lib().zl_kv_append(ctypes.byref(p), None) == zl.ERR_CUDA
+
+
+def test_binding_constants_match_the_header():
+    """The Python names mirror the header's #defines."""
+    import re
+    text = open(zl.HEADER).read()
+
+    def define(name):
+        m = re.search(r"#define\s+" + name + r"\s+\(?([0-9a-fx]+)u?(?:\s*<<\s*(\d+))?", text)
+        assert m, name
+        v = int(m.group(1), 0)
+        return v << int(m.group(2)) if m.group(2) else v
+
+    assert define("ZL_DECODE_SINGLE_LAUNCH") == zl.SINGLE_LAUNCH
+    assert define("ZL_DECODE_TEST_STALL") == zl.TEST_STALL
+    assert define("ZL_DEVERR_BAD_PAGE") == zl.DEVERR_BAD_PAGE
+    assert define("ZL_DEVERR_BAD_PREFIX") == zl.DEVERR_BAD_PREFIX
+    assert define("ZL_NOALLOC_WORKSPACE_BYTES") == zl.NOALLOC_WORKSPACE_BYTES

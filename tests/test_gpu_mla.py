@@ -68,6 +68,28 @@ def test_mla_empty_and_bad_page():
     assert_close(g.out64(), ref, "mla empty/bad")
 
 
+@pytest.mark.parametrize("num_ctas", [0, 12])
+def test_mla_bad_page_seen_by_the_newest_token_only(num_ctas):
+    """Two query tokens; the bad page holds only the newest token (position
+    L - 1 starts its page), so only the second token's rows are zeroed."""
+    P = 64
+    lens = [P + 1, 3 * P + 1, 150]
+    w = wl.random_case(615, B=len(lens), Hq=128, Hkv=1, D=576, D_v=512, mla=True,
+                       page_size=P, lens=lens, pool_factor=1.5, q_len=2)
+    d = device_inputs(w)
+    bt = w.block_table.copy()
+    bt[0, 1] = -1
+    bt[1, 3] = w.num_pages
+    g = run_gpu(w, d, block_table=torch.from_numpy(bt).cuda(), num_ctas=num_ctas)
+    assert int(g.err.item()) & zl.DEVERR_BAD_PAGE
+    ref, ref_lse, st = run_oracle(w, block_table=bt)
+    assert st & 1
+    assert_close(g.out64(), ref, "mla newest-page out")
+    assert_close(g.lse64(), ref_lse, "mla newest-page lse")
+    for b in (0, 1):
+        assert (g.out[b, 1] == 0).all() and (g.out[b, 0] != 0).any()
+
+
 def test_mla_full_workload():
     _parity(wl.mla_decode())
 

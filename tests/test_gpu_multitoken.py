@@ -95,6 +95,40 @@ def test_bad_first_page_zeroes_every_row():
     assert torch.all(g.out[1].float() == 0)
 
 
+@pytest.mark.parametrize("Hq,q_len,num_ctas,single", [
+    (32, 3, 0, False),     # one row group of 12 rows, whole units
+    (32, 3, 40, False),    # units cut between CTAs: the bad rows cross the merge
+    (32, 3, 40, True),     # ... merged inside the attention kernel
+    (32, 8, 0, False),     # two row groups of 4 tokens in every CTA
+    (32, 8, 40, False),
+    (64, 2, 40, False),    # group of 8: 16 rows, the upper half of the tile
+])
+def test_bad_page_seen_by_the_newest_token_only(Hq, q_len, num_ctas, single):
+    """A bad page that holds only the newest token (position L - 1 is the first
+    slot of its page): only the last query row sees it, so only that row of the
+    sequence is zeroed (lse = -inf); the rows before it keep their values. The
+    oracle zeroes exactly the rows whose visible range holds the bad page."""
+    P = 16
+    lens = [P * 2 + 1, P * 3 + 1, 70, 45]  # sequences 0 and 1 end one token into a page
+    w = wl.random_case(845 + Hq + q_len, B=len(lens), Hq=Hq, Hkv=8, lens=lens, q_len=q_len,
+                       page_size=P)
+    d = device_inputs(w)
+    bt = d["bt"].clone()
+    bt[0, 2] = -3                  # the page of sequence 0's newest token
+    bt[1, 3] = w.num_pages + 1     # the page of sequence 1's newest token
+    g = run_gpu(w, d, block_table=bt, num_ctas=num_ctas, single_launch=single)
+    assert int(g.err.item()) & zl.DEVERR_BAD_PAGE
+    ref, ref_lse, st = run_oracle(w, block_table=bt.cpu().numpy())
+    assert st & 1
+    assert_close(g.out64(), ref, "out")
+    assert_close(g.lse64(), ref_lse, "lse")
+    out = g.out.float().cpu()
+    for b in (0, 1):
+        assert torch.all(out[b, -1] == 0)
+        assert torch.all(torch.isneginf(g.lse[b, -1].cpu()))
+        assert torch.all(out[b, :-1].abs().sum(-1) > 0)  # the other rows are not zeroed
+
+
 def test_full_size_llama3_8b_mtp_sampled():
     """Llama-3-8B decode shape at batch 64 with 4 query tokens per sequence,
     sampled rows against the oracle at full context lengths."""
