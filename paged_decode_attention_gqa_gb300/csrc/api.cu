@@ -265,7 +265,7 @@ zl_status mla_plan(const zl_decode_attn_params* a, MlaPlan* plan) {
   plan->off_span = plan->off_split + round_up((size_t(clusters) + 1) * sizeof(int32_t), 256);
   plan->off_lse = plan->off_span + round_up(units * 2 * sizeof(int32_t), 256);
   plan->off_o = plan->off_lse + round_up(rows * sizeof(float), 256);
-  plan->bytes = plan->off_o + rows * zl::kMlaDv * sizeof(__nv_bfloat16);
+  plan->bytes = plan->off_o + rows * zl::kMlaDv * sizeof(float);
   return ZL_OK;
 }
 
@@ -507,7 +507,7 @@ zl_status zl_decode_attn_mla(const zl_decode_attn_params* a, zl_stream_t stream)
   p.ws_split = reinterpret_cast<int32_t*>(ws + plan.off_split);
   p.ws_span = reinterpret_cast<int32_t*>(ws + plan.off_span);
   p.ws_lse = reinterpret_cast<float*>(ws + plan.off_lse);
-  p.ws_o = reinterpret_cast<__nv_bfloat16*>(ws + plan.off_o);
+  p.ws_o = reinterpret_cast<float*>(ws + plan.off_o);
   p.err_flags = a->err_flags;
   p.B = a->B;
   p.q_len = a->q_len;

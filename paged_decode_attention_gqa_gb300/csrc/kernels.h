@@ -97,7 +97,7 @@ struct MlaParams {
   int32_t* ws_prefix;   // [B + 1] tile prefix sums
   int32_t* ws_split;    // [clusters + 1] first tile of each cluster's range
   int32_t* ws_span;     // [B][2] first and last cluster holding tiles of each unit
-  __nv_bfloat16* ws_o;  // [clusters][2][128][512] normalised partial outputs (bf16)
+  float* ws_o;          // [clusters][2][128][512] normalised partial outputs (fp32)
   float* ws_lse;        // [clusters][2][128] base-2 lse of partials (NaN = bad piece)
   uint32_t* err_flags;
   int B, q_len, page_size, num_pages;

@@ -698,11 +698,20 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
           float f[32];
 #pragma unroll
           for (int k = 0; k < 32; ++k) f[k] = bad ? 0.f : __uint_as_float(o[h][k]) * inv;
-          // a whole unit goes to out; a piece of one to this cluster's partial slot
-          __nv_bfloat16* dst =
-              partial ? p.ws_o + ((int64_t(cid) * 2 + slot) * kRows + row) * kMlaDv + col
-                      : p.out + (int64_t(b) * kRows + row) * kMlaDv + col;
-          const bool v8 = partial || p.out_align32;
+          if (partial) {
+            // a piece of a unit: fp32 into this cluster's partial slot
+            float* pdst = p.ws_o + ((int64_t(cid) * 2 + slot) * kRows + row) * kMlaDv + col;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              st_global_v8(pdst + 8 * k, __float_as_uint(f[8 * k]), __float_as_uint(f[8 * k + 1]),
+                           __float_as_uint(f[8 * k + 2]), __float_as_uint(f[8 * k + 3]),
+                           __float_as_uint(f[8 * k + 4]), __float_as_uint(f[8 * k + 5]),
+                           __float_as_uint(f[8 * k + 6]), __float_as_uint(f[8 * k + 7]));
+            continue;
+          }
+          // a whole unit: bf16 to out
+          __nv_bfloat16* dst = p.out + (int64_t(b) * kRows + row) * kMlaDv + col;
+          const bool v8 = p.out_align32;
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
             uint32_t w[8];
@@ -789,13 +798,9 @@ __global__ void __launch_bounds__(128) mla_merge_kernel(const __grid_constant__ 
       // clusters without tiles hold no partial of this unit
       live[i] = c0 + i <= c_hi && p.ws_split[c] != p.ws_split[c + 1];
       lse[i] = p.ws_lse[wrow];
-      const uint2* src = reinterpret_cast<const uint2*>(p.ws_o + wrow * kMlaDv);
+      const float4* src = reinterpret_cast<const float4*>(p.ws_o + wrow * kMlaDv);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint2 u = src[lane + 32 * k];
-        const float2 lo = unpack_bf16x2(u.x), hi = unpack_bf16x2(u.y);
-        v[i][k] = make_float4(lo.x, lo.y, hi.x, hi.y);
-      }
+      for (int k = 0; k < 4; ++k) v[i][k] = src[lane + 32 * k];
     }
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
