@@ -103,9 +103,10 @@ def test_noalloc_single_launch_after_calls_of_other_shapes():
 
 
 def test_noalloc_takes_a_smaller_grid_when_the_default_one_does_not_fit():
-    """32 query heads on one kv head at the default grid need more partial
-    slots than the array holds; the call runs on a grid that fits instead."""
-    w = wl.random_case(923, B=12, Hq=32, Hkv=1, max_len=3000)
+    """The 70B head shape (64 query heads over 8 kv heads) at the default grid
+    needs more partial slots than the array holds (152 CTAs x 2 slots x 8 kv
+    heads x 8 rows, ~10 MB); the call runs on a grid that fits instead."""
+    w = wl.random_case(923, B=12, Hq=64, Hkv=8, max_len=3000)
     d = device_inputs(w)
     out = torch.empty(w.B, 1, w.Hq, 128, dtype=torch.bfloat16, device="cuda")
     p = _params(w, d, out, None, max_seq_len=0)
