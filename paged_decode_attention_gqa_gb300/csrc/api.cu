@@ -167,10 +167,14 @@ zl_status gqa_plan(const zl_decode_attn_params* a, GqaPlan* plan) {
   const int rows_per_warp = plan->prefix_tiles > 0 ? plan->sgs * rps : rps;
   int grid = a->num_ctas;
   if (grid == 0) {
+    // the kernel's tile-offset table: one entry per unit (prefix groups and
+    // sequences) plus the total; the launch takes the same layout
+    const bool small = (plan->prefix_tiles > 0 ? plan->ng : 0) + a->B + 1 <= zl::kSmallTable;
     const int per_sm =
         plan->prefix_tiles > 0
-            ? zl::gqa_shared_ctas_per_sm(plan->hpc, rows_per_warp > 8, a->q_len > 1, dev.device)
-            : zl::gqa_ctas_per_sm(plan->hpc, rps > 8, a->q_len > 1, plan->fused, plan->tg,
+            ? zl::gqa_shared_ctas_per_sm(plan->hpc, rows_per_warp > 8, a->q_len > 1, small,
+                                         dev.device)
+            : zl::gqa_ctas_per_sm(plan->hpc, rps > 8, a->q_len > 1, plan->fused, plan->tg, small,
                                   dev.device);
     if (per_sm < 1) return ZL_ERR_CUDA;
     grid = dev.sms * per_sm;

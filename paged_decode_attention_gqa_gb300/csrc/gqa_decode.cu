@@ -34,7 +34,7 @@ auto dispatch(int hpc, bool r16, bool causal, bool fused, A... a)
 
 template <int HPC, bool R16, bool C, bool U>
 struct Occupancy {
-  static int run(int device) { return occupancy<HPC, R16, C, U>(device); }
+  static int run(bool small, int device) { return occupancy<HPC, R16, C, U>(device, small); }
 };
 
 template <int HPC, bool R16, bool C, bool U>
@@ -52,8 +52,8 @@ struct TwoGroups {
   static cudaError_t launch(const GqaParams& p, int grid, cudaStream_t stream) {
     return launch_attn<HPC, R16, true, false, kModePlain, 2>(p, grid, stream);
   }
-  static int ctas_per_sm(int device) {
-    return occupancy<HPC, R16, true, false, kModePlain, 2>(device);
+  static int ctas_per_sm(bool small, int device) {
+    return occupancy<HPC, R16, true, false, kModePlain, 2>(device, small);
   }
 };
 
@@ -69,44 +69,26 @@ cudaError_t launch_two_groups(const GqaParams& p, bool r16, int grid, cudaStream
   }
 }
 
-int two_groups_ctas_per_sm(int hpc, bool r16, int device) {
+int two_groups_ctas_per_sm(int hpc, bool r16, bool small, int device) {
   switch (hpc * 2 + (r16 ? 1 : 0)) {
-    case 2: return TwoGroups<1, false>::ctas_per_sm(device);
-    case 3: return TwoGroups<1, true>::ctas_per_sm(device);
-    case 4: return TwoGroups<2, false>::ctas_per_sm(device);
-    case 5: return TwoGroups<2, true>::ctas_per_sm(device);
-    case 8: return TwoGroups<4, false>::ctas_per_sm(device);
-    case 9: return TwoGroups<4, true>::ctas_per_sm(device);
+    case 2: return TwoGroups<1, false>::ctas_per_sm(small, device);
+    case 3: return TwoGroups<1, true>::ctas_per_sm(small, device);
+    case 4: return TwoGroups<2, false>::ctas_per_sm(small, device);
+    case 5: return TwoGroups<2, true>::ctas_per_sm(small, device);
+    case 8: return TwoGroups<4, false>::ctas_per_sm(small, device);
+    case 9: return TwoGroups<4, true>::ctas_per_sm(small, device);
     default: return 0;
   }
 }
 
-// Pieces per L2 round trip in the merge: 6 (one round trip for a unit cut
-// into up to 6 pieces) when the merge grid fits in one wave at the registers
-// that takes, else 2 (twice the warps resident; a merge of every row of many
-// query tokens has thousands of warps). Both give the same bits.
-int merge_pieces(int64_t blocks) {
-  static int one_wave[kMaxDevices] = {};  // blocks of the 6-piece merge per wave
-  int device = 0;
-  if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices) return 2;
-  if (one_wave[device] == 0) {
-    int per_sm = 0, sms = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gqa_merge_kernel<kModePlain, 6>,
-                                                      128, 0) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
-      return 2;
-    one_wave[device] = per_sm * sms > 0 ? per_sm * sms : 1;
-  }
-  return blocks <= one_wave[device] ? 6 : 2;
-}
-
 }  // namespace
 
-int gqa_ctas_per_sm(int hpc, bool rows16, bool causal, bool fused, int tg, int device) {
+int gqa_ctas_per_sm(int hpc, bool rows16, bool causal, bool fused, int tg, bool small,
+                    int device) {
   // (two groups per CTA always run the causal instances: with one query token
   // every row's limit is the whole cache)
-  if (tg == 2) return fused ? 0 : two_groups_ctas_per_sm(hpc, rows16, device);
-  return dispatch<Occupancy>(hpc, rows16, causal, fused, device);
+  if (tg == 2) return fused ? 0 : two_groups_ctas_per_sm(hpc, rows16, small, device);
+  return dispatch<Occupancy>(hpc, rows16, causal, fused, small, device);
 }
 
 cudaError_t gqa_decode_launch(const GqaParams& p, int grid, bool fused, cudaStream_t stream,
@@ -125,24 +107,7 @@ cudaError_t gqa_decode_launch(const GqaParams& p, int grid, bool fused, cudaStre
   if (e != cudaSuccess) return e;
   if (attn_end && (e = cudaEventRecord(attn_end, stream)) != cudaSuccess) return e;
   if (fused || p.unit_cut) return cudaSuccess;  // nothing left to merge
-  // The merge as a programmatic dependent launch: its CTAs may become resident
-  // before the attention grid ends and wait in griddepcontrol.wait.
-  const int64_t items =
-      int64_t(p.ngroups) * p.B * p.Hkv * ((p.gh * p.q_len + kMergeRows - 1) / kMergeRows);
-  const int64_t blocks = (items + 3) / 4;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(blocks));
-  cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return merge_pieces(blocks) == 6
-             ? cudaLaunchKernelEx(&cfg, gqa_merge_kernel<kModePlain, 6>, p, p.group_ctas)
-             : cudaLaunchKernelEx(&cfg, gqa_merge_kernel<kModePlain, 2>, p, p.group_ctas);
+  return launch_merge<kModePlain>(p, stream);
 }
 
 }  // namespace zl

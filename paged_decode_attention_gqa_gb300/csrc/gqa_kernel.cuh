@@ -43,7 +43,7 @@ constexpr uint32_t kErrBadPage = 1u;
 constexpr uint32_t kErrBadLen = 2u;
 constexpr uint32_t kErrTimeout = 4u;
 constexpr uint32_t kErrBadPrefix = 8u;
-constexpr int kMergeRows = 4;  // rows merged together by the split merge
+constexpr int kMergeRows = 4;  // rows one warp merges together (single launch; large merges)
 
 // What one launch of the attention kernel covers.
 constexpr int kModePlain = 0;   // every sequence over all of its own pages
@@ -66,12 +66,27 @@ struct GqaCfg {
   static constexpr int kConsumers = HPC * TG;  // consumer warps
   static constexpr int kThreads = (kConsumers + 1) * 32;
   static constexpr int kMinBlocks = TG > 1 && kConsumers < 8 ? 8 / kConsumers : 1;
-  // 1 KB alignment slack + stages + barriers + per-stage flags + abort flag + prefix table
-  // + split-piece records (2 per consumer warp)
-  static constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStageBytes + kStages * 16 +
-                                       kStages * 4 + 16 + (kMaxBatch + 1) * 4 +
-                                       kConsumers * 2 * 4;
+  // 1 KB alignment slack + stages + barriers + per-stage flags + abort flag and
+  // longest unit + split-piece records (2 per consumer warp); then the table of
+  // per-unit tile offsets, sized for the call (see table_entries).
+  static constexpr size_t kFixedBytes = 1024 + size_t(kStages) * kStageBytes + kStages * 16 +
+                                        kStages * 4 + 16 + kConsumers * 2 * 4;
+  static constexpr size_t smem_bytes(bool small_table) {
+    return kFixedBytes + size_t(small_table ? kSmallTable : kMaxBatch + 1) * 4;
+  }
+  static constexpr size_t kSmemBytes = smem_bytes(false);  // the largest, for the attribute
 };
+
+// Entries of the tile-offset table a launch needs (one per unit plus the
+// total), and whether they fit the small layout. A call with up to
+// kSmallTable - 1 units takes the small one: at one kv head per CTA that
+// leaves room for a fourth CTA on an SM (4 x 51 KB instead of 4 x 65 KB).
+__host__ __device__ __forceinline__ int table_entries(const GqaParams& p, int mode) {
+  return (mode == kModeShared ? p.ng : 0) + p.B + 1;
+}
+__host__ __device__ __forceinline__ bool small_table(const GqaParams& p, int mode) {
+  return table_entries(p, mode) <= kSmallTable;
+}
 
 __device__ __forceinline__ void raise_error(uint32_t* flags, uint32_t bits) {
   if (flags) atomicOr(flags, bits);
@@ -179,38 +194,42 @@ __device__ __forceinline__ int split_cta_span(const TileCut& cut, int64_t U0, in
 
 // Log-sum-exp merge of the R rows of kv head w (of CTA head group hg) over the
 // pieces of a split unit, by the warp whose arrival was the last (single
-// launch) or by the merge kernel: a running max and rescaled sums per row,
-// always in CTA order, so the result does not depend on who merges. Rows go in blocks of kMergeRows and pieces in
-// batches of kMergePieces: a lane loads every row's lse and its own 4 columns
-// of every row of a batch at once, so a batch costs one round trip to L2.
-// Merging the same pieces with any batch size gives the same bits.
-// Running log-sum-exp merge of kMergeRows rows (base-2 lse): a running max,
-// the rescaled weight sum and the rescaled sum of normalised outputs. A
-// source row with lse NaN (its piece met a bad page) marks that row bad (bit
-// k of `bad`); lse -inf weighs 0.
+// launch, NR = kMergeRows rows per warp) or by the merge kernel (NR = 1 or
+// kMergeRows): a running max and rescaled sums per row, always in CTA
+// order, so the result depends neither on who merges nor on how many rows a
+// warp takes. Pieces go in batches of P: a lane loads every row's lse and its
+// own 4 columns of every row of a batch at once, so a batch costs one round
+// trip to L2. Merging the same pieces with any batch size gives the same bits.
+// Running log-sum-exp merge of NR rows (base-2 lse): a running max, the
+// rescaled weight sum and the rescaled sum of normalised outputs. A source row
+// with lse NaN (its piece met a bad page) marks that row bad (bit k of
+// `bad`); lse -inf weighs 0.
+template <int NR>
 struct MergeAcc {
-  float mx[kMergeRows], den[kMergeRows];
-  float4 acc[kMergeRows];
+  float mx[NR], den[NR];
+  float4 acc[NR];
   uint32_t bad;
   __device__ __forceinline__ void init() {
 #pragma unroll
-    for (int k = 0; k < kMergeRows; ++k) {
+    for (int k = 0; k < NR; ++k) {
       mx[k] = -CUDART_INF_F;
       den[k] = 0.f;
       acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     bad = 0u;
   }
+  // Every product and sum is rounded as written (no contraction left to the
+  // compiler), so the bits do not depend on the code around an inlined copy.
   __device__ __forceinline__ void add(int k, float l, float4 o) {
     bad |= isnan(l) ? 1u << k : 0u;
     const float mn = fmaxf(mx[k], l);
     if (mn != -CUDART_INF_F && !isnan(l)) {
-      const float a = ex2_approx(mx[k] - mn), wgt = ex2_approx(l - mn);
-      den[k] = den[k] * a + wgt;
-      acc[k].x = acc[k].x * a + wgt * o.x;
-      acc[k].y = acc[k].y * a + wgt * o.y;
-      acc[k].z = acc[k].z * a + wgt * o.z;
-      acc[k].w = acc[k].w * a + wgt * o.w;
+      const float a = ex2_approx(__fsub_rn(mx[k], mn)), wgt = ex2_approx(__fsub_rn(l, mn));
+      den[k] = __fmaf_rn(den[k], a, wgt);
+      acc[k].x = __fmaf_rn(wgt, o.x, __fmul_rn(acc[k].x, a));
+      acc[k].y = __fmaf_rn(wgt, o.y, __fmul_rn(acc[k].y, a));
+      acc[k].z = __fmaf_rn(wgt, o.z, __fmul_rn(acc[k].z, a));
+      acc[k].w = __fmaf_rn(wgt, o.w, __fmul_rn(acc[k].w, a));
       mx[k] = mn;
     }
   }
@@ -218,27 +237,28 @@ struct MergeAcc {
 
 // Adds the partials of rows [row_off + r0, row_off + r0 + nrows) (slot stride
 // R) of the pieces of a unit (first tile U0) held by CTAs c_lo..c_hi, in CTA
-// order; pieces go in batches of kMergePieces whose loads are issued together
-// (one L2 round trip per batch).
-template <int kMergePieces>
-__device__ __forceinline__ void merge_add_pieces(MergeAcc& m, const GqaParams& p,
+// order; pieces go in batches of P whose loads are issued together (one L2
+// round trip per batch). Every CTA in c_lo..c_hi holds a piece (the launches
+// cut into at most as many ranges as tiles, so no range is empty); each
+// piece is its CTA's first (slot 0) except where the unit starts inside c_lo's
+// range (slot 1).
+template <int NR, int P>
+__device__ __forceinline__ void merge_add_pieces(MergeAcc<NR>& m, const GqaParams& p,
                                                  const TileCut& cut, int cta0, int64_t U0,
                                                  int c_lo, int c_hi, int w, int R, int row_off,
                                                  int r0, int nrows, int lane) {
-  for (int cb = c_lo; cb <= c_hi; cb += kMergePieces) {
-    float lv[kMergePieces][kMergeRows];
-    float4 ov[kMergePieces][kMergeRows];
-    bool use[kMergePieces];
+  const int sl_lo = U0 > cut.start(c_lo) ? 1 : 0;
+  for (int cb = c_lo; cb <= c_hi; cb += P) {
+    float lv[P][NR];
+    float4 ov[P][NR];
 #pragma unroll
-    for (int q = 0; q < kMergePieces; ++q) {
+    for (int q = 0; q < P; ++q) {
       const int cc = cb + q;
-      const int64_t s_cc = cut.start(cc);
-      use[q] = cc <= c_hi && s_cc < cut.start(cc + 1);
-      const int sl = (cc == c_lo && U0 > s_cc) ? 1 : 0;
+      const int sl = cc == c_lo ? sl_lo : 0;
       const int64_t base = ((int64_t(cta0 + cc) * 2 + sl) * p.hpc + w) * R + row_off + r0;
 #pragma unroll
-      for (int k = 0; k < kMergeRows; ++k) {
-        if (use[q] && k < nrows) {
+      for (int k = 0; k < NR; ++k) {
+        if (cc <= c_hi && k < nrows) {
           lv[q][k] = __ldcg(p.ws_lse + base + k);
           ov[q][k] =
               __ldcg(reinterpret_cast<const float4*>(p.ws_o + (base + k) * kGqaHeadDim) + lane);
@@ -246,23 +266,24 @@ __device__ __forceinline__ void merge_add_pieces(MergeAcc& m, const GqaParams& p
       }
     }
 #pragma unroll
-    for (int q = 0; q < kMergePieces; ++q)
+    for (int q = 0; q < P; ++q)
 #pragma unroll
-      for (int k = 0; k < kMergeRows; ++k)
-        if (use[q] && k < nrows) m.add(k, lv[q][k], ov[q][k]);
+      for (int k = 0; k < NR; ++k)
+        if (cb + q <= c_hi && k < nrows) m.add(k, lv[q][k], ov[q][k]);
   }
 }
 
 // Adds rows (sequence b, tile rows r0 + k of gh * q_len: token r / gh, head
 // head0 + r % gh) from an fp32 store of whole-unit results.
-__device__ __forceinline__ void merge_add_store(MergeAcc& m, const GqaParams& p,
+template <int NR>
+__device__ __forceinline__ void merge_add_store(MergeAcc<NR>& m, const GqaParams& p,
                                                 const float* st_o, const float* st_lse, int b,
                                                 int tok0, int head0, int gh, int r0, int nrows,
                                                 int lane) {
-  float lv[kMergeRows];
-  float4 ov[kMergeRows];
+  float lv[NR];
+  float4 ov[NR];
 #pragma unroll
-  for (int k = 0; k < kMergeRows; ++k) {
+  for (int k = 0; k < NR; ++k) {
     if (k < nrows) {
       const int r = r0 + k;
       const int64_t orow = (int64_t(b) * p.q_total + tok0 + r / gh) * p.Hq + head0 + r % gh;
@@ -271,47 +292,50 @@ __device__ __forceinline__ void merge_add_store(MergeAcc& m, const GqaParams& p,
     }
   }
 #pragma unroll
-  for (int k = 0; k < kMergeRows; ++k)
+  for (int k = 0; k < NR; ++k)
     if (k < nrows) m.add(k, lv[k], ov[k]);
 }
 
 // Writes the merged rows of sequence b (row r: token tok0 + r / gh, head
 // head0 + r % gh) as bf16 out and natural-log lse; a bad source or a row with
 // no weight gives zeros and lse = -inf.
-__device__ __forceinline__ void merge_write_out(const MergeAcc& m, const GqaParams& p, int b,
+template <int NR>
+__device__ __forceinline__ void merge_write_out(const MergeAcc<NR>& m, const GqaParams& p, int b,
                                                 int tok0, int head0, int gh, int r0, int nrows,
                                                 int lane) {
 #pragma unroll
-  for (int k = 0; k < kMergeRows; ++k) {
+  for (int k = 0; k < NR; ++k) {
     if (k < nrows) {
       const int r = r0 + k;
       const int64_t orow = (int64_t(b) * p.q_total + tok0 + r / gh) * p.Hq + head0 + r % gh;
       const bool none = ((m.bad >> k) & 1u) || !(m.den[k] > 0.f);
-      const float inv = none ? 0.f : 1.f / m.den[k];
+      const float inv = none ? 0.f : __frcp_rn(m.den[k]);
       uint2 packed = make_uint2(0u, 0u);
       if (!none) {
-        packed.x = pack_bf16x2(m.acc[k].x * inv, m.acc[k].y * inv);
-        packed.y = pack_bf16x2(m.acc[k].z * inv, m.acc[k].w * inv);
+        packed.x = pack_bf16x2(__fmul_rn(m.acc[k].x, inv), __fmul_rn(m.acc[k].y, inv));
+        packed.y = pack_bf16x2(__fmul_rn(m.acc[k].z, inv), __fmul_rn(m.acc[k].w, inv));
       }
       reinterpret_cast<uint2*>(p.out + orow * kGqaHeadDim)[lane] = packed;
       if (p.lse && lane == 0)
-        p.lse[orow] = none ? -CUDART_INF_F : (m.mx[k] + log2f(m.den[k])) * 0.69314718055994531f;
+        p.lse[orow] = none ? -CUDART_INF_F
+                           : __fmul_rn(__fadd_rn(m.mx[k], log2f(m.den[k])), 0.69314718055994531f);
     }
   }
 }
 
 // A plain unit (sequence b, kv head w of the CTA group, first tile U0) cut
-// between CTAs c_lo..c_hi: merge rows [r_begin, r_end) and write them.
-template <int kMergePieces>
+// between CTAs c_lo..c_hi: merge rows [r_begin, r_end), NR at a time, and
+// write them.
+template <int NR, int P>
 __device__ __forceinline__ void merge_split_rows(const GqaParams& p, const TileCut& cut, int cta0,
                                                  int64_t U0, int c_lo, int c_hi, int b, int tok0,
                                                  int w, int head0, int gh, int R, int r_begin,
                                                  int r_end, int lane) {
-  for (int r0 = r_begin; r0 < r_end; r0 += kMergeRows) {
-    const int nrows = min(kMergeRows, r_end - r0);
-    MergeAcc m;
+  for (int r0 = r_begin; r0 < r_end; r0 += NR) {
+    const int nrows = min(NR, r_end - r0);
+    MergeAcc<NR> m;
     m.init();
-    merge_add_pieces<kMergePieces>(m, p, cut, cta0, U0, c_lo, c_hi, w, R, 0, r0, nrows, lane);
+    merge_add_pieces<NR, P>(m, p, cut, cta0, U0, c_lo, c_hi, w, R, 0, r0, nrows, lane);
     merge_write_out(m, p, b, tok0, head0, gh, r0, nrows, lane);
   }
 }
@@ -362,9 +386,9 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
   uint64_t* empty = full + NS;
   int* stage_bad = reinterpret_cast<int*>(empty + NS);
   volatile int* abort_flag = stage_bad + NS;
-  int* prefix = stage_bad + NS + 4;
-  int* split_rec = prefix + kMaxBatch + 1;  // [HPC][2]: b | hg << 12 of a split piece, or -1
-  int* unit_max = stage_bad + NS + 1;       // tiles of the longest unit
+  int* unit_max = stage_bad + NS + 1;   // tiles of the longest unit
+  int* split_rec = stage_bad + NS + 4;  // [HPC][2]: b | hg << 12 of a split piece, or -1
+  int* prefix = split_rec + Cfg::kConsumers * 2;  // table_entries(p, MODE) entries
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int B = p.B;
@@ -830,8 +854,9 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
     const int64_t U0 = int64_t(nhg) * prefix[b] + int64_t(hg) * n;
     int c_lo, c_hi;
     split_cta_span(cut, U0, n, c_lo, c_hi);
-    merge_split_rows<4>(p, cut, vcta - c, U0, c_lo, c_hi, b, tok0, w,
-                        (hg * HPC + w) * g + rg.hoff, gh, p.gh * p.q_len, 0, gh * qlen, lane);
+    merge_split_rows<kMergeRows, 4>(p, cut, vcta - c, U0, c_lo, c_hi, b, tok0, w,
+                                    (hg * HPC + w) * g + rg.hoff, gh, p.gh * p.q_len, 0,
+                                    gh * qlen, lane);
   }
   }
 
@@ -858,8 +883,11 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
 
 
 // Split-KV merge as its own launch (when the attention kernel runs without
-// FUSED), one warp per block of kMergeRows rows of a (sequence, kv head), with
-// the same arithmetic as the in-kernel merge, so both give the same bits.
+// FUSED), one warp per NR rows of a (sequence, kv head), with the same
+// arithmetic per row as the in-kernel merge, so both give the same bits.
+// launch_merge takes one row per warp while that makes at most 16 warps per
+// SM (short chains of dependent steps, many warps in flight), else
+// kMergeRows (fewer copies of each warp's fixed set-up).
 // Plain: only units cut between CTAs need it. Shared prefix: every row, from
 // its prefix part (the group unit's pieces, or the prefix store when one CTA
 // had the whole unit) then its suffix part (pieces, the suffix store, or
@@ -867,13 +895,13 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
 // Launched as a programmatic dependent of the attention kernel: it may start
 // early and waits here until that grid has finished and its writes are
 // visible.
-template <int MODE, int PIECES = 2>
+template <int MODE, int NR, int PIECES>
 __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ GqaParams p,
                                                         int G) {
   const int lane = threadIdx.x & 31;
   const int rmax = p.gh * p.q_len;  // rows of a partial slot (the largest group's)
-  const int nrb = (rmax + kMergeRows - 1) / kMergeRows;
-  // items: (row group, sequence, kv head, block of kMergeRows rows)
+  const int nrb = (rmax + NR - 1) / NR;
+  // items: (row group, sequence, kv head, block of NR rows)
   const int64_t per_group = int64_t(p.B) * p.Hkv * nrb;
   const int64_t item = int64_t(blockIdx.x) * 4 + (threadIdx.x >> 5);
   const bool live = item < per_group * p.ngroups;
@@ -908,9 +936,9 @@ __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ 
   const int n = live ? seq_unit_tiles<MODE>(p, p.seq_lens[b]) : 0;
   griddep_wait();
   griddep_launch_dependents();  // the next kernels may start their prologue
-  const int r0 = int(gitem % nrb) * kMergeRows;
+  const int r0 = int(gitem % nrb) * NR;
   if (!live || r0 >= rps) return;
-  const int nrows = min(kMergeRows, rps - r0);
+  const int nrows = min(NR, rps - r0);
   const int cta0 = tg * G;  // the group's first CTA (G = CTAs per group)
   const int hg = kvh / p.hpc, w = kvh % p.hpc;
   const int head0 = kvh * p.g + rg.hoff;  // the group's first query head
@@ -924,13 +952,13 @@ __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ 
     // left every unit whole
     if (p.auto_cut && short_units(int64_t(p.B) * p.nhg, nmax, p.hpc, G)) return;
     if (n == 0 || c_lo == c_hi) return;
-    // PIECES pieces per round trip to L2 (the host takes 6 when the merge grid
-    // fits in one wave at the registers that needs, else 2).
-    merge_split_rows<PIECES>(p, cut, cta0, U0, c_lo, c_hi, b, tok0, w, head0, gh, rmax, r0,
-                             r0 + nrows, lane);
+    // PIECES pieces per round trip to L2 (launch_merge takes the larger batch
+    // when the merge grid fits in one wave at the registers that needs).
+    merge_split_rows<NR, PIECES>(p, cut, cta0, U0, c_lo, c_hi, b, tok0, w, head0, gh, rmax, r0,
+                                 r0 + nrows, lane);
   } else {
     const int R = p.sgs * rps;  // rows of a partial slot
-    MergeAcc m;
+    MergeAcc<NR> m;
     m.init();
     {
       const int vp = b / p.sgs;  // the group's prefix unit (each has PT tiles)
@@ -940,20 +968,87 @@ __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ 
       if (p_lo == p_hi)
         merge_add_store(m, p, p.pre_o, p.pre_lse, b, tok0, head0, gh, r0, nrows, lane);
       else
-        merge_add_pieces<2>(m, p, cut, cta0, P0, p_lo, p_hi, w, R, (b % p.sgs) * rps, r0, nrows,
-                            lane);
+        merge_add_pieces<NR, PIECES>(m, p, cut, cta0, P0, p_lo, p_hi, w, R, (b % p.sgs) * rps,
+                                     r0, nrows, lane);
     }
     if (n > 0) {
       if (c_lo == c_hi)
         merge_add_store(m, p, p.suf_o, p.suf_lse, b, tok0, head0, gh, r0, nrows, lane);
       else
-        merge_add_pieces<2>(m, p, cut, cta0, U0, c_lo, c_hi, w, R, 0, r0, nrows, lane);
+        merge_add_pieces<NR, PIECES>(m, p, cut, cta0, U0, c_lo, c_hi, w, R, 0, r0, nrows, lane);
     }
     merge_write_out(m, p, b, tok0, head0, gh, r0, nrows, lane);
   }
 }
 
 constexpr int kMaxDevices = 64;
+
+// Launches the merge kernel for the rows of every (row group, sequence, kv
+// head) (ngroups * B * Hkv * rows_per_slot rows) as a programmatic dependent
+// of the attention kernel: its CTAs may become resident before the attention
+// grid ends and wait in griddepcontrol.wait. Rows per warp (1, or kMergeRows
+// past 16 warps per SM) and pieces per L2 round trip (the larger batch when
+// the grid fits in one wave at the registers that takes) only change how the
+// work is spread: every choice gives the same bits.
+template <int MODE, int NR, int P>
+struct MergeInstance {
+  // blocks of 4 warps over the items (unit, block of NR of its rmax rows)
+  static int64_t blocks(int64_t units, int rmax) {
+    return (units * ((rmax + NR - 1) / NR) + 3) / 4;
+  }
+  static cudaError_t launch(const GqaParams& p, int64_t units, int rmax, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(blocks(units, rmax)));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gqa_merge_kernel<MODE, NR, P>, p, p.group_ctas);
+  }
+  // CTAs of this instance per wave on `device` (0 on error), queried once.
+  static int64_t wave(int device, int sms) {
+    static int cached[kMaxDevices] = {};
+    if (device >= 0 && device < kMaxDevices && cached[device] > 0) return cached[device];
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gqa_merge_kernel<MODE, NR, P>,
+                                                      128, 0) != cudaSuccess)
+      return 0;
+    if (device >= 0 && device < kMaxDevices) cached[device] = per_sm * sms;
+    return int64_t(per_sm) * sms;
+  }
+};
+
+template <int MODE>
+cudaError_t launch_merge(const GqaParams& p, cudaStream_t stream) {
+  static int sms_of[kMaxDevices] = {};
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return e;
+  if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (sms_of[device] == 0 &&
+      (e = cudaDeviceGetAttribute(&sms_of[device], cudaDevAttrMultiProcessorCount, device)) !=
+          cudaSuccess)
+    return e;
+  const int sms = sms_of[device];
+  // units (row group, sequence, kv head), each with a partial slot of rmax
+  // rows (the largest group's; a shared-prefix launch has one group)
+  const int64_t units = int64_t(p.ngroups) * p.B * p.Hkv;
+  const int rmax = p.gh * p.q_len;
+  if (units * rmax <= 16LL * sms) {  // one row per warp
+    using Big = MergeInstance<MODE, 1, 8>;
+    if (Big::blocks(units, rmax) <= Big::wave(device, sms))
+      return Big::launch(p, units, rmax, stream);
+    return MergeInstance<MODE, 1, 4>::launch(p, units, rmax, stream);
+  }
+  using Big = MergeInstance<MODE, kMergeRows, 4>;
+  if (Big::blocks(units, rmax) <= Big::wave(device, sms))
+    return Big::launch(p, units, rmax, stream);
+  return MergeInstance<MODE, kMergeRows, 2>::launch(p, units, rmax, stream);
+}
 
 // Raise the dynamic shared-memory limit of one kernel instance, once per device.
 template <int HPC, bool R16, bool C, bool U, int MODE = kModePlain, int TG = 1>
@@ -977,7 +1072,7 @@ cudaError_t launch_attn(const GqaParams& p, int grid, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(grid));
   cfg.blockDim = dim3(Cfg::kThreads);
-  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.dynamicSmemBytes = Cfg::smem_bytes(small_table(p, MODE));
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -987,19 +1082,21 @@ cudaError_t launch_attn(const GqaParams& p, int grid, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, gqa_decode_kernel<HPC, R16, C, U, MODE, TG>, p);
 }
 
+// CTAs per SM at the small or the full table layout.
 template <int HPC, bool R16, bool C, bool U, int MODE = kModePlain, int TG = 1>
-int occupancy(int device) {
+int occupancy(int device, bool small) {
   using Cfg = GqaCfg<HPC, TG>;
-  // Queried once per device (it does not change), not on every call.
-  static int cached[kMaxDevices] = {};
-  if (device >= 0 && device < kMaxDevices && cached[device] > 0) return cached[device];
+  // Queried once per device and layout (it does not change), not on every call.
+  static int cached[kMaxDevices][2] = {};
+  if (device >= 0 && device < kMaxDevices && cached[device][small] > 0)
+    return cached[device][small];
   if (configure<HPC, R16, C, U, MODE, TG>(device) != cudaSuccess) return 0;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-          &n, gqa_decode_kernel<HPC, R16, C, U, MODE, TG>, Cfg::kThreads, Cfg::kSmemBytes) !=
-      cudaSuccess)
+          &n, gqa_decode_kernel<HPC, R16, C, U, MODE, TG>, Cfg::kThreads,
+          Cfg::smem_bytes(small)) != cudaSuccess)
     return 0;
-  if (device >= 0 && device < kMaxDevices) cached[device] = n;
+  if (device >= 0 && device < kMaxDevices) cached[device][small] = n;
   return n;
 }
 

@@ -34,7 +34,9 @@ auto dispatch_mode(int hpc, bool r16, bool causal, A... a)
 
 template <int HPC, bool R16, bool C, bool U, int MODE>
 struct Occupancy {
-  static int run(int device) { return occupancy<HPC, R16, C, U, MODE>(device); }
+  static int run(bool small, int device) {
+    return occupancy<HPC, R16, C, U, MODE>(device, small);
+  }
 };
 
 template <int HPC, bool R16, bool C, bool U, int MODE>
@@ -46,8 +48,8 @@ struct Launch {
 
 }  // namespace
 
-int gqa_shared_ctas_per_sm(int hpc, bool rows16, bool causal, int device) {
-  return dispatch_mode<Occupancy, kModeShared>(hpc, rows16, causal, device);
+int gqa_shared_ctas_per_sm(int hpc, bool rows16, bool causal, bool small, int device) {
+  return dispatch_mode<Occupancy, kModeShared>(hpc, rows16, causal, small, device);
 }
 
 cudaError_t gqa_shared_launch(const GqaParams& p, int grid, cudaStream_t stream,
@@ -61,19 +63,7 @@ cudaError_t gqa_shared_launch(const GqaParams& p, int grid, cudaStream_t stream,
       cudaSuccess)
     return e;
   if (attn_end && (e = cudaEventRecord(attn_end, stream)) != cudaSuccess) return e;
-  const int rps = p.gh * p.q_len;
-  const int64_t items = int64_t(p.B) * p.Hkv * ((rps + kMergeRows - 1) / kMergeRows);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned((items + 3) / 4));
-  cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gqa_merge_kernel<kModeShared>, p, p.group_ctas);
+  return launch_merge<kModeShared>(p, stream);
 }
 
 }  // namespace zl

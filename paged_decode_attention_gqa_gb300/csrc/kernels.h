@@ -11,6 +11,9 @@ namespace zl {
 constexpr int kGqaTile = 16;     // tokens per pipeline stage of the GQA kernel
 constexpr int kGqaHeadDim = 128; // D_qk = D_v
 constexpr int kMaxBatch = 4096;  // sequences per call (prefix table lives in smem)
+// Entries of the GQA kernel's small tile-offset table (units + 1); calls with
+// more units take the full one of kMaxBatch + 1 entries.
+constexpr int kSmallTable = 512;
 // A call whose longest (sequence, head group) unit has at most this many K and
 // V bytes gives each unit a CTA of its own and merges nothing (when the units
 // fit in the grid): one CTA streams that in about the time a merge costs.
@@ -112,11 +115,13 @@ cudaError_t mla_decode_launch(const MlaParams& p, int clusters, cudaStream_t str
 
 // kv heads handled by one CTA for this Hkv (largest of 8, 4, 2, 1 dividing it).
 int gqa_heads_per_cta(int Hkv);
-// CTAs of the attention kernel that fit on one SM (0 on error).
-int gqa_ctas_per_sm(int hpc, bool rows16, bool causal, bool fused, int tg, int device);
+// CTAs of the attention kernel that fit on one SM (0 on error); small: the
+// call's units + 1 fit the small table (at most kSmallTable entries).
+int gqa_ctas_per_sm(int hpc, bool rows16, bool causal, bool fused, int tg, bool small,
+                    int device);
 // Shared-prefix decode: CTAs per SM of its attention kernel, and its two
 // launches (attention over prefix groups and suffixes, then the merge).
-int gqa_shared_ctas_per_sm(int hpc, bool rows16, bool causal, int device);
+int gqa_shared_ctas_per_sm(int hpc, bool rows16, bool causal, bool small, int device);
 cudaError_t gqa_shared_launch(const GqaParams& p, int grid, cudaStream_t stream,
                               cudaEvent_t attn_begin, cudaEvent_t attn_end);
 // Launches the attention kernel on `grid` CTAs. fused: split units are merged
