@@ -53,6 +53,9 @@ constexpr int kModePlain = 0;   // every sequence over all of its own pages
 // and suffix stores, and the merge kernel combines both parts of every row.
 constexpr int kModeShared = 1;
 constexpr uint64_t kTestStallNs = 50ull * 1000 * 1000;  // bound of the test-hook wait
+// A row's softmax base moves only when a tile's scores exceed it by more than
+// this (base 2): P stays at most 2^8 in between.
+constexpr float kLazyLog2 = 8.f;
 
 template <int HPC, int TG = 1>
 struct GqaCfg {
@@ -659,28 +662,40 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
     // page: those rows, and only those, are written as zeros.
     bool bad_a = false, bad_b = false;
 
-    // One row's online-softmax step in base 2 over this thread's four scores
-    // (tokens 2t4, 2t4+1, 2t4+8, 2t4+9 of the tile; vis = visible tokens of
-    // the row in this tile). A row with nothing visible yet keeps m = -inf and
-    // contributes zeros.
-    auto row_step = [&](float sa, float sb, float sc, float sd, int vis, float& m, float& l,
-                        uint32_t& p_lo, uint32_t& p_hi) -> float {
-      const float x0 = 2 * t4 < vis ? sa * scale_log2 : -CUDART_INF_F;
-      const float x1 = 2 * t4 + 1 < vis ? sb * scale_log2 : -CUDART_INF_F;
-      const float x2 = 2 * t4 + 8 < vis ? sc * scale_log2 : -CUDART_INF_F;
-      const float x3 = 2 * t4 + 9 < vis ? sd * scale_log2 : -CUDART_INF_F;
-      float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+    // Online softmax in base 2 with a lazy base. Each row exponentiates
+    // against a base m that moves only when a tile's max exceeds it by more
+    // than kLazyLog2; then every row of the warp takes max(m, tile max) at once
+    // (one vote per tile) and O and l are rescaled. Meanwhile P may reach
+    // 2^kLazyLog2, well inside bf16 and fp32 range, and a tile costs no
+    // rescale of the 64 O values a thread holds. The result is the same
+    // softmax up to rounding; the lse is m + log2(l) with the final base.
+    // This thread's four scores of a row (tokens 2t4, 2t4+1, 2t4+8, 2t4+9 of
+    // the tile), scaled to base 2 with the tokens past vis masked to -inf,
+    // and the row's max over the tile (a row that sees nothing gives -inf).
+    auto row_scores = [&](float sa, float sb, float sc, float sd, int vis, float (&x)[4]) -> float {
+      x[0] = 2 * t4 < vis ? sa * scale_log2 : -CUDART_INF_F;
+      x[1] = 2 * t4 + 1 < vis ? sb * scale_log2 : -CUDART_INF_F;
+      x[2] = 2 * t4 + 8 < vis ? sc * scale_log2 : -CUDART_INF_F;
+      x[3] = 2 * t4 + 9 < vis ? sd * scale_log2 : -CUDART_INF_F;
+      float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const float mn = fmaxf(m, mx);
-      const float base = mn == -CUDART_INF_F ? 0.f : mn;
-      const float alpha = ex2_approx(m - base);
+      return fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    };
+    // Moves a row's base to mn >= m; returns the factor for its O and l (0
+    // while the row has seen nothing).
+    auto move_base = [&](float& m, float mn) -> float {
+      const float alpha = m == -CUDART_INF_F ? 0.f : ex2_approx(m - mn);
       m = mn;
-      p_lo = pack_bf16x2(ex2_approx(x0 - base), ex2_approx(x1 - base));
-      p_hi = pack_bf16x2(ex2_approx(x2 - base), ex2_approx(x3 - base));
-      const float2 f0 = unpack_bf16x2(p_lo), f2 = unpack_bf16x2(p_hi);
-      l = l * alpha + ((f0.x + f0.y) + (f2.x + f2.y));
       return alpha;
+    };
+    // P of a row against its base (a row that has seen nothing has P = 0) and
+    // its sum, taken over the bf16-rounded P that the PV product uses.
+    auto row_p = [&](const float (&x)[4], float m, float& l, uint32_t& p_lo, uint32_t& p_hi) {
+      const float base = m == -CUDART_INF_F ? 0.f : m;
+      p_lo = pack_bf16x2(ex2_approx(x[0] - base), ex2_approx(x[1] - base));
+      p_hi = pack_bf16x2(ex2_approx(x[2] - base), ex2_approx(x[3] - base));
+      const float2 f0 = unpack_bf16x2(p_lo), f2 = unpack_bf16x2(p_hi);
+      l += (f0.x + f0.y) + (f2.x + f2.y);
     };
 
     for (int t = 0; t < ntiles; ++t, ++it) {
@@ -721,24 +736,36 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
 
       uint32_t pa[4];
       {
-        const float alpha = row_step(s[0][0], s[0][1], s[1][0], s[1][1],
-                                     CAUSAL ? min(valid, lim_a - tok0) : valid, m0, l0, pa[0], pa[2]);
+        float xa[4], xb[4];
+        const float mxa = row_scores(s[0][0], s[0][1], s[1][0], s[1][1],
+                                     CAUSAL ? min(valid, lim_a - tok0) : valid, xa);
+        const float mxb = ROWS16 ? row_scores(s[0][2], s[0][3], s[1][2], s[1][3],
+                                              CAUSAL ? min(valid, lim_b - tok0) : valid, xb)
+                                 : -CUDART_INF_F;
+        if (__any_sync(0xffffffffu, mxa > m0 + kLazyLog2 || mxb > m1 + kLazyLog2)) {
+          const float aa = move_base(m0, fmaxf(m0, mxa));
+          l0 *= aa;
 #pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-          o[nt][0] *= alpha;
-          o[nt][1] *= alpha;
-        }
-      }
-      if (ROWS16) {
-        const float alpha = row_step(s[0][2], s[0][3], s[1][2], s[1][3],
-                                     CAUSAL ? min(valid, lim_b - tok0) : valid, m1, l1, pa[1], pa[3]);
+          for (int nt = 0; nt < 16; ++nt) {
+            o[nt][0] *= aa;
+            o[nt][1] *= aa;
+          }
+          if (ROWS16) {
+            const float ab = move_base(m1, fmaxf(m1, mxb));
+            l1 *= ab;
 #pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-          o[nt][2] *= alpha;
-          o[nt][3] *= alpha;
+            for (int nt = 0; nt < 16; ++nt) {
+              o[nt][2] *= ab;
+              o[nt][3] *= ab;
+            }
+          }
         }
-      } else {
-        pa[1] = pa[3] = 0u;
+        row_p(xa, m0, l0, pa[0], pa[2]);
+        if (ROWS16) {
+          row_p(xb, m1, l1, pa[1], pa[3]);
+        } else {
+          pa[1] = pa[3] = 0u;
+        }
       }
 
       // O += P V. Token rows of V past the cache end are zeroed in registers so
