@@ -183,7 +183,7 @@ typedef struct {
  *   with ZL_DECODE_SINGLE_LAUNCH, one launch per group, and attn_begin is
  *   recorded before the first and attn_end after the last.
  *   With shared_prefix_pages > 0, g * q_len <= 16. When max_seq_len shows that
- *   every (sequence, head group) is short (at most 512 KB of K and V), each
+ *   every (sequence, head group) is short (at most 8 tiles of 16 tokens), each
  *   gets a CTA of its own and no merge is launched. A query row that
  *   sees no token (seq_lens[b] < q_len) gives out = 0 and lse = -inf. A bad
  *   page id zeroes (out = 0, lse = -inf) every query row whose visible tokens

@@ -98,7 +98,7 @@ struct GqaPlan {
 constexpr int kMaxQueryTokens = 128;
 constexpr int kMaxGroupHeads = 128;
 // A call whose longest (sequence, head group) unit has at most
-// zl::kGqaUnitCutBytes of K and V (known from max_seq_len) gives each unit a
+// zl::kGqaUnitCutTiles tiles (known from max_seq_len) gives each unit a
 // CTA of its own and skips the merge launch. Without max_seq_len the kernels
 // take the same decision on the device (GqaParams::auto_cut).
 
@@ -181,9 +181,7 @@ zl_status gqa_plan(const zl_decode_attn_params* a, GqaPlan* plan) {
     if (a->max_seq_len > 0 && plan->prefix_tiles == 0) {
       const int64_t max_tiles = (int64_t(a->max_seq_len) + zl::kGqaTile - 1) / zl::kGqaTile;
       const int64_t units = int64_t(a->B) * plan->nhg;
-      // K and V bytes of the longest unit (sequence, head group).
-      const int64_t unit_bytes = max_tiles * zl::kGqaTile * plan->hpc * zl::kGqaHeadDim * 2 * 2;
-      if (units <= grid && unit_bytes <= zl::kGqaUnitCutBytes) {
+      if (units <= grid && max_tiles <= zl::kGqaUnitCutTiles) {
         // Short contexts: one CTA per whole unit. Streaming the longest unit
         // alone costs less than cutting units and merging their pieces.
         plan->unit_cut = true;

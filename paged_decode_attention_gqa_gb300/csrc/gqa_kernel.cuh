@@ -135,11 +135,10 @@ struct TileCut {
 };
 
 // Whether every unit of the launch is short enough for a CTA of its own (the
-// unit cut): at most kGqaUnitCutBytes of K and V in the longest unit (n_max
-// tiles of hpc kv heads), and no more units than the group's CTAs.
-__device__ __forceinline__ bool short_units(int64_t units, int n_max, int hpc, int ctas) {
-  const int64_t tile_bytes = int64_t(kGqaTile) * hpc * kGqaHeadDim * 2 * 2;
-  return units <= ctas && int64_t(n_max) * tile_bytes <= kGqaUnitCutBytes;
+// unit cut): at most kGqaUnitCutTiles tiles in the longest unit (n_max), and
+// no more units than the group's CTAs.
+__device__ __forceinline__ bool short_units(int64_t units, int n_max, int ctas) {
+  return units <= ctas && n_max <= kGqaUnitCutTiles;
 }
 
 // 64-bit compare-and-swap with acquire-release semantics at GPU scope: the
@@ -501,7 +500,7 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
   int64_t e_c = c < int(cut.G) ? cut.start(c + 1) : W;
   const bool unit_cut =
       MODE == kModePlain &&
-      (p.unit_cut || (p.auto_cut && short_units(int64_t(V) * nhg, unit_max[0], HPC, G)));
+      (p.unit_cut || (p.auto_cut && short_units(int64_t(V) * nhg, unit_max[0], G)));
   if (unit_cut) {
     // Unit (v, hg) holds tiles [nhg * prefix[v] + hg * n, + n) of the line.
     s_c = e_c = 0;
@@ -977,7 +976,7 @@ __global__ void __launch_bounds__(128) gqa_merge_kernel(const __grid_constant__ 
   if constexpr (MODE == kModePlain) {
     // a unit-cut launch (chosen on the device, as the attention kernel did)
     // left every unit whole
-    if (p.auto_cut && short_units(int64_t(p.B) * p.nhg, nmax, p.hpc, G)) return;
+    if (p.auto_cut && short_units(int64_t(p.B) * p.nhg, nmax, G)) return;
     if (n == 0 || c_lo == c_hi) return;
     // PIECES pieces per round trip to L2 (launch_merge takes the larger batch
     // when the merge grid fits in one wave at the registers that needs).

@@ -14,10 +14,12 @@ constexpr int kMaxBatch = 4096;  // sequences per call (prefix table lives in sm
 // Entries of the GQA kernel's small tile-offset table (units + 1); calls with
 // more units take the full one of kMaxBatch + 1 entries.
 constexpr int kSmallTable = 512;
-// A call whose longest (sequence, head group) unit has at most this many K and
-// V bytes gives each unit a CTA of its own and merges nothing (when the units
-// fit in the grid): one CTA streams that in about the time a merge costs.
-constexpr int64_t kGqaUnitCutBytes = 512 * 1024;
+// A call whose longest (sequence, head group) unit has at most this many
+// 16-token tiles gives each unit a CTA of its own and merges nothing (when the
+// units fit in the grid). With few units a CTA's tiles are latency-bound
+// (~0.5 us each, whatever the head count), so a unit this short costs about
+// what a merge launch does; longer ones are cut and merged.
+constexpr int kGqaUnitCutTiles = 8;
 
 // Everything the GQA attention kernel reads.
 struct GqaParams {

@@ -57,7 +57,7 @@ def test_page_sizes_and_layouts(P):
 def test_short_contexts_one_cta_per_unit():
     """max_seq_len shows every unit short: one CTA per unit, no merge launch;
     without it the kernel decides the same on the device."""
-    lens = [0, 1, 16, 17, 64, 200]
+    lens = [0, 1, 16, 17, 64, 128]
     w = wl.random_case(1230, B=len(lens), Hq=32, Hkv=1, lens=lens)
     g = _parity(w)
     assert torch.all(g.out[0] == 0) and torch.all(torch.isneginf(g.lse[0].cpu()))
