@@ -48,6 +48,17 @@ def test_hnd_layout_is_bit_identical_to_nhd():
     assert torch.equal(ga.out.view(torch.int16), gb.out.view(torch.int16))
 
 
+@pytest.mark.parametrize("B,Hq,Hkv", [(511, 8, 2), (512, 8, 2), (600, 32, 1)])
+@pytest.mark.parametrize("hint", [True, False])
+def test_batches_around_the_small_table(B, Hq, Hkv, hint):
+    """Up to 511 sequences keep their tile offsets in the small shared-memory
+    table (more CTAs fit on an SM), more in the full one: both sides of the
+    edge (512 and 513 entries), and the two-row-group instance (32 heads on
+    one kv head) on the full one; with and without max_seq_len."""
+    w = wl.random_case(500 + B + Hq, B=B, Hq=Hq, Hkv=Hkv, max_len=48)
+    _parity(w, **({} if hint else {"max_seq_len": 0}))
+
+
 @pytest.mark.parametrize("num_ctas", [1, 2, 7, 64, 151, 1000, 5000])
 def test_any_split_matches(num_ctas):
     """Every grid size (one CTA = unsplit, many CTAs = many split pieces)."""

@@ -55,6 +55,15 @@ def test_suffix_edges():
     _parity(w, 5)
 
 
+@pytest.mark.parametrize("B", [300, 400])
+def test_many_sequences_around_the_small_table(B):
+    """Prefix groups plus sequences make the table's units: 150 + 300 fit the
+    small shared-memory table, 200 + 400 take the full one."""
+    rng = np.random.default_rng(B)
+    w = _case(1300 + B, B=B, Hq=64, Hkv=8, npref=4, extra=rng.integers(0, 40, size=B))
+    _parity(w, 4)
+
+
 @pytest.mark.parametrize("num_ctas", [1, 3, 40, 151, 900])
 def test_any_grid(num_ctas):
     w = _case(1220, B=9, Hq=32, Hkv=8, npref=8)
