@@ -310,7 +310,7 @@ class Case:
     C-ABI params and workspace, the optional KV append and L2 flush."""
 
     def __init__(self, w, dev, *, single_launch=False, shared_prefix=False, with_append=False,
-                 hint=True):
+                 hint=True, fused_append=False):
         import paged_decode_attention_gqa_gb300 as zl
         self.zl, self.w, self.dev = zl, w, dev
         self.kind = "mla" if w.mla else "gqa"
@@ -327,10 +327,21 @@ class Case:
             assert self.npref > 0, "--shared-prefix needs a workload with a shared prefix"
         self.single_launch = single_launch and not w.mla
         self.max_seq_len = w.max_seq_len if hint else 0
+        # fused_append: each step's decode call itself first stores the q_len new
+        # tokens' K/V rows (k_new / v_new in the params): one launch less.
+        self.k_new = self.v_new = None
+        if fused_append:
+            from paged_decode_attention_gqa_gb300 import workloads as _wl
+            k_new, v_new = _wl.new_token_rows(w.seed, w.B, w.q_len, w.Hkv, w.D_qk,
+                                              None if w.mla else w.D_v)
+            self.k_new = k_new.to(dev)
+            self.v_new = None if v_new is None else v_new.to(dev)
+        self.fused_append = fused_append
         self.p = zl.make_params(self.q, self.k, self.v, self.bt, self.sl, self.out,
                                 page_size=w.page_size, scale=w.scale, Hkv=w.Hkv, D_v=w.D_v,
                                 lse=self.lse, err_flags=self.err, max_seq_len=self.max_seq_len,
-                                single_launch=self.single_launch, shared_prefix_pages=self.npref)
+                                single_launch=self.single_launch, shared_prefix_pages=self.npref,
+                                k_new=self.k_new, v_new=self.v_new)
         need = zl.workspace_size_mla(self.p) if w.mla else zl.workspace_size(self.p)
         self.ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
         self.p.workspace, self.p.workspace_bytes = self.ws.data_ptr(), self.ws.numel()
@@ -640,7 +651,8 @@ def run_ours(args, world, rank, local):
 
     w = make_workload(args.workload, args.batch, args.q_len)
     c = Case(w, dev, single_launch=args.single_launch, shared_prefix=args.shared_prefix,
-             with_append=args.with_append, hint=not args.no_hint)
+             with_append=args.with_append, hint=not args.no_hint,
+             fused_append=args.fused_append)
     kind = c.kind
 
     for _ in range(max(args.warmup, 3)):
@@ -690,7 +702,7 @@ def run_ours(args, world, rank, local):
         cpu_s, cpu_calls, cores, res = time_oracle(w)
         cpu = {"value": kvb / cpu_s / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"the whole workload per call, {cpu_calls} calls (median)"}
-        if c.ap is None:  # (with the append the device pools hold the new rows)
+        if c.ap is None and not c.fused_append:  # (an append puts the new rows in the pools)
             parity = parity_summary(c.out, c.lse, res)
     line = {
         "metric": metric_name(args.workload, args.q_len),
@@ -731,6 +743,9 @@ def run_ours(args, world, rank, local):
     if c.ap is not None:
         line["config"]["step"] = "kv append + attention"
         line["kv_append"] = append
+    if c.fused_append:
+        line["config"]["step"] = "kv append fused into the attention launch + attention"
+
     if c.npref:
         line["config"]["shared_prefix_pages"] = c.npref
     if args.no_hint:
@@ -743,7 +758,7 @@ def run_ours(args, world, rank, local):
                           "peak_kind": tpeak_kind}
     if not args.no_workloads and world == 1 and args.workload == WORKLOAD and args.q_len == 1 \
             and not (args.single_launch or args.with_append or args.shared_prefix or args.no_hint
-                     or args.batch):
+                     or args.batch or args.fused_append):
         del c
         torch.cuda.empty_cache()
         line["workloads"] = measure_extra(dev, 200, 5, oracle_seconds=3.0)
@@ -765,6 +780,9 @@ def main():
     ap.add_argument("--batch", type=int, default=None, help="override the batch size")
     ap.add_argument("--with-append", action="store_true",
                     help="each step writes the new tokens' K/V (zl_kv_append) before attending")
+    ap.add_argument("--fused-append", action="store_true",
+                    help="each step's decode call stores the new tokens' K/V itself (k_new / "
+                         "v_new), then attends, in one launch")
     ap.add_argument("--shared-prefix", action="store_true",
                     help="pass the workload's shared prefix pages (read once per group)")
     ap.add_argument("--single-launch", action="store_true",

@@ -152,6 +152,22 @@ typedef struct {
      ZL_DEVERR_BAD_PREFIX if either fails (results are then undefined). Not
      with ZL_DECODE_SINGLE_LAUNCH. */
   int32_t shared_prefix_pages;
+
+  /* Optional fused KV append; NULL = the cache already holds the new tokens.
+     The q_len new tokens' rows, bf16, contiguous, 16-byte aligned:
+     zl_decode_attn: k_new [B, q_len, Hkv, D_qk] and v_new [B, q_len, Hkv,
+     D_v], both required; zl_decode_attn_mla: k_new [B, q_len, D_qk] (the
+     latent rows) and v_new NULL. The attention launch itself stores them in
+     their page slots first, exactly as zl_kv_append would (new token i of
+     sequence b is position seq_lens[b] - q_len + i; the pools must be
+     writable), and attends over the result: a decode step needs no separate
+     append launch. After the call the pools hold the new rows, bit-exact,
+     except rows on a bad page (skipped and flagged, as zl_kv_append does) and
+     the rows of a sequence with fewer than q_len tokens or a bad length
+     (skipped; only a bad length is flagged, by the attention). With
+     shared_prefix_pages the new tokens must lie past the shared pages. */
+  const void* k_new;
+  const void* v_new;
 } zl_decode_attn_params;
 
 /* zl_decode_attn: merge the split-KV partials inside the attention kernel
@@ -276,6 +292,8 @@ zl_status zl_decode_attn_noalloc(const zl_decode_attn_params* params, zl_stream_
  *   - Every written element is a copy: the result is bit-exact.
  *   - The writes are ordinary stores on the given stream; a decode call
  *     enqueued after it on the same stream sees them.
+ *   - zl_decode_attn_params.k_new / v_new do the same stores inside the
+ *     attention launch (one launch less per decode step).
  */
 typedef struct {
   size_t struct_size; /* sizeof(zl_kv_append_params) */

@@ -78,6 +78,8 @@ class Params(ctypes.Structure):
         ("attn_end", ctypes.c_void_p),
         ("flags", ctypes.c_uint32),
         ("shared_prefix_pages", ctypes.c_int32),
+        ("k_new", ctypes.c_void_p),
+        ("v_new", ctypes.c_void_p),
     ]
 
 
@@ -169,7 +171,10 @@ def _pool_strides(pool: torch.Tensor, layout: str):
 def make_params(q, k_pool, v_pool, block_table, seq_lens, out, *, page_size, scale, Hkv,
                 D_v, lse=None, workspace=None, err_flags=None, num_ctas=0, max_seq_len=0,
                 layout="NHD", events=None, single_launch=False,
-                shared_prefix_pages=0) -> Params:
+                shared_prefix_pages=0, k_new=None, v_new=None) -> Params:
+    """k_new / v_new: the fused KV append (the new tokens' K and V rows, bf16
+    [B, q_len, Hkv, D]; MLA: the latent rows in k_new, v_new None); the call
+    then stores them in their page slots before attending."""
     B, q_len, Hq, D_qk = q.shape
     ps, ts, hs = _pool_strides(k_pool, layout)
     if v_pool is not None and _pool_strides(v_pool, layout) != (ps, ts, hs):
@@ -197,10 +202,15 @@ def make_params(q, k_pool, v_pool, block_table, seq_lens, out, *, page_size, sca
     p.num_ctas = int(num_ctas)
     p.flags = SINGLE_LAUNCH if single_launch else 0
     p.shared_prefix_pages = int(shared_prefix_pages)
+    for t in (k_new, v_new):
+        if t is not None and not t.is_contiguous():
+            raise ValueError("k_new and v_new must be contiguous")
+    p.k_new, p.v_new = _ptr(k_new), _ptr(v_new)
     if events is not None:
         p.attn_begin, p.attn_end = events[0].cuda_event, events[1].cuda_event
     # The struct holds raw device pointers: keep the tensors alive with it.
-    p.tensors = (q, k_pool, v_pool, block_table, seq_lens, out, lse, workspace, err_flags, events)
+    p.tensors = (q, k_pool, v_pool, block_table, seq_lens, out, lse, workspace, err_flags, events,
+                 k_new, v_new)
     return p
 
 
@@ -267,13 +277,14 @@ def call(params: Params, *, mla: bool, stream=None):
 
 def _run(q, k_pool, v_pool, block_table, seq_lens, *, mla, page_size, scale, Hkv, D_v, out, lse,
          workspace, err_flags, num_ctas, max_seq_len, layout, stream, events, single_launch=False,
-         shared_prefix_pages=0):
+         shared_prefix_pages=0, k_new=None, v_new=None):
     if out is None:
         out = torch.empty(q.shape[:3] + (D_v,), dtype=torch.bfloat16, device=q.device)
     p = make_params(q, k_pool, v_pool, block_table, seq_lens, out, page_size=page_size,
                     scale=scale, Hkv=Hkv, D_v=D_v, lse=lse, err_flags=err_flags,
                     num_ctas=num_ctas, max_seq_len=max_seq_len, layout=layout, events=events,
-                    single_launch=single_launch, shared_prefix_pages=shared_prefix_pages)
+                    single_launch=single_launch, shared_prefix_pages=shared_prefix_pages,
+                    k_new=k_new, v_new=v_new)
     need = workspace_size_mla(p) if mla else workspace_size(p)
     if workspace is None:
         counters = 8 * q.shape[0] * Hkv if single_launch else 0
@@ -287,7 +298,8 @@ def _run(q, k_pool, v_pool, block_table, seq_lens, *, mla, page_size, scale, Hkv
 
 def decode_attn(q, k_pool, v_pool, block_table, seq_lens, *, page_size, scale, out=None, lse=None,
                 workspace=None, err_flags=None, num_ctas=0, max_seq_len=0, layout="NHD",
-                stream=None, events=None, single_launch=False, shared_prefix_pages=0):
+                stream=None, events=None, single_launch=False, shared_prefix_pages=0,
+                k_new=None, v_new=None):
     """GQA/MHA/MQA paged decode attention (zl_decode_attn).
 
     q [B, q_len, Hq, 128] bf16; k_pool, v_pool [pages, page_size, Hkv, 128]
@@ -298,27 +310,32 @@ def decode_attn(q, k_pool, v_pool, block_table, seq_lens, *, page_size, scale, o
     arrival counters, see the header; the default cached one is kept so).
     shared_prefix_pages: the first pages of every block-table row are the same
     shared prefix (read once per group of sequences; see the header).
+    k_new, v_new: the q_len new tokens' K and V rows [B, q_len, Hkv, 128] bf16;
+    the call stores them in their page slots (as kv_append does) and then
+    attends, in the same launch.
     """
     Hkv = k_pool.shape[2] if layout == "NHD" else k_pool.shape[1]
     return _run(q, k_pool, v_pool, block_table, seq_lens, mla=False, page_size=page_size,
                 scale=scale, Hkv=Hkv, D_v=q.shape[3], out=out, lse=lse, workspace=workspace,
                 err_flags=err_flags, num_ctas=num_ctas, max_seq_len=max_seq_len, layout=layout,
                 stream=stream, events=events, single_launch=single_launch,
-                shared_prefix_pages=shared_prefix_pages)
+                shared_prefix_pages=shared_prefix_pages, k_new=k_new, v_new=v_new)
 
 
 def decode_attn_mla(q, kv_pool, block_table, seq_lens, *, page_size, scale, D_v=512, out=None,
                     lse=None, workspace=None, err_flags=None, num_ctas=0, max_seq_len=0,
-                    stream=None, events=None):
+                    stream=None, events=None, kv_new=None):
     """Absorbed MLA paged decode (zl_decode_attn_mla).
 
-    q [B, 1, Hq, 576] bf16; kv_pool [pages, page_size, 1, 576] bf16 (V = first
-    D_v columns). Returns out [B, 1, Hq, D_v] bf16.
+    q [B, q_len, Hq, 576] bf16; kv_pool [pages, page_size, 1, 576] bf16 (V =
+    first D_v columns). Returns out [B, q_len, Hq, D_v] bf16. kv_new: the new
+    tokens' latent rows [B, q_len, 1, 576] bf16, stored in their page slots by
+    the same launch before it attends.
     """
     return _run(q, kv_pool, None, block_table, seq_lens, mla=True, page_size=page_size,
                 scale=scale, Hkv=1, D_v=D_v, out=out, lse=lse, workspace=workspace,
                 err_flags=err_flags, num_ctas=num_ctas, max_seq_len=max_seq_len, layout="NHD",
-                stream=stream, events=events)
+                stream=stream, events=events, k_new=kv_new)
 
 
 def make_append_params(k_new, v_new, k_pool, v_pool, block_table, seq_lens, *, page_size,

@@ -330,6 +330,11 @@ zl_status validate_pointers(const zl_decode_attn_params* a, bool need_v) {
   if (a->page_stride <= 0 || a->token_stride <= 0 || a->head_stride <= 0 ||
       a->page_stride % 8 || a->token_stride % 8 || a->head_stride % 8)
     return ZL_ERR_INVALID_ARG;
+  // fused KV append: GQA takes k_new and v_new together, MLA k_new alone
+  if (!a->k_new && a->v_new) return ZL_ERR_INVALID_ARG;
+  if (a->k_new && (need_v != (a->v_new != nullptr))) return ZL_ERR_INVALID_ARG;
+  if ((a->k_new && !aligned(a->k_new, 16)) || (a->v_new && !aligned(a->v_new, 16)))
+    return ZL_ERR_INVALID_ARG;
   return ZL_OK;
 }
 
@@ -415,6 +420,15 @@ zl_status zl_decode_attn(const zl_decode_attn_params* a, zl_stream_t stream) {
   p.pre_o = reinterpret_cast<float*>(ws + plan.off_pre_o);
   p.suf_lse = reinterpret_cast<float*>(ws + plan.off_suf_lse);
   p.suf_o = reinterpret_cast<float*>(ws + plan.off_suf_o);
+  if (a->k_new) {  // the attention launch stores the new tokens' rows first
+    p.k_new = static_cast<const uint4*>(a->k_new);
+    p.v_new = static_cast<const uint4*>(a->v_new);
+    p.k_pool = static_cast<uint4*>(const_cast<void*>(a->k_pool));
+    p.v_pool = static_cast<uint4*>(const_cast<void*>(a->v_pool));
+    p.page_stride16 = a->page_stride / 8;
+    p.token_stride16 = a->token_stride / 8;
+    p.head_stride16 = a->head_stride / 8;
+  }
 
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int ngroups = plan.ngroups;
@@ -517,6 +531,12 @@ zl_status zl_decode_attn_mla(const zl_decode_attn_params* a, zl_stream_t stream)
   p.num_pages = a->num_pages;
   p.scale_log2 = float(double(a->scale) * kLog2e);
   p.out_align32 = aligned(a->out, 32) ? 1 : 0;
+  if (a->k_new) {  // the attention launch stores the new tokens' latent rows first
+    p.kv_new = static_cast<const uint4*>(a->k_new);
+    p.kv_pool = static_cast<uint4*>(const_cast<void*>(a->k_pool));
+    p.page_stride16 = a->page_stride / 8;
+    p.token_stride16 = a->token_stride / 8;
+  }
   const cudaError_t e = zl::mla_decode_launch(p, plan.clusters,
                                               reinterpret_cast<cudaStream_t>(stream),
                                               reinterpret_cast<cudaEvent_t>(a->attn_begin),

@@ -372,6 +372,42 @@ __device__ __forceinline__ RowGroup row_group(const GqaParams& p, int k) {
   return r;
 }
 
+// Fused KV append, by the 32 lanes of a producer warp: new tokens [inew,
+// inew + nn) of sequence b, which sit in slots [slot0, slot0 + nn) of page pg,
+// for kv heads [kh0, kh0 + HPC): their K and V rows (16 chunks of 16 bytes
+// each) are copied from k_new / v_new into the pools. Each lane then fences
+// its stores against the bulk copies that read the page next.
+template <int HPC>
+__device__ __forceinline__ void append_tile_rows(const GqaParams& p, int b, int pg, int slot0,
+                                                 int inew, int nn, int kh0, int lane) {
+  constexpr int kChunks = kGqaHeadDim * 2 / 16;
+  const int total = nn * HPC * 2 * kChunks;
+  for (int c0 = 0; c0 < total; c0 += 4 * 32) {
+    uint4 v[4];
+    uint4* dst[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c = c0 + 32 * u + lane;
+      dst[u] = nullptr;
+      if (c < total) {
+        const int cc = c % kChunks, row = c / kChunks;  // row = (j * HPC + hh) * 2 + (K or V)
+        const bool is_v = row & 1;
+        const int hh = (row >> 1) % HPC, j = (row >> 1) / HPC;
+        const int64_t src =
+            ((int64_t(b) * p.q_total + inew + j) * p.Hkv + kh0 + hh) * kChunks + cc;
+        v[u] = __ldg((is_v ? p.v_new : p.k_new) + src);
+        dst[u] = (is_v ? p.v_pool : p.k_pool) + int64_t(pg) * p.page_stride16 +
+                 int64_t(slot0 + j) * p.token_stride16 + int64_t(kh0 + hh) * p.head_stride16 +
+                 cc;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (dst[u]) *dst[u] = v[u];
+  }
+  fence_proxy_async_global();
+}
+
 template <int HPC, bool ROWS16, bool CAUSAL, bool FUSED, int MODE = kModePlain, int TG = 1>
 __global__ void __launch_bounds__(GqaCfg<HPC, TG>::kThreads, GqaCfg<HPC, TG>::kMinBlocks)
 gqa_decode_kernel(const __grid_constant__ GqaParams p) {
@@ -533,6 +569,9 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
       // lane i resolves tile base + i: page id, slot and head group
       const int64_t idx = base + lane;
       int page = 0, slot = 0, hg = 0, bad = 0;
+      // fused append: new tokens the tile holds (count, index of the first
+      // among the call's new tokens, its slot) and their sequence
+      int nnew = 0, inew = 0, nslot = 0, nseq = 0;
       if (idx < e_c) {
         const int v = locate_seq(prefix, V, nhg, idx);
         const int n = prefix[v + 1] - prefix[v];
@@ -544,6 +583,17 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
         slot = tok0 % p.page_size;
         page = p.block_table[int64_t(trow) * p.bt_stride + tok0 / p.page_size];
         bad = (page < 0 || page >= p.num_pages) ? 1 : 0;
+        if (p.k_new && !pre) {
+          const int L = p.seq_lens[trow];
+          const int t0 = L - p.q_total;  // the call's first new token
+          const int lo = max(tok0, t0), hi = min(tok0 + kGqaTile, L);
+          if (t0 >= 0 && hi > lo) {
+            nnew = hi - lo;
+            inew = lo - t0;
+            nslot = slot + (lo - tok0);
+            nseq = trow;
+          }
+        }
       }
       const int cnt = int(min(int64_t(32), e_c - base));
       for (int k = 0; k < cnt; ++k, ++it) {
@@ -551,6 +601,15 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
         const int sl = __shfl_sync(0xffffffffu, slot, k);
         const int h = __shfl_sync(0xffffffffu, hg, k);
         const int bd = __shfl_sync(0xffffffffu, bad, k);
+        const int nn = __shfl_sync(0xffffffffu, nnew, k);
+        if (nn > 0 && !bd) {
+          // Store the new tokens' rows of this CTA's kv heads before the tile's
+          // loads (every CTA that loads the tile stores the same bytes).
+          append_tile_rows<HPC>(p, __shfl_sync(0xffffffffu, nseq, k), pg,
+                                __shfl_sync(0xffffffffu, nslot, k),
+                                __shfl_sync(0xffffffffu, inew, k), nn, h * HPC, lane);
+          __syncwarp();
+        }
         int ok = 1;
         if (lane == 0) {
           const int stage = it % NS;

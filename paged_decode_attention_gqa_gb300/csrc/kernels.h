@@ -81,6 +81,15 @@ struct GqaParams {
   int hpc;             // kv heads per CTA
   int nhg;             // Hkv / hpc head groups
   float scale_log2;    // scale * log2(e)
+  // Fused KV append (k_new = nullptr: none). The new tokens' rows [B, q_total,
+  // Hkv, 128] bf16 as 16-byte chunks; before loading a tile that holds new
+  // tokens, the producer warp stores their rows of the CTA's kv heads into the
+  // pools (raw pointers, strides in 16-byte chunks).
+  const uint4* k_new;
+  const uint4* v_new;
+  uint4* k_pool;
+  uint4* v_pool;
+  int64_t page_stride16, token_stride16, head_stride16;
 };
 
 constexpr int kMlaTile = 64;       // tokens per MLA tile (page sizes are multiples of it)
@@ -108,6 +117,13 @@ struct MlaParams {
   int B, q_len, page_size, num_pages;
   float scale_log2;
   int out_align32;      // out is 32-byte aligned: 32-byte stores
+  // Fused KV append (kv_new = nullptr: none): the new tokens' latent rows
+  // [B, q_len, 576] bf16 as 16-byte chunks; each producer warp stores the
+  // columns it loads of the new tokens its cluster's tiles hold, before its
+  // first load (raw pool pointer, strides in 16-byte chunks).
+  const uint4* kv_new;
+  uint4* kv_pool;
+  int64_t page_stride16, token_stride16;
 };
 
 size_t mla_smem_bytes();

@@ -65,6 +65,7 @@ enum : int {
   B_L_FULL0 = B_E_EMPTY0 + kStages, B_L_EMPTY0 = B_L_FULL0 + kStages,
   B_S_FULL = B_L_EMPTY0 + kStages, B_S_EMPTY, B_P_FULL, B_PV_DONE, B_FINAL,
   B_Q_STAGED, B_Q_USED,  // the softmax threads' own syncs around the Q staging buffer
+  B_APPEND_E, B_APPEND_L,  // fused append: lanes 1-31 of a producer warp stored the new rows
   B_COUNT
 };
 constexpr int kOffMisc = kOffBar + 8 * B_COUNT;
@@ -157,6 +158,8 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     mbar_init(bar(B_FINAL), 1);
     mbar_init(bar(B_Q_STAGED), kRows);
     mbar_init(bar(B_Q_USED), kRows);
+    mbar_init(bar(B_APPEND_E), 31);
+    mbar_init(bar(B_APPEND_L), 31);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -243,6 +246,40 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
   // grid to finish before it reads anything.
   griddep_launch_dependents();
 
+  if ((warp == 0 || warp == 6) && lane != 0) {
+    // Fused KV append, by lanes 1-31 of each producer warp while lane 0
+    // starts the loads: of every new token this cluster's tiles hold, store
+    // the columns this warp loads (E: the other latent half and the rope; L:
+    // this rank's half), then release them to lane 0, which waits before it
+    // loads a tile that holds a new token. Both CTAs of the pair, and every
+    // unit of a sequence that sees the token, store the same bytes.
+    const bool e_part = warp == 0;
+    if (p.kv_new) {
+      const int nchunk = e_part ? 40 : 32;  // 16-byte chunks of a row
+      for (int u = e_c > s_c ? locate(prefix, B, s_c) : B; u < B && prefix[u] < e_c; ++u) {
+        const int64_t j_lo = max(s_c, int64_t(prefix[u])) - prefix[u];
+        const int64_t j_hi = min(e_c, int64_t(prefix[u + 1])) - prefix[u];
+        if (j_hi <= j_lo) continue;
+        const int b = u / p.q_len;
+        const int t0 = p.seq_lens[b] - p.q_len;  // the call's first new token
+        const int t_lo = max(int(j_lo) * kTile, t0);
+        const int t_hi = min(int(j_hi) * kTile, vis_len(u));
+        for (int t = t_lo; t < t_hi; ++t) {
+          const int page = p.block_table[int64_t(b) * p.bt_stride + t / p.page_size];
+          if (page < 0 || page >= p.num_pages) continue;
+          const uint4* src = p.kv_new + (int64_t(b) * p.q_len + (t - t0)) * (kMlaDqk / 8);
+          uint4* dst = p.kv_pool + int64_t(page) * p.page_stride16 +
+                       int64_t(t % p.page_size) * p.token_stride16;
+          for (int c = lane - 1; c < nchunk; c += 31) {
+            const int col = e_part ? (c < 32 ? other * 32 + c : 64 + (c - 32)) : rank * 32 + c;
+            dst[col] = __ldg(src + col);
+          }
+        }
+      }
+      fence_proxy_async_global();  // before the bulk copies that read those pages
+    }
+    mbar_arrive(bar(e_part ? B_APPEND_E : B_APPEND_L));
+  }
   if ((warp == 0 || warp == 6) && lane == 0) {
     // ------------------------------------------------------------ producers
     // Warp 0 streams the E parts (the other latent half and the rope), warp 6
@@ -264,6 +301,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       return p.block_table[int64_t(u / p.q_len) * p.bt_stride + (jt * kTile) / p.page_size];
     };
     int page = total > 0 ? page_of(b, j) : 0;
+    bool appended = false;  // lanes 1-31 stored the new rows (fused append)
     int it = 0;
     bool ok = true;
     for (; it < total; ++it) {
@@ -286,6 +324,16 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       if (page < 0 || page >= p.num_pages) {
         mbar_arrive(bar(full0 + s));  // nothing loaded; the piece is discarded
       } else {
+        if (p.kv_new && !appended) {  // a tile that holds a new token waits for its rows
+          const int t0 = p.seq_lens[b / p.q_len] - p.q_len;
+          if (tok0 + kTile > t0 && tok0 < vis_len(b)) {
+            if (!mbar_wait(bar(e_part ? B_APPEND_E : B_APPEND_L), 0, abort_flag)) {
+              ok = false;
+              break;
+            }
+            appended = true;
+          }
+        }
         const int slot = tok0 % p.page_size;
         mbar_arrive_expect_tx(bar(full0 + s), uint32_t(stage_bytes));
         for (int i = 0; i < nbox; ++i) {

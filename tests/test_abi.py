@@ -63,6 +63,9 @@ def _params(**over):
     (dict(flags=zl.TEST_STALL | 4), zl.ERR_INVALID_ARG),
     (dict(page_size=8), zl.ERR_UNSUPPORTED),
     (dict(B=5000), zl.ERR_UNSUPPORTED),
+    (dict(k_new=1 << 20), zl.ERR_INVALID_ARG),     # fused append: K rows without V rows
+    (dict(v_new=1 << 20), zl.ERR_INVALID_ARG),     # ... V rows without K rows
+    (dict(k_new=(1 << 20) + 8, v_new=1 << 20), zl.ERR_INVALID_ARG),  # misaligned new rows
 ])
 def test_host_validation(over, code):
     p = _params(**over)
@@ -106,6 +109,9 @@ def _mla_params(**over):
     (dict(flags=zl.SINGLE_LAUNCH), zl.ERR_UNSUPPORTED),
     (dict(flags=zl.TEST_STALL), zl.ERR_UNSUPPORTED),
     (dict(flags=4), zl.ERR_INVALID_ARG),
+    (dict(k_new=1 << 20, v_new=1 << 20), zl.ERR_INVALID_ARG),  # latent rows only: no v_new
+    (dict(v_new=1 << 20), zl.ERR_INVALID_ARG),
+    (dict(k_new=(1 << 20) + 2), zl.ERR_INVALID_ARG),
 ])
 def test_mla_host_validation(over, code):
     p = _mla_params(**over)
