@@ -194,14 +194,15 @@ __device__ __forceinline__ int split_cta_span(const TileCut& cut, int64_t U0, in
   return c_hi - c_lo + 1;
 }
 
-// Log-sum-exp merge of the R rows of kv head w (of CTA head group hg) over the
-// pieces of a split unit, by the warp whose arrival was the last (single
-// launch, NR = kMergeRows rows per warp) or by the merge kernel (NR = 1 or
-// kMergeRows): a running max and rescaled sums per row, always in CTA
+// Split-KV merge. The R rows of kv head w (of CTA head group hg) are merged
+// over the pieces of a split unit by the warp whose arrival was the last
+// (single launch, NR = kMergeRows rows per warp) or by the merge kernel (NR =
+// 1 or kMergeRows): a running max and rescaled sums per row, always in CTA
 // order, so the result depends neither on who merges nor on how many rows a
 // warp takes. Pieces go in batches of P: a lane loads every row's lse and its
 // own 4 columns of every row of a batch at once, so a batch costs one round
 // trip to L2. Merging the same pieces with any batch size gives the same bits.
+
 // Running log-sum-exp merge of NR rows (base-2 lse): a running max, the
 // rescaled weight sum and the rescaled sum of normalised outputs. A source row
 // with lse NaN (its piece met a bad page) marks that row bad (bit k of
