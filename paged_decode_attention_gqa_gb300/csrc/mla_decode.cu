@@ -65,7 +65,7 @@ enum : int {
   B_L_FULL0 = B_E_EMPTY0 + kStages, B_L_EMPTY0 = B_L_FULL0 + kStages,
   B_S_FULL = B_L_EMPTY0 + kStages, B_S_EMPTY, B_P_FULL, B_PV_DONE, B_FINAL,
   B_Q_STAGED, B_Q_USED,  // the softmax threads' own syncs around the Q staging buffer
-  B_APPEND_E, B_APPEND_L,  // fused append: lanes 1-31 of a producer warp stored the new rows
+  B_APPEND,  // fused append: the softmax threads stored the new rows
   B_COUNT
 };
 constexpr int kOffMisc = kOffBar + 8 * B_COUNT;
@@ -115,6 +115,41 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// Fused KV append, by the softmax threads (thread `tid` of `nthreads`) while
+// the first loads are in flight: every new token that the tiles [s_c, e_c) of
+// the units `prefix` lays out hold is copied from kv_new into its pool slot
+// (all 576 columns), and the stores are fenced against the bulk copies that
+// read those pages. Both CTAs of the pair, and every unit of a sequence that
+// sees the token, store the same bytes.
+__device__ __noinline__ void append_new_rows(const MlaParams& p, const int* prefix, int B,
+                                             int64_t s_c, int64_t e_c, int tid, int nthreads) {
+  constexpr int kChunks = kMlaDqk / 8;  // 16-byte chunks of a row
+  const int64_t cap = p.bt_stride * int64_t(p.page_size);
+  for (int u = e_c > s_c ? locate(prefix, B, s_c) : B; u < B && prefix[u] < e_c; ++u) {
+    const int64_t j_lo = max(s_c, int64_t(prefix[u])) - prefix[u];
+    const int64_t j_hi = min(e_c, int64_t(prefix[u + 1])) - prefix[u];
+    if (j_hi <= j_lo) continue;
+    const int b = u / p.q_len;
+    const int L = p.seq_lens[b];
+    if (!(L >= p.q_len && int64_t(L) <= cap)) continue;
+    const int t0 = L - p.q_len;            // the call's first new token
+    const int vis = t0 + 1 + u % p.q_len;  // tokens unit u sees
+    const int t_lo = max(int(j_lo) * kTile, t0);
+    const int t_hi = min(int(j_hi) * kTile, vis);
+    for (int c = tid; c < (t_hi - t_lo) * kChunks; c += nthreads) {
+      const int t = t_lo + c / kChunks, col = c % kChunks;
+      const int page = p.block_table[int64_t(b) * p.bt_stride + t / p.page_size];
+      if (page < 0 || page >= p.num_pages) continue;
+      p.kv_pool[int64_t(page) * p.page_stride16 + int64_t(t % p.page_size) * p.token_stride16 +
+                col] = __ldg(p.kv_new + (int64_t(b) * p.q_len + (t - t0)) * kChunks + col);
+    }
+  }
+  fence_proxy_async_global();
+}
+
+// APPEND: the instance that also stores the new tokens' rows (p.kv_new); the
+// plain instance has none of that code.
+template <bool APPEND>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 mla_decode_kernel(const __grid_constant__ MlaParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -158,8 +193,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     mbar_init(bar(B_FINAL), 1);
     mbar_init(bar(B_Q_STAGED), kRows);
     mbar_init(bar(B_Q_USED), kRows);
-    mbar_init(bar(B_APPEND_E), 31);
-    mbar_init(bar(B_APPEND_L), 31);
+    if constexpr (APPEND) mbar_init(bar(B_APPEND), kRows);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -246,40 +280,6 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
   // grid to finish before it reads anything.
   griddep_launch_dependents();
 
-  if ((warp == 0 || warp == 6) && lane != 0) {
-    // Fused KV append, by lanes 1-31 of each producer warp while lane 0
-    // starts the loads: of every new token this cluster's tiles hold, store
-    // the columns this warp loads (E: the other latent half and the rope; L:
-    // this rank's half), then release them to lane 0, which waits before it
-    // loads a tile that holds a new token. Both CTAs of the pair, and every
-    // unit of a sequence that sees the token, store the same bytes.
-    const bool e_part = warp == 0;
-    if (p.kv_new) {
-      const int nchunk = e_part ? 40 : 32;  // 16-byte chunks of a row
-      for (int u = e_c > s_c ? locate(prefix, B, s_c) : B; u < B && prefix[u] < e_c; ++u) {
-        const int64_t j_lo = max(s_c, int64_t(prefix[u])) - prefix[u];
-        const int64_t j_hi = min(e_c, int64_t(prefix[u + 1])) - prefix[u];
-        if (j_hi <= j_lo) continue;
-        const int b = u / p.q_len;
-        const int t0 = p.seq_lens[b] - p.q_len;  // the call's first new token
-        const int t_lo = max(int(j_lo) * kTile, t0);
-        const int t_hi = min(int(j_hi) * kTile, vis_len(u));
-        for (int t = t_lo; t < t_hi; ++t) {
-          const int page = p.block_table[int64_t(b) * p.bt_stride + t / p.page_size];
-          if (page < 0 || page >= p.num_pages) continue;
-          const uint4* src = p.kv_new + (int64_t(b) * p.q_len + (t - t0)) * (kMlaDqk / 8);
-          uint4* dst = p.kv_pool + int64_t(page) * p.page_stride16 +
-                       int64_t(t % p.page_size) * p.token_stride16;
-          for (int c = lane - 1; c < nchunk; c += 31) {
-            const int col = e_part ? (c < 32 ? other * 32 + c : 64 + (c - 32)) : rank * 32 + c;
-            dst[col] = __ldg(src + col);
-          }
-        }
-      }
-      fence_proxy_async_global();  // before the bulk copies that read those pages
-    }
-    mbar_arrive(bar(e_part ? B_APPEND_E : B_APPEND_L));
-  }
   if ((warp == 0 || warp == 6) && lane == 0) {
     // ------------------------------------------------------------ producers
     // Warp 0 streams the E parts (the other latent half and the rope), warp 6
@@ -301,7 +301,10 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       return p.block_table[int64_t(u / p.q_len) * p.bt_stride + (jt * kTile) / p.page_size];
     };
     int page = total > 0 ? page_of(b, j) : 0;
-    bool appended = false;  // lanes 1-31 stored the new rows (fused append)
+    bool appended = false;  // the softmax threads stored the new rows (APPEND instance)
+    // APPEND: the unit's first new token, read one unit ahead like the pages
+    int t0_cur = 0;
+    if constexpr (APPEND) t0_cur = total > 0 ? p.seq_lens[b / p.q_len] - p.q_len : 0;
     int it = 0;
     bool ok = true;
     for (; it < total; ++it) {
@@ -317,6 +320,10 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         nj = 0;
       }
       const int page_next = it + 1 < total ? page_of(nb, nj) : 0;
+      int t0_next = t0_cur;
+      if constexpr (APPEND) {
+        if (nb != b && it + 1 < total) t0_next = p.seq_lens[nb / p.q_len] - p.q_len;
+      }
       if (!mbar_wait(bar(empty0 + s), ((it / kStages) & 1) ^ 1u, abort_flag)) {
         ok = false;
         break;
@@ -324,10 +331,10 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       if (page < 0 || page >= p.num_pages) {
         mbar_arrive(bar(full0 + s));  // nothing loaded; the piece is discarded
       } else {
-        if (p.kv_new && !appended) {  // a tile that holds a new token waits for its rows
-          const int t0 = p.seq_lens[b / p.q_len] - p.q_len;
-          if (tok0 + kTile > t0 && tok0 < vis_len(b)) {
-            if (!mbar_wait(bar(e_part ? B_APPEND_E : B_APPEND_L), 0, abort_flag)) {
+        if constexpr (APPEND) {  // a tile that holds a new token waits for its rows
+          const int vis = t0_cur + 1 + b % p.q_len;  // tokens unit b sees
+          if (!appended && tok0 + kTile > t0_cur && tok0 < vis) {
+            if (!mbar_wait(bar(B_APPEND), 0, abort_flag)) {
               ok = false;
               break;
             }
@@ -346,6 +353,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       b = nb;
       j = nj;
       page = page_next;
+      t0_cur = t0_next;
     }
     if (!ok) {
       raise_error(p.err_flags, kErrTimeout);
@@ -602,6 +610,13 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       const int v0 = locate(prefix, B, s_c);
       q_stage(v0);
       ok = q_finish(v0);
+      if constexpr (APPEND) {
+        // Fused KV append while the first tile's QK runs (the softmax threads
+        // wait for its scores anyway); a producer loads a tile that holds a
+        // new token only after this.
+        append_new_rows(p, prefix, B, s_c, e_c, stid, kRows);
+        mbar_arrive(bar(B_APPEND));
+      }
     }
     int it = 0;
     for (int64_t idx = s_c; idx < e_c && ok;) {
@@ -896,16 +911,18 @@ size_t mla_smem_bytes() { return kSmemBytes; }
 
 cudaError_t mla_decode_launch(const MlaParams& p, int clusters, cudaStream_t stream,
                               cudaEvent_t attn_begin, cudaEvent_t attn_end) {
-  static bool configured[kMaxDevices] = {};
+  static bool configured[kMaxDevices][2] = {};
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
   if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!configured[device]) {
-    e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const bool append = p.kv_new != nullptr;
+  auto kernel = append ? mla_decode_kernel<true> : mla_decode_kernel<false>;
+  if (!configured[device][append]) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(kSmemBytes));
     if (e != cudaSuccess) return e;
-    configured[device] = true;
+    configured[device][append] = true;
   }
   if (attn_begin && (e = cudaEventRecord(attn_begin, stream)) != cudaSuccess) return e;
   {
@@ -919,7 +936,7 @@ cudaError_t mla_decode_launch(const MlaParams& p, int clusters, cudaStream_t str
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if ((e = cudaLaunchKernelEx(&cfg, mla_decode_kernel, p)) != cudaSuccess) return e;
+    if ((e = cudaLaunchKernelEx(&cfg, kernel, p)) != cudaSuccess) return e;
   }
   if (attn_end && (e = cudaEventRecord(attn_end, stream)) != cudaSuccess) return e;
   const int64_t rows = int64_t(p.B) * p.q_len * kRows;
