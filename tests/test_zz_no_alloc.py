@@ -113,3 +113,32 @@ def test_noalloc_takes_a_smaller_grid_when_the_default_one_does_not_fit():
     assert zl.workspace_size(p) > zl.NOALLOC_WORKSPACE_BYTES
     _noalloc_against_oracle(w, single_launch=False, max_seq_len=0)
     _noalloc_against_oracle(w, single_launch=True, max_seq_len=0)
+
+
+def test_noalloc_with_fused_append():
+    """The fused KV append through the no-workspace entry point: the same pools
+    and output, bit for bit, as the workspace entry point with the same rows."""
+    w = wl.random_case(925, B=6, Hq=32, Hkv=8, max_len=400, q_len=2)
+    k_new, v_new = wl.new_token_rows(925, w.B, 2, 8, 128, 128)
+    kn, vn = k_new.cuda(), v_new.cuda()
+    outs, pools = [], []
+    for noalloc in (False, True):
+        d = device_inputs(w)
+        out = torch.empty((w.B, w.q_len, w.Hq, w.D_v), dtype=torch.bfloat16, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        if noalloc:
+            p = zl.make_params(d["q"], d["k"], d["v"], d["bt"], d["sl"], out,
+                               page_size=w.page_size, scale=w.scale, Hkv=w.Hkv, D_v=w.D_v,
+                               err_flags=err, max_seq_len=w.max_seq_len, k_new=kn, v_new=vn)
+            zl.call_noalloc(p)
+        else:
+            zl.decode_attn(d["q"], d["k"], d["v"], d["bt"], d["sl"], page_size=w.page_size,
+                           scale=w.scale, out=out, err_flags=err, max_seq_len=w.max_seq_len,
+                           k_new=kn, v_new=vn)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        outs.append(out)
+        pools.append((d["k"], d["v"]))
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    for a, b in zip(pools[0], pools[1]):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
