@@ -206,11 +206,12 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
-def time_oracle(w, min_seconds=10.0, max_calls=50):
-    """The oracle as it stands, on all host cores: (seconds per call, calls, threads)."""
+def time_oracle(w, min_seconds=10.0, max_calls=50, threads=None):
+    """The oracle as it stands, on all host cores (or `threads` of them):
+    (seconds per call, calls, threads, the last call's result)."""
     import oracle
     orc = oracle.load()
-    threads = cpu_cores()
+    threads = cpu_cores() if threads is None else threads
     q, k = w.bits(w.q), w.bits(w.k_pool)
     v = None if w.mla else w.bits(w.v_pool)
     times = []
@@ -702,6 +703,11 @@ def run_ours(args, world, rank, local):
         cpu_s, cpu_calls, cores, res = time_oracle(w)
         cpu = {"value": kvb / cpu_s / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"the whole workload per call, {cpu_calls} calls (median)"}
+        # the same oracle on one core, for the scaling of the host baseline
+        one_s, one_calls, _, _ = time_oracle(w, min_seconds=3.0, max_calls=3, threads=1)
+        cpu["single_core"] = {"value": kvb / one_s / 1e9, "unit": UNIT, "cores": 1,
+                              "sample": f"the whole workload per call, {one_calls} calls "
+                                        "(median)"}
         if c.ap is None and not c.fused_append:  # (an append puts the new rows in the pools)
             parity = parity_summary(c.out, c.lse, res)
     line = {
