@@ -66,6 +66,30 @@ def test_any_split_matches(num_ctas):
     _parity(w, num_ctas=num_ctas)
 
 
+@pytest.mark.parametrize("trend", ["rising", "falling", "spike"])
+@pytest.mark.parametrize("num_ctas", [0, 1, 37])
+def test_softmax_base_moves_often(trend, num_ctas):
+    """Scores that climb by much more than 2^8 from tile to tile (the kernel's
+    softmax base moves on nearly every tile), that fall after a large first
+    tile (P far below 1 against a stale base), or that jump at one token late
+    in the context; whole and split, against the oracle."""
+    w = wl.random_case(1600 + num_ctas + len(trend), B=4, Hq=32, Hkv=8,
+                       lens=[700, 333, 1000, 17])
+    k = w.k_pool.float()
+    for b, L in enumerate(w.seq_lens):
+        for t in range(int(L)):
+            page, slot = w.block_table[b, t // w.page_size], t % w.page_size
+            if trend == "rising":
+                f = 1.0 + 40.0 * t / L
+            elif trend == "falling":
+                f = 41.0 - 40.0 * t / L
+            else:
+                f = 30.0 if t == int(L) * 3 // 4 else 1.0
+            k[page, slot] *= f
+    w.k_pool = k.to(torch.bfloat16)
+    _parity(w, num_ctas=num_ctas)
+
+
 def test_split_vs_unsplit_close():
     w = wl.random_case(401, B=4, Hq=32, Hkv=8, lens=[1000, 2000, 17, 513])
     d = device_inputs(w)

@@ -158,3 +158,28 @@ def test_mla_deepseek_mtp_shape_sampled():
     assert st == 0
     assert_close(g.out64()[bs], ref, "sampled out")
     assert_close(g.lse64()[bs], ref_lse, "sampled lse")
+
+
+@pytest.mark.parametrize("trend", ["rising", "falling", "spike"])
+@pytest.mark.parametrize("num_ctas", [0, 2, 40])
+def test_mla_softmax_max_moves_often(trend, num_ctas):
+    """The rope columns of the latent rows scaled so that the scores climb far
+    past 2^8 from tile to tile (the kernel's running max moves and O in TMEM is
+    rescaled), fall after a large first tile, or jump at one late token; whole
+    and split. (Only the rope: scaling the latent would scale V as well, and
+    the bf16 rounding of P would then exceed the absolute tolerance wherever
+    large V rows cancel.)"""
+    w = _mla_case(1650 + num_ctas + len(trend), [700, 1500, 65, 1024])
+    k = w.k_pool.float()
+    for b, L in enumerate(w.seq_lens):
+        for t in range(int(L)):
+            page, slot = w.block_table[b, t // w.page_size], t % w.page_size
+            if trend == "rising":
+                f = 1.0 + 40.0 * t / L
+            elif trend == "falling":
+                f = 41.0 - 40.0 * t / L
+            else:
+                f = 40.0 if t == int(L) * 3 // 4 else 1.0
+            k[page, slot, :, 512:] *= f
+    w.k_pool = k.to(torch.bfloat16)
+    _parity(w, num_ctas=num_ctas)
