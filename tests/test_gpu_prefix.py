@@ -47,6 +47,15 @@ def test_groups_and_query_tokens(Hq, Hkv, q_len):
     _parity(w, 6)
 
 
+@pytest.mark.parametrize("npref,B", [(20, 5), (64, 40), (129, 3)])
+def test_long_prefixes(npref, B):
+    """Long prefixes (20, 64 and 129 pages of 16 tokens) cut between several
+    CTAs, with 2 sequences per prefix group at g = 8 and a partly empty last
+    group for odd B."""
+    w = _case(1260 + npref + B, B=B, Hq=64, Hkv=8, npref=npref)
+    _parity(w, npref)
+
+
 def test_suffix_edges():
     """Sequences that end exactly at the prefix, one token past it, at tile and
     page edges, and long ones."""
