@@ -3,7 +3,7 @@
 //
 // Work decomposition. For sequence b the context is cut into n_b tiles of 16
 // tokens. The tiles of all (sequence, kv-head-group) units are laid end to end
-// and the line is cut into G equal ranges, one per CTA ("split-KV" of the
+// and the line is cut into min(G, tiles) equal ranges, one per CTA ("split-KV" of the
 // flash_decoding family named under "技术架构：五层模块化设计" on the
 // "ZhiLight：知乎开源的高性能 LLM 推理加速引擎" page). A CTA whose range covers a
 // whole unit writes the final output; a unit cut between CTAs leaves one
@@ -24,10 +24,11 @@
 // ("fused batch attention for decoding using tensor core instructions", the
 // "ZhiLight: Zhihu's CUDA Inference Engine..." page, "Dual streams, host
 // all-reduce and the memory model"), S = Q K^T and O += P V run on mma.sync,
-// and the online softmax (running max, rescaled sum) stays in registers with
-// quad shuffles. With q_len > 1 query tokens per sequence the rows are the
-// (token, head) pairs, g * q_len <= 16 of them, each with its causal limit
-// (the CAUSAL instances; q_len = 1 runs the instances without the limit).
+// and the online softmax (a lazily moved base, the sum) stays in registers
+// with quad shuffles. With q_len > 1 query tokens per sequence the rows are
+// the (token, head) pairs, at most 16 per row group (more rows go in several
+// groups), each with its causal limit (the CAUSAL instances; q_len = 1 runs
+// the instances without the limit).
 #pragma once
 
 #include "kernels.h"
